@@ -1,5 +1,19 @@
 """TQ1_0 ternary mat-vec for GB300 (sm_103a): Python binding of libtq1.
 
 Importing the package loads nothing; the CUDA library is loaded on first use
-of a binding function (see ``_lib``).
+of a binding function.  The functions carry the names of the C entry points
+declared in include/tq1.h.
 """
+_EXPORTS = (
+    "tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_partials", "tq1_mmv_id",
+    "tq1_mmv_id_workspace_size", "tq1_sync_status", "tq1_blocks_bytes", "tq1_q8_1_bytes", "Tq1Error",
+    "library", "library_path", "STATUS",
+)
+__all__ = list(_EXPORTS)
+
+
+def __getattr__(name):
+    if name in _EXPORTS:
+        from . import _lib
+        return getattr(_lib, name)
+    raise AttributeError(name)

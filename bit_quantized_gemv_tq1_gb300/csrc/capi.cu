@@ -1,0 +1,210 @@
+// capi.cu -- the extern "C" entry points of libtq1 (declared in include/tq1.h):
+// host-side argument checks, rung/route selection and launches.
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/tq1.h"
+#include "tq1_device.cuh"
+#include "tq1_internal.h"
+
+// Device status word of this library (see tq1_sync_status).  Kernels get its
+// address as an argument.
+static __device__ unsigned int g_tq1_status;
+
+namespace tq1 {
+
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxK = 62720;  // activation records of one column must fit the staging budget
+constexpr int64_t kPrefillMinT = 256;
+std::mutex g_mu;
+DeviceInfo g_info[kMaxDevices];
+unsigned* g_status_ptr[kMaxDevices];
+bool g_have[kMaxDevices];
+
+thread_local char g_last_err[256] = "";
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+int current_device() {
+  int d = 0;
+  if (!cuda_ok(cudaGetDevice(&d)) || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+bool ensure_device(int d) {
+  if (g_have[d]) return true;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_have[d]) return true;
+  DeviceInfo di{};
+  di.device = d;
+  int v = 0;
+  if (!cuda_ok(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d))) return false;
+  di.num_sms = v;
+  if (!cuda_ok(cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d))) return false;
+  di.max_smem_optin = static_cast<size_t>(v);
+  void* p = nullptr;
+  if (!cuda_ok(cudaGetSymbolAddress(&p, g_tq1_status))) return false;
+  g_info[d] = di;
+  g_status_ptr[d] = static_cast<unsigned*>(p);
+  g_have[d] = true;
+  return true;
+}
+
+unsigned* status_ptr() {
+  const int d = current_device();
+  if (d < 0 || !ensure_device(d)) return nullptr;
+  return g_status_ptr[d];
+}
+
+int check_mmv_shape(int64_t n, int64_t k, int64_t t) {
+  if (n < 0 || t < 0 || k <= 0 || (k % kQK) != 0) return TQ1_ERR_SHAPE;
+  return TQ1_OK;
+}
+}  // namespace
+
+bool cuda_ok(cudaError_t err) {
+  if (err == cudaSuccess) return true;
+  snprintf(g_last_err, sizeof(g_last_err), "%s: %s", cudaGetErrorName(err), cudaGetErrorString(err));
+  return false;
+}
+
+const DeviceInfo& device_info() {
+  static DeviceInfo dummy{};
+  const int d = current_device();
+  if (d < 0 || !ensure_device(d)) return dummy;
+  return g_info[d];
+}
+
+}  // namespace tq1
+
+using namespace tq1;
+
+extern "C" {
+
+const char* tq1_status_string(int status) {
+  switch (status) {
+    case TQ1_OK: return "ok";
+    case TQ1_ERR_NULL: return "null pointer argument";
+    case TQ1_ERR_SHAPE: return "invalid shape (k must be a positive multiple of 256; n, t, top_k >= 0)";
+    case TQ1_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case TQ1_ERR_UNSUPPORTED: return "shape beyond the kernels' limits";
+    case TQ1_ERR_WORKSPACE: return "workspace too small";
+    case TQ1_ERR_CUDA: return "CUDA runtime error";
+    case TQ1_ERR_TIMEOUT: return "a kernel timed out waiting for a transfer";
+    case TQ1_ERR_BAD_ID: return "routing id outside [0, n_experts)";
+    default: return "unknown status";
+  }
+}
+
+const char* tq1_version(void) { return "0.1.0"; }
+
+const char* tq1_last_cuda_error(void) { return g_last_err; }
+
+size_t tq1_blocks_bytes(int64_t n, int64_t k) {
+  if (n < 0 || k < 0) return 0;
+  return static_cast<size_t>(n) * static_cast<size_t>(k / kQK) * kBlockBytes;
+}
+
+size_t tq1_q8_1_bytes(int64_t t, int64_t k) {
+  if (t < 0 || k < 0) return 0;
+  return static_cast<size_t>(t) * static_cast<size_t>(k / kQK8) * kQ8Bytes;
+}
+
+int tq1_quantize_rows(const float* w, void* blocks, int64_t n, int64_t k, void* stream) {
+  if (n < 0 || k <= 0 || (k % kQK) != 0) return TQ1_ERR_SHAPE;
+  if (n == 0) return TQ1_OK;
+  if (!w || !blocks) return TQ1_ERR_NULL;
+  if (misaligned(w) || misaligned(blocks)) return TQ1_ERR_ALIGN;
+  if (!status_ptr()) return TQ1_ERR_CUDA;
+  return launch_quantize_rows(w, static_cast<uint8_t*>(blocks), n, k, static_cast<cudaStream_t>(stream));
+}
+
+int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* stream) {
+  if (t < 0 || k <= 0 || (k % kQK8) != 0) return TQ1_ERR_SHAPE;
+  if (t == 0) return TQ1_OK;
+  if (!x || !q8) return TQ1_ERR_NULL;
+  if (misaligned(x) || misaligned(q8)) return TQ1_ERR_ALIGN;
+  if (!status_ptr()) return TQ1_ERR_CUDA;
+  return launch_quantize_acts(x, static_cast<uint8_t*>(q8), t, k, static_cast<cudaStream_t>(stream));
+}
+
+static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* part, int64_t n, int64_t k,
+                      int64_t t, void* stream) {
+  int rc = check_mmv_shape(n, k, t);
+  if (rc != TQ1_OK) return rc;
+  if (n == 0 || t == 0) return TQ1_OK;
+  if (!blocks || !q8 || (!y && !part)) return TQ1_ERR_NULL;
+  if (misaligned(blocks) || misaligned(q8) || (y && misaligned(y)) || (part && misaligned(part)))
+    return TQ1_ERR_ALIGN;
+  if (k > kMaxK) return TQ1_ERR_UNSUPPORTED;
+  unsigned* st = status_ptr();
+  if (!st) return TQ1_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* w = static_cast<const uint8_t*>(blocks);
+  const uint8_t* a = static_cast<const uint8_t*>(q8);
+  const int64_t q8_row = (k / kQK8) * kQ8Bytes;
+  if (y && t >= kPrefillMinT) {
+    rc = launch_prefill(w, a, y, n, k, t, nullptr, 0, s, st);
+    if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise fall through to 32-column slices
+  }
+  for (int64_t c0 = 0; c0 < t; c0 += 32) {
+    const int64_t tc = t - c0 < 32 ? t - c0 : 32;
+    rc = launch_mmv(w, a + c0 * q8_row, y ? y + c0 * n : nullptr, part ? part + c0 * n * (k / kQK8) : nullptr, n,
+                    k, tc, s, st);
+    if (rc != TQ1_OK) return rc;
+  }
+  return TQ1_OK;
+}
+
+int tq1_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream) {
+  return mmv_common(blocks, q8, y, nullptr, n, k, t, stream);
+}
+
+int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,
+                     void* stream) {
+  if (!part && n > 0 && t > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;
+  return mmv_common(blocks, q8, nullptr, part, n, k, t, stream);
+}
+
+size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k) {
+  if (n_experts < 0 || t < 0 || top_k < 0) return 0;
+  const size_t words = moe_ws_words(n_experts, t * top_k);
+  return (words * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+}
+
+int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+               int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_mmv_shape(n, k, t);
+  if (rc != TQ1_OK) return rc;
+  if (n_experts <= 0 || top_k < 0) return TQ1_ERR_SHAPE;
+  if (n == 0 || t == 0 || top_k == 0) return TQ1_OK;
+  if (!expert_blocks || !q8 || !ids || !y || !ws) return TQ1_ERR_NULL;
+  if (misaligned(expert_blocks) || misaligned(q8) || misaligned(ids) || misaligned(y) || misaligned(ws))
+    return TQ1_ERR_ALIGN;
+  if (ws_bytes < tq1_mmv_id_workspace_size(n_experts, t, top_k)) return TQ1_ERR_WORKSPACE;
+  if (k > kMaxK || n_experts > 12288 || t * top_k > (int64_t{1} << 30)) return TQ1_ERR_UNSUPPORTED;
+  unsigned* st = status_ptr();
+  if (!st) return TQ1_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* table = static_cast<int32_t*>(ws);
+  rc = launch_moe_compact(ids, t, top_k, n_experts, table, s, st);
+  if (rc != TQ1_OK) return rc;
+  return launch_mmv_id(static_cast<const uint8_t*>(expert_blocks), n_experts, static_cast<const uint8_t*>(q8), y,
+                       n, k, t, top_k, table, s, st);
+}
+
+int tq1_sync_status(void* stream) {
+  unsigned* st = status_ptr();
+  if (!st) return TQ1_ERR_CUDA;
+  if (!cuda_ok(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)))) return TQ1_ERR_CUDA;
+  unsigned v = 0;
+  if (!cuda_ok(cudaMemcpy(&v, st, sizeof(v), cudaMemcpyDeviceToHost))) return TQ1_ERR_CUDA;
+  const unsigned zero = 0;
+  if (!cuda_ok(cudaMemcpy(st, &zero, sizeof(zero), cudaMemcpyHostToDevice))) return TQ1_ERR_CUDA;
+  if (v & kStatusTimeout) return TQ1_ERR_TIMEOUT;
+  if (v & kStatusBadId) return TQ1_ERR_BAD_ID;
+  return TQ1_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// tq1_internal.h -- host-side launchers shared between the library's
+// translation units.  Not part of the public C ABI (include/tq1.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tq1 {
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  size_t max_smem_optin;
+};
+
+// Cached per current device; first call per device queries the runtime.
+const DeviceInfo& device_info();
+
+// Record a failed CUDA runtime call for tq1_last_cuda_error(); returns
+// err == cudaSuccess.
+bool cuda_ok(cudaError_t err);
+
+// Kernel launchers.  All return a TQ1_* status code and never synchronise.
+int launch_quantize_rows(const float* w, uint8_t* blocks, int64_t n, int64_t k, cudaStream_t s);
+int launch_quantize_acts(const float* x, uint8_t* q8, int64_t t, int64_t k, cudaStream_t s);
+
+// y[c][r] (y != nullptr) or int32 partials part[c][r][k/32] (part != nullptr)
+// for columns c < t <= 32.
+int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int64_t n, int64_t k, int64_t t,
+               cudaStream_t s, unsigned* status);
+
+// Expert-routed mat-vec over a compacted routing table in `ws`.
+int launch_moe_compact(const int32_t* ids, int64_t t, int64_t top_k, int64_t n_experts, int32_t* ws,
+                       cudaStream_t s, unsigned* status);
+int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float* y, int64_t n, int64_t k,
+                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status);
+
+// Dense prefill (t >= 256) on the tensor cores.
+int launch_prefill(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, void* ws,
+                   size_t ws_bytes, cudaStream_t s, unsigned* status);
+
+// Workspace layout of the routing table (int32 words):
+//   [0]                 n_active
+//   [1, 1+E+1)          expert bounds (exclusive prefix sum of counts)
+//   [E+2, E+2+E)        active expert ids, ascending
+//   [2E+2, 2E+2+P)      pair indices (token*top_k + slot) sorted by expert,
+//                       stable within an expert
+inline size_t moe_ws_words(int64_t n_experts, int64_t pairs) { return 1 + (size_t)(n_experts + 1) + n_experts + pairs; }
+
+}  // namespace tq1

@@ -1,0 +1,152 @@
+/*
+ * tq1.h -- C ABI of libtq1: ternary TQ1_0 weights x Q8_1 activations on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Formats (PrismML-Eng/llama.cpp issue #139, "Current behavior": five trits
+ * per byte in base 3, chunk c of a 256-element block reading digit c of
+ * qs[0..31]; the block specification that accompanies it fixes the rest):
+ *
+ *   TQ1_0 block, 54 bytes, 256 weights:
+ *     bytes  0..47  qs[48]  five trits per byte
+ *     bytes 48..51  qh[4]   four trits per byte
+ *     bytes 52..53  d       fp16 scale, little-endian
+ *   byte b holding trits u0..u4 (u in {0,1,2}, u0 most significant) is
+ *   ceil((sum u_i 3^(4-i)) * 256 / 243); digit k of b is ((uint8)(b*3^k)*3)>>8;
+ *   trit 0/1/2 means weight -d/0/+d.  Element e of a block is
+ *     e <  160: qs[e % 32] digit e / 32
+ *     e <  240: qs[32 + (e - 160) % 16] digit (e - 160) / 16
+ *     e >= 240: qh[(e - 240) % 4] digit (e - 240) / 4
+ *   A matrix of n rows and k columns (k % 256 == 0) is [n][k/256] blocks,
+ *   rows contiguous.
+ *
+ *   Q8_1 block, 36 bytes, 32 activations: fp16 d @0, fp16 s @2, int8 q[32] @4.
+ *   A [t][k] activation matrix is [t][k/32] blocks.
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller and must be
+ *     16-byte aligned (TQ1_ERR_ALIGN otherwise).  The library allocates no
+ *     memory and never synchronises; work is enqueued on `stream` (a
+ *     cudaStream_t, NULL for the legacy default stream) on the current device.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failed check returns its negative code and launches nothing.
+ *   - Shapes: k must be a positive multiple of 256; n, t >= 0 (0 means there
+ *     is nothing to do and TQ1_OK is returned).
+ *   - Errors met while kernels run (a bulk-copy wait that timed out, a
+ *     routing id out of range) set a device status word; tq1_sync_status()
+ *     synchronises `stream` and returns and clears it.
+ *   - Kernels are launched with programmatic dependent launch: the mat-vec
+ *     kernels start streaming weight blocks before the previous kernel in the
+ *     stream has finished, so weight blocks must not be written by a kernel
+ *     that lets its dependents start early (tq1_quantize_rows does not).
+ */
+#ifndef TQ1_H_
+#define TQ1_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum tq1_status {
+  TQ1_OK = 0,
+  TQ1_ERR_NULL = -1,        /* a required pointer is NULL */
+  TQ1_ERR_SHAPE = -2,       /* k not a positive multiple of 256, or n/t/top_k negative */
+  TQ1_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+  TQ1_ERR_UNSUPPORTED = -4, /* shape beyond the kernels' limits (e.g. k > 62720) */
+  TQ1_ERR_WORKSPACE = -5,   /* workspace too small */
+  TQ1_ERR_CUDA = -6,        /* a CUDA runtime call failed */
+  TQ1_ERR_TIMEOUT = -7,     /* a kernel gave up waiting on a transfer (device status) */
+  TQ1_ERR_BAD_ID = -8       /* a routing id was outside [0, n_experts) (device status) */
+};
+
+/* Text for a status code (static storage). */
+const char* tq1_status_string(int status);
+
+/* Library version, e.g. "0.1.0". */
+const char* tq1_version(void);
+
+/* Name and text of the last CUDA runtime error this thread saw inside the
+ * library (empty if none); explains a TQ1_ERR_CUDA. */
+const char* tq1_last_cuda_error(void);
+
+/* Bytes of a TQ1_0 matrix [n][k/256] and of a Q8_1 matrix [t][k/32]. */
+size_t tq1_blocks_bytes(int64_t n, int64_t k);
+size_t tq1_q8_1_bytes(int64_t t, int64_t k);
+
+/*
+ * Quantise fp32 weights w[n][k] (row-major) to TQ1_0 blocks.
+ * Per 256-weight block: d = fp16(max |w|); trit = clamp(round_half_away(w / max|w|),
+ * -1, 1), or 0 when the block is all zero.  Bit-exact, deterministic.
+ * Format: PrismML-Eng/llama.cpp issue #139, "Current behavior"; rounding is
+ * this library's reading (the pages do not state one).
+ */
+int tq1_quantize_rows(const float* w, void* blocks, int64_t n, int64_t k, void* stream);
+
+/*
+ * Quantise fp32 activations x[t][k] to Q8_1 blocks q8[t][k/32].
+ * Per 32-value block: d = max|x| / 127 (fp32); q = clamp(round_half_away(x / d),
+ * -127, 127), or 0 when d == 0; stored fp16(d), fp16(d * sum q), q.
+ * k must be a positive multiple of 32 here.  Bit-exact, deterministic.
+ */
+int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* stream);
+
+/*
+ * Mat-vec for t token columns: y[c][r] = sum_k w[r][k] * x[c][k] with
+ * w = d_w * trit and x = d_a * q, accumulated as
+ *   sum_blocks d_w * sum_{chunks j} d_a[j] * I_j,   I_j = sum (trit * q) (exact int32)
+ * in fp32.  blocks [n][k/256] TQ1_0, q8 [t][k/32] Q8_1, y fp32 [t][n].
+ * t <= 32 runs the byte-major dp4a kernel laddered at 1/2/4/8/16/32 columns;
+ * 32 < t < 256 runs it on 32-column slices; t >= 256 runs the tensor-core
+ * prefill kernel.  Deterministic: repeated calls give identical bits.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Proposed approach" (a dedicated
+ * whole-block kernel that iterates over packed bytes); laddered column
+ * counts: Neroued/ninfer issue #293.
+ */
+int tq1_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream);
+
+/*
+ * Debug entry: the exact integer partials part[c][r][j] = I_j (int32,
+ * [t][n][k/32]) that tq1_mmv scales.  t <= 32.  Bit-exact by construction.
+ */
+int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,
+                     void* stream);
+
+/*
+ * Workspace bytes tq1_mmv_id needs for n_experts experts and t*top_k routed pairs.
+ */
+size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k);
+
+/*
+ * Expert-routed mat-vec (MoE "mul_mat_id"): y[c][s][r] = expert ids[c][s]'s
+ * matrix times token c's activations, for every token c < t and slot s < top_k.
+ *   expert_blocks: n_experts matrices [n][k/256] back to back (expert e starts
+ *                  at byte e * tq1_blocks_bytes(n, k))
+ *   q8:            [t][k/32] Q8_1, one row per token (shared by its slots)
+ *   ids:           int32 [t][top_k] expert ids
+ *   y:             fp32 [t][top_k][n]
+ *   ws, ws_bytes:  caller-owned device workspace of at least
+ *                  tq1_mmv_id_workspace_size() bytes (TQ1_ERR_WORKSPACE otherwise);
+ *                  it holds the compacted routing table between the two launches.
+ * Ids outside [0, n_experts) skip their slot (its output is left untouched) and
+ * set TQ1_ERR_BAD_ID in the device status.  n_experts <= 12288.
+ * Source: AMD-Ecosystem/llama.cpp PR #76, "Summary" (ids -> expert_bounds ->
+ * compacted grid); PrismML-Eng/llama.cpp issue #139, "Acceptance criteria"
+ * (MUL_MAT_ID with fewer experts used than available).
+ */
+int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+               int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word:
+ * TQ1_OK, TQ1_ERR_TIMEOUT or TQ1_ERR_BAD_ID (or TQ1_ERR_CUDA if the stream
+ * itself reported an error).
+ */
+int tq1_sync_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ1_H_ */

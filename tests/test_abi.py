@@ -1,0 +1,83 @@
+"""The C ABI: the library loads, exports every function include/tq1.h
+declares, and rejects bad arguments on the host without launching anything
+(these checks run before any CUDA call, so they need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_quantized_gemv_tq1_gb300 import _lib as L
+from bit_quantized_gemv_tq1_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tq1.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_id", "tq1_mmv_partials",
+                 "tq1_mmv_id_workspace_size", "tq1_sync_status", "tq1_status_string"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in L.STATUS:
+        assert lib.tq1_status_string(code)
+    assert lib.tq1_version() == b"0.1.0"
+
+
+def test_sizes(lib):
+    assert L.tq1_blocks_bytes(5120, 6144) == 5120 * 24 * 54
+    assert L.tq1_q8_1_bytes(3, 6144) == 3 * 192 * 36
+    assert L.tq1_mmv_id_workspace_size(128, 32, 8) >= 4 * (1 + 129 + 128 + 256)
+    assert L.tq1_mmv_id_workspace_size(128, 32, 8) % 256 == 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, FAKE, FAKE, 10, 300, 1), -2),   # k not a multiple of 256
+    ((FAKE, FAKE, FAKE, -1, 256, 1), -2),   # negative n
+    ((FAKE, FAKE, FAKE, 10, 0, 1), -2),     # k == 0
+    ((FAKE, FAKE, FAKE, 10, 256, -3), -2),  # negative t
+    ((None, FAKE, FAKE, 10, 256, 1), -1),   # null weights
+    ((FAKE, FAKE, None, 10, 256, 1), -1),   # null output
+    ((FAKE + 4, FAKE, FAKE, 10, 256, 1), -3),  # misaligned
+    ((FAKE, FAKE, FAKE, 10, 256 * 246, 1), -4),  # k beyond the staging limit
+    ((None, None, None, 0, 256, 1), 0),     # empty: nothing to do
+    ((None, None, None, 5, 256, 0), 0),
+])
+def test_mmv_host_checks(lib, args, code):
+    assert lib.tq1_mmv(*args, None) == code
+
+
+def test_other_host_checks(lib):
+    assert lib.tq1_quantize_rows(FAKE, FAKE, 4, 100, None) == -2
+    assert lib.tq1_quantize_rows(None, FAKE, 4, 256, None) == -1
+    assert lib.q8_1_quantize_acts(FAKE, FAKE, 1, 48, None) == -2
+    assert lib.q8_1_quantize_acts(FAKE + 8, FAKE, 1, 64, None) == -3
+    assert lib.tq1_mmv_partials(FAKE, FAKE, None, 4, 256, 1, None) == -1
+    ws = L.tq1_mmv_id_workspace_size(8, 2, 2)
+    assert lib.tq1_mmv_id(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 2, 2, FAKE, ws - 1, None) == -5
+    assert lib.tq1_mmv_id(FAKE, 0, FAKE, FAKE, FAKE, 16, 256, 2, 2, FAKE, ws, None) == -2
+    assert lib.tq1_mmv_id(FAKE, 8, FAKE, None, FAKE, 16, 256, 2, 2, FAKE, ws, None) == -1
+    assert lib.tq1_mmv_id(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 0, 2, FAKE, ws, None) == 0

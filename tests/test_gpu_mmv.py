@@ -1,0 +1,150 @@
+"""Mat-vec on the GPU vs the oracle: exact integer partials, fp32 outputs
+within max(1e-3 |ref|, 1e-4), layout probes, ladder consistency and
+determinism.  Full-size workloads are checked on sampled rows."""
+import numpy as np
+import pytest
+
+from oracle import oracle as orc
+from bit_quantized_gemv_tq1_gb300 import synth
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(p):
+    blocks = G.quantize_rows(p.w)
+    q8 = G.quantize_acts(p.x)
+    return blocks, q8
+
+
+def _oracle(p):
+    return orc.tq1_encode_rows(p.w), orc.q8_1_quantize(p.x)
+
+
+# Small shapes spanning several passes (256 units each), several CTAs and
+# ragged tails: all outputs compared.
+SMALL = [
+    (1, 256, 1), (3, 256, 2), (7, 512, 3), (33, 1024, 1), (256, 1024, 1), (100, 2048, 4),
+    (77, 6144, 5), (301, 768 * 4, 8), (64, 4096, 16), (130, 2048, 32), (45, 256 * 9, 31),
+    (17, 6144, 2), (1000, 512, 1), (5, 256 * 63, 1),
+]
+
+
+@pytest.mark.parametrize("n,k,t", SMALL)
+def test_partials_bit_exact_small(n, k, t):
+    p = synth.matvec(n, k, t, seed=n + k + t)
+    blocks, q8 = _run(p)
+    ob, oq = _oracle(p)
+    np.testing.assert_array_equal(G.partials(blocks, q8, n, k, t), orc.mmv_partials(ob, oq, n, k, t))
+
+
+@pytest.mark.parametrize("n,k,t", SMALL)
+def test_mmv_small(n, k, t):
+    p = synth.matvec(n, k, t, p_zero=0.4, seed=2 * n + k + t)
+    blocks, q8 = _run(p)
+    ob, oq = _oracle(p)
+    G.assert_close(G.mmv(blocks, q8, n, k, t), orc.mmv_f64(ob, oq, n, k, t))
+
+
+def test_config1_full():
+    p = synth.config_matvec("c1")
+    blocks, q8 = _run(p)
+    ob, oq = _oracle(p)
+    G.assert_close(G.mmv(blocks, q8, p.n, p.k, p.t), orc.mmv_f64(ob, oq, p.n, p.k, p.t))
+    np.testing.assert_array_equal(G.partials(blocks, q8, p.n, p.k, p.t), orc.mmv_partials(ob, oq, p.n, p.k, p.t))
+
+
+def test_config2_full():
+    p = synth.config_matvec("c2")
+    blocks, q8 = _run(p)
+    ob, oq = _oracle(p)
+    G.assert_close(G.mmv(blocks, q8, p.n, p.k, p.t), orc.mmv_f64(ob, oq, p.n, p.k, p.t))
+    np.testing.assert_array_equal(G.partials(blocks, q8, p.n, p.k, p.t), orc.mmv_partials(ob, oq, p.n, p.k, p.t))
+
+
+def test_config3_every_t_sampled_rows():
+    p = synth.config_matvec("c3")
+    blocks = G.quantize_rows(p.w)
+    rng = np.random.default_rng(33)
+    rows = np.unique(np.concatenate([[0, 1, p.n - 1], rng.integers(0, p.n, 125)]))
+    ob = orc.tq1_encode_rows(p.w[rows])  # the oracle encodes only the sampled rows
+    for t in range(1, 33):
+        x = p.x[:t]
+        q8 = G.quantize_acts(x)
+        y = G.mmv(blocks, q8, p.n, p.k, t)
+        ref = orc.mmv_f64(ob, orc.q8_1_quantize(x), rows.size, p.k, t)
+        G.assert_close(y[:, rows], ref)
+
+
+def test_config3_partials_t32_sampled_rows():
+    p = synth.config_matvec("c3")
+    blocks, q8 = _run(p)
+    rows = np.arange(0, p.n, 97)
+    part = G.partials(blocks, q8, p.n, p.k, 32)
+    ref = orc.mmv_partials(orc.tq1_encode_rows(p.w[rows]), orc.q8_1_quantize(p.x), rows.size, p.k, 32)
+    np.testing.assert_array_equal(part[:, rows], ref)
+
+
+def test_columns_beyond_32_use_slices():
+    p = synth.matvec(90, 1024, 75, seed=75)
+    blocks, q8 = _run(p)
+    ob, oq = _oracle(p)
+    G.assert_close(G.mmv(blocks, q8, p.n, p.k, p.t), orc.mmv_f64(ob, oq, p.n, p.k, p.t))
+    np.testing.assert_array_equal(G.partials(blocks, q8, p.n, p.k, p.t), orc.mmv_partials(ob, oq, p.n, p.k, p.t))
+
+
+def test_extreme_partials():
+    w = np.full((3, 512), np.float32(0.25))
+    w[1] = -0.25
+    w[2, ::2] = -0.25
+    x = np.full((2, 512), np.float32(5.0))
+    x[1, 100:] = -5.0
+    blocks, q8 = G.quantize_rows(w), G.quantize_acts(x)
+    part = G.partials(blocks, q8, 3, 512, 2)
+    np.testing.assert_array_equal(part, orc.mmv_partials(orc.tq1_encode_rows(w), orc.q8_1_quantize(x), 3, 512, 2))
+    assert part[0, 0, 0] == 4064 and part[0, 1, 0] == -4064
+
+
+def test_one_hot_layout_probes():
+    # Weight element e = +1 of row e, everything else 0; activation one-hot at
+    # e' in column e'.  y[e'][e] != 0 exactly when e == e'.  Covers all 256.
+    k = 256
+    w = np.eye(k, dtype=np.float32)
+    x = np.eye(k, dtype=np.float32)[:32]
+    blocks = G.quantize_rows(w)
+    for c0 in range(0, k, 32):
+        xs = np.eye(k, dtype=np.float32)[c0:c0 + 32]
+        y = G.mmv(blocks, G.quantize_acts(xs), k, k, 32)
+        nz = y != 0
+        expect = np.zeros_like(nz)
+        for c in range(32):
+            expect[c, c0 + c] = True
+        np.testing.assert_array_equal(nz, expect)
+    del x
+
+
+def test_multi_column_equals_single_columns():
+    # strata PR #1418 method: a multi-column call equals single-column calls.
+    p = synth.matvec(5120, 6144, 8, seed=8)
+    blocks, q8 = _run(p)
+    y = G.mmv(blocks, q8, p.n, p.k, 8)
+    part = G.partials(blocks, q8, p.n, p.k, 8)
+    for c in range(8):
+        q1 = G.quantize_acts(p.x[c:c + 1])
+        np.testing.assert_array_equal(G.partials(blocks, q1, p.n, p.k, 1)[0], part[c])
+        np.testing.assert_array_equal(G.mmv(blocks, q1, p.n, p.k, 1)[0], y[c])
+
+
+def test_deterministic_repeat():
+    p = synth.matvec(5120, 6144, 3, seed=9)
+    blocks, q8 = _run(p)
+    a = G.mmv(blocks, q8, p.n, p.k, 3)
+    b = G.mmv(blocks, q8, p.n, p.k, 3)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_empty_is_noop():
+    L = G.lib()
+    L.tq1_mmv(0, 0, 0, 0, 256, 1)
+    L.tq1_mmv(0, 0, 0, 7, 256, 0)
+    assert L.tq1_sync_status() == 0

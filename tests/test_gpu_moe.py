@@ -1,0 +1,125 @@
+"""Expert-routed mat-vec on the GPU vs the oracle."""
+import numpy as np
+import pytest
+
+from oracle import oracle as orc
+from bit_quantized_gemv_tq1_gb300 import synth
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _experts_gpu(m):
+    t = G.torch()
+    eb = m.n * (m.k // 256) * 54
+    blocks = t.empty(m.n_experts * eb, dtype=t.uint8, device="cuda")
+    for e in range(m.n_experts):
+        blocks[e * eb:(e + 1) * eb] = G.quantize_rows(m.expert_weights(e))
+    return blocks
+
+
+def _mmv_id(blocks, m, ids, q8, fill=float("nan")):
+    L = G.lib()
+    t = G.torch()
+    ws_bytes = L.tq1_mmv_id_workspace_size(m.n_experts, m.t, m.top_k)
+    ws = t.zeros(ws_bytes, dtype=t.uint8, device="cuda")
+    y = t.full((m.t, m.top_k, m.n), fill, dtype=t.float32, device="cuda")
+    L.tq1_mmv_id(blocks, m.n_experts, q8, G.dev(ids.astype(np.int32)), y, m.n, m.k, m.t, m.top_k, ws)
+    return y, L.tq1_sync_status()
+
+
+def _oracle_blocks(m, experts):
+    eb = m.n * (m.k // 256) * 54
+    out = np.zeros((m.n_experts, eb), np.uint8)
+    for e in experts:
+        out[e] = orc.tq1_encode_rows(m.expert_weights(e)).reshape(-1)
+    return out
+
+
+@pytest.mark.parametrize("t", [1, 32])
+def test_config4_sampled_rows(t):
+    m = synth.config_moe(t)
+    blocks = _experts_gpu(m)
+    q8 = G.quantize_acts(m.x)
+    y, st = _mmv_id(blocks, m, m.ids, q8)
+    assert st == 0
+    used = np.unique(m.ids)
+    ob = _oracle_blocks(m, used)
+    rows = np.unique(np.concatenate([[0, m.n - 1], np.random.default_rng(t).integers(0, m.n, 62)]))
+    ref = orc.mmv_id_f64_rows(ob, m.n_experts, orc.q8_1_quantize(m.x), m.ids, m.n, m.k, m.t, m.top_k, rows)
+    G.assert_close(G.host(y)[:, :, rows], ref)
+
+
+ROUTINGS = {
+    "repeated_and_unused": np.array([[0, 3], [3, 0], [3, 5], [0, 3], [5, 3]]),
+    "all_on_one": np.array([[2], [2], [2], [2], [2]]),
+    "top1": np.array([[1], [4], [1], [0], [6]]),
+    "every_expert": np.array([[0, 1, 2, 3, 4, 5, 6], [6, 5, 4, 3, 2, 1, 0], [1, 3, 5, 0, 2, 4, 6],
+                              [2, 2, 2, 2, 2, 2, 2], [0, 6, 0, 6, 0, 6, 0]]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROUTINGS))
+def test_small_routings_full(name):
+    ids = ROUTINGS[name].astype(np.int32)
+    t, top_k = ids.shape
+    m = synth.moe(7, 300, 1024, t, top_k, seed=41)
+    m.ids = ids
+    blocks = _experts_gpu(m)
+    q8 = G.quantize_acts(m.x)
+    y, st = _mmv_id(blocks, m, ids, q8)
+    assert st == 0
+    ob = _oracle_blocks(m, range(7))
+    ref = orc.mmv_id_f64(ob, 7, orc.q8_1_quantize(m.x), ids, m.n, m.k, t, top_k)
+    G.assert_close(G.host(y), ref)
+
+
+def test_many_tokens_one_expert_beyond_32_columns():
+    m = synth.moe(4, 96, 512, 40, 2, seed=3)
+    m.ids = np.stack([np.full(40, 1), np.arange(40) % 4], axis=1).astype(np.int32)
+    blocks = _experts_gpu(m)
+    y, st = _mmv_id(blocks, m, m.ids, G.quantize_acts(m.x))
+    assert st == 0
+    ref = orc.mmv_id_f64(_oracle_blocks(m, range(4)), 4, orc.q8_1_quantize(m.x), m.ids, m.n, m.k, m.t, m.top_k)
+    G.assert_close(G.host(y), ref)
+
+
+def test_equals_per_expert_mmv():
+    m = synth.moe(6, 256, 2048, 4, 3, seed=12)
+    blocks = _experts_gpu(m)
+    q8 = G.quantize_acts(m.x)
+    y, st = _mmv_id(blocks, m, m.ids, q8)
+    assert st == 0
+    y = G.host(y)
+    eb = m.n * 8 * 54
+    for c in range(m.t):
+        q1 = G.quantize_acts(m.x[c:c + 1])
+        for s in range(m.top_k):
+            e = int(m.ids[c, s])
+            ref = G.mmv(blocks[e * eb:(e + 1) * eb], q1, m.n, m.k, 1)[0]
+            np.testing.assert_array_equal(y[c, s], ref)
+
+
+def test_bad_id_sets_status_and_skips_slot():
+    m = synth.moe(5, 64, 512, 3, 2, seed=5)
+    ids = m.ids.copy()
+    ids[1, 0] = 9
+    ids[2, 1] = -1
+    blocks = _experts_gpu(m)
+    y, st = _mmv_id(blocks, m, ids, G.quantize_acts(m.x), fill=123.0)
+    assert st == -8
+    y = G.host(y)
+    assert np.all(y[1, 0] == 123.0) and np.all(y[2, 1] == 123.0)
+    ref = orc.mmv_id_f64(_oracle_blocks(m, range(5)), 5, orc.q8_1_quantize(m.x), ids, m.n, m.k, m.t, m.top_k)
+    ok = ~np.isnan(ref)
+    G.assert_close(y[ok], ref[ok])
+    assert G.lib().tq1_sync_status() == 0  # cleared
+
+
+def test_deterministic_repeat():
+    m = synth.config_moe(32)
+    blocks = _experts_gpu(m)
+    q8 = G.quantize_acts(m.x)
+    a, _ = _mmv_id(blocks, m, m.ids, q8)
+    b, _ = _mmv_id(blocks, m, m.ids, q8)
+    np.testing.assert_array_equal(G.host(a), G.host(b))
