@@ -1,0 +1,500 @@
+#!/usr/bin/env python3
+"""Benchmark of the TQ1_0 decode mat-vec on GB300.
+
+Workload (config 2 of the mat-vec workloads): N=5120 output rows, K=6144,
+T=1 token, TQ1_0 weights with P(0)=0.4, fp16 block scales U[0.005, 0.05],
+fp32 N(0,1) activations.  One step is the whole hot path over one batch:
+one Q8_1 quantisation launch over the batch's activations, then one tq1_mmv
+call per weight copy.  The batch uses R distinct weight copies whose total
+exceeds 4x the L2 size (so every call streams its weights from HBM; no L2
+flush is needed), captured once in a CUDA graph and replayed.
+
+Reported (one JSON line on rank 0):
+  value         effective GB/s = R * (W + A + Y) bytes / step time, W = packed
+                weights, A = Q8_1 activations, Y = fp32 outputs of one call
+  roofline      the mat-vec kernel alone (graph of R calls): algorithmic bytes
+                per call / average call duration, against the measured HBM peak
+  t_sweep       us per call for T = 1..32 (config 3 distribution), interleaved
+                one T per pass to spread clock drift
+  e2e           the same metric with host buffers: pinned-host activations in,
+                outputs back to pinned host memory, every step
+  cpu_baseline  the plain fp64 CPU oracle on the same workload (bounded sample)
+
+--impl reference times that oracle as the reference arm.
+With torchrun (N > 1), every rank runs its own replica (independent
+problems, weak scaling); times are the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TQ1_0 mat-vec effective HBM GB/s (% of GB300 peak) at T=1; µs/call vs T=1..32"
+QK, BLOCK_BYTES, QK8, Q8_BYTES = 256, 54, 32, 36
+N2, K2 = 5120, 6144
+
+
+def alg_bytes(n: int, k: int, t: int) -> int:
+    """Algorithmic bytes of one call: packed weights once, Q8_1 activations, fp32 outputs."""
+    return n * (k // QK) * BLOCK_BYTES + t * (k // QK8) * Q8_BYTES + 4 * t * n
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "_source": "fallback"}
+
+
+# ------------------------------------------------------------ distributed --
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max over ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks --
+CLOCK_FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) while the timed region runs."""
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and parts[1] != self.uuid and not self.uuid.endswith(parts[1]) and not parts[1].endswith(self.uuid):
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        pw = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------- CPU oracle --
+def cpu_oracle_baseline(budget_s: float = 12.0, min_calls: int = 1, max_calls: int = 10 ** 6) -> dict:
+    """The plain fp64 oracle (as it stands) on config 2, on the host cores:
+    Q8_1 quantisation + mat-vec per call, repeated for about `budget_s`."""
+    from bit_quantized_gemv_tq1_gb300 import synth
+    from oracle import oracle as orc
+
+    p = synth.config_matvec("c2")
+    blocks = orc.tq1_encode_rows(p.w)            # weights are set-up, not timed
+    orc.mmv_f64(blocks, orc.q8_1_quantize(p.x), p.n, p.k, 1)   # warm caches / threads
+    calls, t0 = 0, time.perf_counter()
+    while calls < min_calls or (time.perf_counter() - t0 < budget_s and calls < max_calls):
+        q8 = orc.q8_1_quantize(p.x)
+        orc.mmv_f64(blocks, q8, p.n, p.k, 1)
+        calls += 1
+    dt = time.perf_counter() - t0
+    return {"calls": calls, "seconds": dt, "value": calls * alg_bytes(p.n, p.k, 1) / dt / 1e9,
+            "cores": orc.num_threads()}
+
+
+# ------------------------------------------------------------------ ours ---
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from bit_quantized_gemv_tq1_gb300 import _lib as L
+    from bit_quantized_gemv_tq1_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    lib = L.library()
+    n, k = N2, K2
+    wbytes = n * (k // QK) * BLOCK_BYTES
+    qbytes = (k // QK8) * Q8_BYTES
+    R = args.layers or max(64, math.ceil(4 * l2 / wbytes))
+    c2 = synth.CONFIGS["c2"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 * c2["seed"] + rank)
+
+    blocks = torch.empty(R * wbytes, dtype=torch.uint8, device=dev)
+    for l in range(R):
+        w = synth.device_weights(n, k, c2["p_zero"], c2["d_lo"], c2["d_hi"], gen, dev)
+        L.tq1_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+        del w
+    x = synth.device_activations((R, k), gen, dev)
+    q8 = torch.empty(R * qbytes, dtype=torch.uint8, device=dev)
+    y = torch.empty((R, n), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    bp, qp, yp, xp = blocks.data_ptr(), q8.data_ptr(), y.data_ptr(), x.data_ptr()
+
+    def step_calls(s, with_quant=True):
+        if with_quant:
+            assert lib.q8_1_quantize_acts(xp, qp, R, k, s) == 0
+        for l in range(R):
+            assert lib.tq1_mmv(bp + l * wbytes, qp + l * qbytes, yp + l * n * 4, n, k, 1, s) == 0
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn(stream.cuda_stream)          # eager warm-up (module load, attributes)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=stream):
+                fn(stream.cuda_stream)
+        torch.cuda.synchronize(dev)
+        return g
+
+    g_step = capture(lambda s: step_calls(s, True))
+    g_kern = capture(lambda s: step_calls(s, False))
+    assert lib.tq1_sync_status(stream.cuda_stream) == 0
+
+    def timed(graph, reps, warm):
+        for _ in range(warm):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        return e0.elapsed_time(e1)  # ms
+
+    uuid = None
+    try:
+        uuid = str(props.uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        step_ms_total = timed(g_step, args.steps, args.warmup)
+        kern_ms_total = timed(g_kern, args.steps, args.warmup)
+    clocks = clk.summary()
+    step_ms = reduce_max(step_ms_total, dev) / args.steps
+    kern_ms = reduce_max(kern_ms_total, dev) / args.steps
+    per_call_bytes = alg_bytes(n, k, 1)
+    value = ws * R * per_call_bytes / (step_ms * 1e-3) / 1e9
+    kern_us = kern_ms * 1e3 / R
+    achieved = per_call_bytes / (kern_us * 1e-6) / 1e9
+    peaks = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+
+    # ---- end to end: pinned host activations in, outputs out, every step
+    xh = torch.empty((R, k), dtype=torch.float32).pin_memory()
+    xh.copy_(x.cpu())
+    yh = torch.empty((R, n), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x.copy_(xh, non_blocking=True)
+            g_step.replay()
+            yh.copy_(y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    stream.synchronize()
+    e2e_s = reduce_max(time.perf_counter() - t0, dev) / args.steps
+    e2e = {"value": ws * R * per_call_bytes / e2e_s / 1e9, "unit": "GB/s", "ms_per_step": e2e_s * 1e3,
+           "h2d_bytes_per_step": R * k * 4, "d2h_bytes_per_step": R * n * 4,
+           "path": "pinned host fp32 activations -> device, captured library calls, fp32 outputs -> pinned host"}
+    assert lib.tq1_sync_status(stream.cuda_stream) == 0
+
+    # ---- T sweep (config 3 distribution), interleaved over T per pass
+    sweep = None
+    if not args.no_sweep:
+        c3 = synth.CONFIGS["c3"]
+        gen3 = torch.Generator(device=dev)
+        gen3.manual_seed(1000 * c3["seed"] + rank)
+        del g_step, g_kern
+        for l in range(R):
+            w = synth.device_weights(n, k, c3["p_zero"], c3["d_lo"], c3["d_hi"], gen3, dev)
+            L.tq1_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+            del w
+        tmax = 32
+        x3 = synth.device_activations((R * tmax, k), gen3, dev)
+        q83 = torch.empty(R * tmax * qbytes, dtype=torch.uint8, device=dev)
+        y3 = torch.empty((R * tmax, n), dtype=torch.float32, device=dev)
+        L.q8_1_quantize_acts(x3, q83, R * tmax, k)
+        q3p, y3p = q83.data_ptr(), y3.data_ptr()
+
+        def sweep_calls(s, t):
+            for l in range(R):
+                assert lib.tq1_mmv(bp + l * wbytes, q3p + l * tmax * qbytes, y3p + l * tmax * n * 4, n, k, t, s) == 0
+
+        graphs = {t: capture(lambda s, t=t: sweep_calls(s, t)) for t in range(1, tmax + 1)}
+        times = {t: [] for t in graphs}
+        for _ in range(2):
+            for g in graphs.values():
+                g.replay()
+        torch.cuda.synchronize(dev)
+        for _ in range(args.sweep_passes):
+            for t, g in graphs.items():
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                with torch.cuda.stream(stream):
+                    g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                times[t].append(e0.elapsed_time(e1) * 1e3 / R)
+        assert lib.tq1_sync_status(stream.cuda_stream) == 0
+        sweep = {str(t): round(reduce_max(statistics.median(v), dev), 3) for t, v in times.items()}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        c = cpu_oracle_baseline(args.cpu_seconds)
+        cpu = {"value": round(c["value"], 4), "unit": "GB/s", "cores": c["cores"], "kind": "oracle",
+               "sample": f"{c['calls']} calls of the config-2 mat-vec (N=5120, K=6144, T=1), each = oracle Q8_1 "
+                         f"quantise + fp64 mat-vec, {c['seconds']:.1f} s on {c['cores']} host threads"}
+
+    launches = args.steps * (1 + R)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+        "config": {"workload": "c2: TQ1_0 decode mat-vec N=5120 K=6144 T=1 (P(0)=0.4, d~U[0.005,0.05])",
+                   "calls_per_step": R, "quant_launches_per_step": 1,
+                   "l2": f"inputs larger than L2: {R} distinct weight copies, {R * wbytes / 2**20:.0f} MiB vs "
+                         f"L2 {l2 / 2**20:.0f} MiB", "timing": "CUDA graph replay, CUDA events on the launch stream",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "us_per_call": round(step_ms * 1e3 / R, 3),
+        "pct_of_peak": round(100 * value / ws / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "kernel": "mmv_kernel<1,0> (tq1_mmv, T=1)", "us_per_launch": round(kern_us, 3),
+                     "bytes_per_launch": per_call_bytes, "peak_source": f"{peaks['_source']} hbm_gbs"},
+        "e2e": {kk: (round(v, 3) if isinstance(v, float) else v) for kk, v in e2e.items()},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if sweep:
+        out["t_sweep_us_per_call"] = sweep
+    if cpu:
+        out["cpu_baseline"] = cpu
+    return out
+
+
+# ------------------------------------------------------------- reference --
+def run_reference(args, ws, rank):
+    """The reference arm: the plain CPU oracle as it stands, on config 2."""
+    if rank != 0:
+        return None
+    from bit_quantized_gemv_tq1_gb300 import synth
+    from oracle import oracle as orc
+
+    orc.build()
+    p = synth.config_matvec("c2")
+    blocks = orc.tq1_encode_rows(p.w)
+    for _ in range(args.warmup):
+        orc.mmv_f64(blocks, orc.q8_1_quantize(p.x), p.n, p.k, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.mmv_f64(blocks, orc.q8_1_quantize(p.x), p.n, p.k, 1)
+    dt = time.perf_counter() - t0
+    value = args.steps * alg_bytes(p.n, p.k, 1) / dt / 1e9
+    cores = orc.num_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "c2: TQ1_0 decode mat-vec N=5120 K=6144 T=1 (P(0)=0.4, d~U[0.005,0.05])",
+                   "calls_per_step": 1, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} calls of the config-2 mat-vec, each = oracle Q8_1 quantise + "
+                                   f"fp64 mat-vec"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def run_profile_case(args, local):
+    """A fixed, small, eager workload for Nsight Compute captures: set-up, then
+    `--profile-calls` mat-vec calls over distinct weight copies (larger than L2
+    in total), no timing.  Cases: c2 (T=1), c3t<T> (config 3 at T columns),
+    c4t<T> (MoE), c5 (prefill)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from bit_quantized_gemv_tq1_gb300 import _lib as L
+    from bit_quantized_gemv_tq1_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = L.library()
+    case = args.profile
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    if case.startswith("c2") or case.startswith("c3") or case.startswith("c5"):
+        name = case[:2]
+        c = synth.CONFIGS[name]
+        n, k = c["n"], c["k"]
+        t = int(case[3:]) if len(case) > 3 else c["t"]
+        wbytes = n * (k // QK) * BLOCK_BYTES
+        copies = max(1, min(args.layers or 40, (2 * 2 ** 30) // wbytes))
+        blocks = torch.empty(copies * wbytes, dtype=torch.uint8, device=dev)
+        for l in range(copies):
+            w = synth.device_weights(n, k, c["p_zero"], c["d_lo"], c["d_hi"], gen, dev)
+            L.tq1_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+            del w
+        x = synth.device_activations((t, k), gen, dev)
+        q8 = torch.empty(t * (k // QK8) * Q8_BYTES, dtype=torch.uint8, device=dev)
+        y = torch.empty((t, n), dtype=torch.float32, device=dev)
+        L.q8_1_quantize_acts(x, q8, t, k)
+        for i in range(args.profile_calls):
+            l = i % copies
+            assert lib.tq1_mmv(blocks.data_ptr() + l * wbytes, q8.data_ptr(), y.data_ptr(), n, k, t, s) == 0
+    elif case.startswith("c4"):
+        t = int(case[3:]) if len(case) > 3 else 1
+        m = synth.config_moe(t)
+        eb = m.n * (m.k // QK) * BLOCK_BYTES
+        blocks = torch.empty(m.n_experts * eb, dtype=torch.uint8, device=dev)
+        for e in range(m.n_experts):
+            w = synth.device_weights(m.n, m.k, m.p_zero, m.d_lo, m.d_hi, gen, dev)
+            L.tq1_quantize_rows(w, blocks[e * eb:(e + 1) * eb], m.n, m.k)
+        q8 = torch.empty(t * (m.k // QK8) * Q8_BYTES, dtype=torch.uint8, device=dev)
+        L.q8_1_quantize_acts(torch.from_numpy(m.x).to(dev), q8, t, m.k)
+        ids = torch.from_numpy(m.ids).to(dev)
+        y = torch.empty((t, m.top_k, m.n), dtype=torch.float32, device=dev)
+        ws_bytes = L.tq1_mmv_id_workspace_size(m.n_experts, t, m.top_k)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        for _ in range(args.profile_calls):
+            assert lib.tq1_mmv_id(blocks.data_ptr(), m.n_experts, q8.data_ptr(), ids.data_ptr(), y.data_ptr(), m.n,
+                                  m.k, t, m.top_k, ws.data_ptr(), ws_bytes, s) == 0
+    else:
+        raise SystemExit(f"unknown profile case {case}")
+    assert lib.tq1_sync_status(s) == 0
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_case": case, "calls": args.profile_calls}), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=0, help="weight copies per step (default: > 4x L2)")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-passes", type=int, default=15)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per mat-vec launch from an ncu capture of the current kernel")
+    ap.add_argument("--profile", default=None,
+                    help="run a fixed eager workload for ncu instead of timing (c2, c3t<T>, c4t<T>, c5)")
+    ap.add_argument("--profile-calls", type=int, default=12)
+    args = ap.parse_args(argv)
+    if args.profile:
+        return run_profile_case(args, dist_env()[2])
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, ws, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out = run_ours(args, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

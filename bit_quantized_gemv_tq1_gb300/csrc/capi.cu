@@ -148,6 +148,10 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
     rc = launch_prefill(w, a, y, n, k, t, nullptr, 0, s, st);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise fall through to 32-column slices
   }
+  if (y && t <= 4) {
+    rc = launch_mmv_small(w, a, y, n, k, t, s, st);
+    if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
+  }
   for (int64_t c0 = 0; c0 < t; c0 += 32) {
     const int64_t tc = t - c0 < 32 ? t - c0 : 32;
     rc = launch_mmv(w, a + c0 * q8_row, y ? y + c0 * n : nullptr, part ? part + c0 * n * (k / kQK8) : nullptr, n,

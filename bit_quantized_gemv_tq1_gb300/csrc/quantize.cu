@@ -82,11 +82,14 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) quantize_rows_kernel(const 
   __threadfence();
 }
 
-// One warp per Q8_1 block of 32 activations.
+// One warp per Q8_1 block of 32 activations.  This kernel does not signal
+// its dependents early: its grid spans several waves, and a dependent grid
+// admitted while those waves are still being placed ends up unevenly spread
+// over the SMs (measured: a following chain of one-CTA-per-SM mat-vec
+// launches ran ~50% slower).  Dependents start as its CTAs retire.
 __global__ void __launch_bounds__(kWarpsPerCta * 32) quantize_acts_kernel(const float* __restrict__ x,
                                                                           uint8_t* __restrict__ out,
                                                                           int64_t nblocks) {
-  pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t blk = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);

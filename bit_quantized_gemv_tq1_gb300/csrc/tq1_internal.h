@@ -30,6 +30,11 @@ int launch_quantize_acts(const float* x, uint8_t* q8, int64_t t, int64_t k, cuda
 int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int64_t n, int64_t k, int64_t t,
                cudaStream_t s, unsigned* status);
 
+// Decode-path kernel for 1 <= t <= 4 columns.  Returns TQ1_ERR_UNSUPPORTED
+// without launching when the shape does not fit its staging.
+int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
+                     unsigned* status);
+
 // Expert-routed mat-vec over a compacted routing table in `ws`.
 int launch_moe_compact(const int32_t* ids, int64_t t, int64_t top_k, int64_t n_experts, int32_t* ws,
                        cudaStream_t s, unsigned* status);

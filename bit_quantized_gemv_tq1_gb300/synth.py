@@ -154,3 +154,25 @@ def config_moe(t: int) -> Moe:
     c = CONFIGS["c4"]
     return moe(c["n_experts"], c["n"], c["k"], t, c["top_k"], c["zipf_s"], c["p_zero"], c["d_lo"], c["d_hi"],
                c["seed"])
+
+
+def device_weights(n: int, k: int, p_zero: float, d_lo: float, d_hi: float, generator, device="cuda"):
+    """The same weight recipe drawn on the device with a seeded torch generator
+    (for workloads too large to draw on the host, e.g. many distinct weight
+    copies).  Returns fp32 [n][k] = fp16(d) * t."""
+    import torch
+
+    u = torch.rand((n, k), generator=generator, device=device)
+    half = (1.0 - p_zero) / 2.0
+    t = torch.zeros((n, k), dtype=torch.float32, device=device)
+    t[u < half] = -1.0
+    t[(u >= half) & (u < 2 * half)] = 1.0
+    d = torch.empty((n, k // QK, 1), dtype=torch.float32, device=device).uniform_(d_lo, d_hi, generator=generator)
+    d = d.half().float()
+    return (t.view(n, k // QK, QK) * d).view(n, k)
+
+
+def device_activations(shape, generator, device="cuda"):
+    import torch
+
+    return torch.randn(shape, generator=generator, device=device, dtype=torch.float32)

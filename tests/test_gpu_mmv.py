@@ -123,16 +123,24 @@ def test_one_hot_layout_probes():
     del x
 
 
-def test_multi_column_equals_single_columns():
+@pytest.mark.parametrize("t", [2, 3, 4, 8, 32])
+def test_multi_column_equals_single_columns(t):
     # strata PR #1418 method: a multi-column call equals single-column calls.
-    p = synth.matvec(5120, 6144, 8, seed=8)
+    # Integer partials always bit-exact; fp32 outputs bitwise equal where the
+    # same kernel runs (1..4 columns share one accumulation order), else
+    # within the float tolerance.
+    p = synth.matvec(5120, 6144, t, seed=8)
     blocks, q8 = _run(p)
-    y = G.mmv(blocks, q8, p.n, p.k, 8)
-    part = G.partials(blocks, q8, p.n, p.k, 8)
-    for c in range(8):
+    y = G.mmv(blocks, q8, p.n, p.k, t)
+    part = G.partials(blocks, q8, p.n, p.k, t)
+    for c in range(t):
         q1 = G.quantize_acts(p.x[c:c + 1])
         np.testing.assert_array_equal(G.partials(blocks, q1, p.n, p.k, 1)[0], part[c])
-        np.testing.assert_array_equal(G.mmv(blocks, q1, p.n, p.k, 1)[0], y[c])
+        y1 = G.mmv(blocks, q1, p.n, p.k, 1)[0]
+        if t <= 4:
+            np.testing.assert_array_equal(y1, y[c])
+        else:
+            G.assert_close(y[c], y1)
 
 
 def test_deterministic_repeat():
