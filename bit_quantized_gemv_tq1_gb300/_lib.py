@@ -66,9 +66,10 @@ def library() -> ctypes.CDLL:
         lib.tq1_mmv_id_workspace_size.restype = SZ
         lib.tq1_mmv_id_workspace_size.argtypes = [I64, I64, I64]
         lib.tq1_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
+        lib.tq1_mmv_id_noalloc.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P]
         lib.tq1_sync_status.argtypes = [P]
         for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_partials", "tq1_mmv_id",
-                     "tq1_sync_status"):
+                     "tq1_mmv_id_noalloc", "tq1_sync_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -136,6 +137,16 @@ def tq1_mmv_id(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, t: int
         ws_bytes = ws.numel() * ws.element_size()
     _check(library().tq1_mmv_id(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(y), n, k, t, top_k,
                                 _addr(ws), ws_bytes, _stream(stream)), "tq1_mmv_id")
+
+
+def tq1_mmv_id_noalloc(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, t: int, top_k: int,
+                       stream=None) -> None:
+    """tq1_mmv_id for callers that cannot allocate a workspace: the routing
+    table lives in a fixed array inside the library (limits: 1024 experts,
+    16384 routed token/slot pairs).  Make the first call on a device before
+    any stream capture; calls that may overlap on the GPU race on the array."""
+    _check(library().tq1_mmv_id_noalloc(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(y), n, k, t,
+                                        top_k, _stream(stream)), "tq1_mmv_id_noalloc")
 
 
 def tq1_sync_status(stream=None) -> int:

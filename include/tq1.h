@@ -139,6 +139,24 @@ int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, con
                int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * tq1_mmv_id without a workspace argument, for callers that cannot allocate
+ * device memory (inside a stream capture, under a fixed memory budget, in a
+ * latency-critical loop, or from plain C with no allocator at hand).  The
+ * routing table lives in a fixed array that is part of the library image
+ * (about 72 KiB on every GPU that loads the library, held until exit).
+ * Limits: n_experts <= 1024 and t * top_k <= 16384; larger calls return
+ * TQ1_ERR_WORKSPACE and launch nothing.  Same arguments, layouts, results
+ * and errors as tq1_mmv_id otherwise.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture begins.
+ * All calls on a device share the array (each call rewrites what it reads,
+ * so nothing needs clearing); calls that may overlap on the GPU race on it.
+ * The pages have no counterpart to this entry point.
+ */
+int tq1_mmv_id_noalloc(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+                       int64_t n, int64_t k, int64_t t, int64_t top_k, void* stream);
+
+/*
  * Synchronise `stream`, then return and clear the device status word:
  * TQ1_OK, TQ1_ERR_TIMEOUT or TQ1_ERR_BAD_ID (or TQ1_ERR_CUDA if the stream
  * itself reported an error).

@@ -1,0 +1,65 @@
+"""tq1_mmv_id_noalloc: the expert-routed mat-vec for callers that cannot
+allocate device memory (stream-capture regions, fixed memory budgets,
+latency-critical loops, plain C callers without an allocator).  Its routing
+table lives in a fixed array inside the library instead of a caller
+workspace.
+
+Checked through the C ABI against tq1_mmv_id (which takes a workspace) on two
+calls in a row with different routings, so a table left over from the first
+call cannot leak into the second.  This file is collected last on purpose."""
+import numpy as np
+import pytest
+
+from bit_quantized_gemv_tq1_gb300 import synth
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _experts_gpu(m):
+    t = G.torch()
+    eb = m.n * (m.k // 256) * 54
+    blocks = t.empty(m.n_experts * eb, dtype=t.uint8, device="cuda")
+    for e in range(m.n_experts):
+        blocks[e * eb:(e + 1) * eb] = G.quantize_rows(m.expert_weights(e))
+    return blocks
+
+
+def _with_workspace(L, blocks, m, q8, ids):
+    t = G.torch()
+    ws_bytes = L.tq1_mmv_id_workspace_size(m.n_experts, m.t, m.top_k)
+    ws = t.zeros(ws_bytes, dtype=t.uint8, device="cuda")
+    y = t.full((m.t, m.top_k, m.n), float("nan"), dtype=t.float32, device="cuda")
+    L.tq1_mmv_id(blocks, m.n_experts, q8, ids, y, m.n, m.k, m.t, m.top_k, ws)
+    assert L.tq1_sync_status() == 0
+    return G.host(y)
+
+
+def _no_alloc(L, blocks, m, q8, ids):
+    t = G.torch()
+    y = t.full((m.t, m.top_k, m.n), float("nan"), dtype=t.float32, device="cuda")
+    L.tq1_mmv_id_noalloc(blocks, m.n_experts, q8, ids, y, m.n, m.k, m.t, m.top_k)
+    assert L.tq1_sync_status() == 0
+    return G.host(y)
+
+
+def test_no_alloc_matches_workspace_entry_on_two_calls():
+    L = G.lib()
+    m = synth.moe(n_experts=24, n=320, k=1024, t=6, top_k=4, seed=31)
+    blocks = _experts_gpu(m)
+    q8 = G.quantize_acts(m.x)
+    routings = [m.ids.astype(np.int32),
+                np.roll(m.ids, 1, axis=0).astype(np.int32)[:, ::-1].copy()]
+    routings[1][0] = [5, 5 + 1, 23, 0]  # a different expert set for the second call
+    for ids_np in routings:
+        ids = G.dev(ids_np)
+        ref = _with_workspace(L, blocks, m, q8, ids)
+        got = _no_alloc(L, blocks, m, q8, ids)
+        G.assert_close(got, ref)
+
+
+def test_no_alloc_rejects_calls_beyond_its_table():
+    lib = G.lib().library()
+    fake = 1 << 20
+    assert lib.tq1_mmv_id_noalloc(fake, 1025, fake, fake, fake, 16, 256, 1, 1, None) == -5
+    assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 4097, 4, None) == -5
