@@ -50,6 +50,29 @@ def alg_bytes(n: int, k: int, t: int) -> int:
     return n * (k // QK) * BLOCK_BYTES + t * (k // QK8) * Q8_BYTES + 4 * t * n
 
 
+# DRAM bytes (read + write) per launch of the T=1 decode kernel, from one ncu
+# capture of the bench's own workload, valid only for the kernel sources with
+# this digest; any later change to them makes the figure stale and it is
+# reported as null until it is captured again.
+DECODE_SOURCES = ("bit_quantized_gemv_tq1_gb300/csrc/mmv_small.cu", "bit_quantized_gemv_tq1_gb300/csrc/tq1_device.cuh")
+DECODE_TRAFFIC = {"sha256": "879beebdbf0ac74c0fb2fbaf969917d104b70c9b3de491fdfb0aed5f1edd5f8d", "bytes": 6702080}
+
+
+def decode_sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(hashlib.sha256(f.read()).digest())
+    return h.hexdigest()
+
+
+def decode_traffic(override):
+    if override is not None:
+        return override
+    return DECODE_TRAFFIC["bytes"] if decode_sources_digest() == DECODE_TRAFFIC["sha256"] else None
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -323,6 +346,11 @@ def run_ours(args, ws, rank, local):
         assert lib.tq1_sync_status(stream.cuda_stream) == 0
         sweep = {str(t): round(reduce_max(statistics.median(v), dev), 3) for t, v in times.items()}
 
+    extra = {}
+    if not args.no_extra:
+        extra["prefill_c5"] = prefill_bench(lib, L, synth, dev, stream, capture, args)
+        extra["moe_c4"] = moe_bench(lib, L, synth, dev, stream, capture, args)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         c = cpu_oracle_baseline(args.cpu_seconds)
@@ -343,8 +371,8 @@ def run_ours(args, ws, rank, local):
         "us_per_call": round(step_ms * 1e3 / R, 3),
         "pct_of_peak": round(100 * value / ws / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
-                     "kernel": "mmv_kernel<1,0> (tq1_mmv, T=1)", "us_per_launch": round(kern_us, 3),
+                     "frac": round(achieved / peak, 4), "traffic": decode_traffic(args.traffic),
+                     "kernel": "mmv_small_kernel<1> (tq1_mmv, T=1)", "us_per_launch": round(kern_us, 3),
                      "bytes_per_launch": per_call_bytes, "peak_source": f"{peaks['_source']} hbm_gbs"},
         "e2e": {kk: (round(v, 3) if isinstance(v, float) else v) for kk, v in e2e.items()},
         "gpu_launches": launches,
@@ -352,8 +380,110 @@ def run_ours(args, ws, rank, local):
     }
     if sweep:
         out["t_sweep_us_per_call"] = sweep
+    out.update(extra)
     if cpu:
         out["cpu_baseline"] = cpu
+    return out
+
+
+def _time_graph(g, stream, reps):
+    import torch
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps  # ms
+
+
+def prefill_bench(lib, L, synth, dev, stream, capture, args) -> dict:
+    """Config 5: N=14336, K=4096, T=512 prefill on the tensor cores; weight
+    copies cycled so their total exceeds L2."""
+    import torch
+
+    c5 = synth.CONFIGS["c5"]
+    n, k, t = c5["n"], c5["k"], c5["t"]
+    wbytes = n * (k // QK) * BLOCK_BYTES
+    copies = 12
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5000)
+    blocks = torch.empty(copies * wbytes, dtype=torch.uint8, device=dev)
+    for l in range(copies):
+        w = synth.device_weights(n, k, c5["p_zero"], c5["d_lo"], c5["d_hi"], gen, dev)
+        L.tq1_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+        del w
+    x = synth.device_activations((t, k), gen, dev)
+    q8 = torch.empty(t * (k // QK8) * Q8_BYTES, dtype=torch.uint8, device=dev)
+    y = torch.empty((t, n), dtype=torch.float32, device=dev)
+    L.q8_1_quantize_acts(x, q8, t, k)
+    bp, qp, yp = blocks.data_ptr(), q8.data_ptr(), y.data_ptr()
+
+    def calls(s):
+        for l in range(copies):
+            assert lib.tq1_mmv(bp + l * wbytes, qp, yp, n, k, t, s) == 0
+
+    g = capture(calls)
+    ms = _time_graph(g, stream, 5) / copies
+    assert lib.tq1_sync_status(stream.cuda_stream) == 0
+    flops = 2.0 * n * k * t
+    peaks = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    del g, blocks
+    return {"workload": "c5: N=14336 K=4096 T=512", "us_per_call": round(ms * 1e3, 2),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+            "tensor_tflops_issued": round(2 * flops / (ms * 1e-3) / 1e12, 1),
+            "peak_tflops": peak, "frac": round(flops / (ms * 1e-3) / 1e12 / peak, 4),
+            "note": "tflops counts the method's MACs once; the kernel issues each twice (fp16 hi and lo "
+                    "parts of the activations); peak = measured bf16 dense (fp16 runs at the same rate)"}
+
+
+def moe_bench(lib, L, synth, dev, stream, capture, args) -> dict:
+    """Config 4: 128 experts of N=768, K=2048, Zipf top-8 routing, T=1 and 32.
+    Effective bytes count the packed weights of the experts actually routed
+    to, the activations and the outputs."""
+    import numpy as np
+    import torch
+
+    c4 = synth.CONFIGS["c4"]
+    E, n, k, top_k = c4["n_experts"], c4["n"], c4["k"], c4["top_k"]
+    eb = n * (k // QK) * BLOCK_BYTES
+    sets = max(1, int(math.ceil(4 * 126 * 2 ** 20 / (E * eb))))  # expert tables > 4x L2 in total
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4000)
+    blocks = torch.empty(sets * E * eb, dtype=torch.uint8, device=dev)
+    for i in range(sets * E):
+        w = synth.device_weights(n, k, c4["p_zero"], c4["d_lo"], c4["d_hi"], gen, dev)
+        L.tq1_quantize_rows(w, blocks[i * eb:(i + 1) * eb], n, k)
+        del w
+    out = {"workload": "c4: 128 experts x (N=768, K=2048), Zipf(1.1) top-8", "expert_sets": sets}
+    for t in (1, 32):
+        m = synth.config_moe(t)
+        q8 = torch.empty(t * (k // QK8) * Q8_BYTES, dtype=torch.uint8, device=dev)
+        L.q8_1_quantize_acts(torch.from_numpy(m.x).to(dev), q8, t, k)
+        ids = torch.from_numpy(m.ids).to(dev)
+        y = torch.empty((t, top_k, n), dtype=torch.float32, device=dev)
+        wsb = L.tq1_mmv_id_workspace_size(E, t, top_k)
+        wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+        def calls(s, q8=q8, ids=ids, y=y, wsp=wsp, wsb=wsb, t=t):
+            for i in range(sets):
+                assert lib.tq1_mmv_id(blocks.data_ptr() + i * E * eb, E, q8.data_ptr(), ids.data_ptr(), y.data_ptr(),
+                                      n, k, t, top_k, wsp.data_ptr(), wsb, s) == 0
+
+        g = capture(calls)
+        ms = _time_graph(g, stream, 10) / sets
+        assert lib.tq1_sync_status(stream.cuda_stream) == 0
+        used = len(np.unique(m.ids))
+        byts = used * eb + t * (k // QK8) * Q8_BYTES + 4 * t * top_k * n
+        out[f"t{t}"] = {"us_per_call": round(ms * 1e3, 2), "experts_used": used,
+                        "effective_gbs": round(byts / (ms * 1e-3) / 1e9, 1)}
+        del g
+    del blocks
     return out
 
 
@@ -463,6 +593,7 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--sweep-passes", type=int, default=15)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the config 4 (MoE) and config 5 (prefill) lines")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per mat-vec launch from an ncu capture of the current kernel")
