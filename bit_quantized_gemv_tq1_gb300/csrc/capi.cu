@@ -16,7 +16,12 @@ namespace tq1 {
 namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxK = 62720;  // activation records of one column must fit the staging budget
-constexpr int64_t kPrefillMinT = 256;
+// Columns from which tq1_mmv runs on the tensor cores; fewer columns take the
+// dp4a decode kernel.
+#ifndef TQ1_TILE_MIN_T
+#define TQ1_TILE_MIN_T 5
+#endif
+constexpr int64_t kTileMinT = TQ1_TILE_MIN_T;
 std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
@@ -144,9 +149,9 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
   const uint8_t* w = static_cast<const uint8_t*>(blocks);
   const uint8_t* a = static_cast<const uint8_t*>(q8);
   const int64_t q8_row = (k / kQK8) * kQ8Bytes;
-  if (y && t >= kPrefillMinT) {
-    rc = launch_prefill(w, a, y, n, k, t, nullptr, 0, s, st);
-    if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise fall through to 32-column slices
+  if (y && t >= kTileMinT) {
+    rc = launch_tile(w, a, y, n, k, t, s, st);
+    if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the dp4a kernels below
   }
   if (y && t <= 4) {
     rc = launch_mmv_small(w, a, y, n, k, t, s, st);

@@ -1,0 +1,886 @@
+// tile.cu -- TQ1_0 x Q8_1 contraction on the 5th-generation tensor cores
+// (tcgen05, operands and accumulators in tensor memory) for 5 to hundreds of
+// token columns.
+//
+// Once a call carries more than a few columns, the dp4a mat-vec spends its
+// time on integer dot products that grow with T, while the tensor cores
+// finish them almost for free; what is left is the weights' base-3
+// expansion, which does not grow with T.  sm_103a has no integer MMA kind, so
+// the contraction runs in kind::f16 on operands that reproduce the method's
+// products exactly (PrismML-Eng/llama.cpp issue #139 "Proposed approach":
+// expand each packed byte once, reuse the activation fragment across rows and
+// columns):
+//
+//   A[row][k] = fp16(d_w * trit)           exact: trit in {-1, 0, 1}, d_w is fp16
+//   x[t][k]   = d_a * q * 2^-e_t           exact in fp32 (11 + 7 significant bits)
+//   x = hi + lo, hi = fp16(x), lo = fp16(x - hi)   (lo exact unless subnormal)
+//   y[t][row] = 2^e_t * (sum_k A*hi + sum_k A*lo)   fp32 accumulation in TMEM
+//
+// e_t is a per-token power of two that keeps 127 * max d_a below 2^14 (0 for
+// ordinary activations).  Every product is exact; only the fp32 accumulation
+// rounds.
+//
+// A call runs two kernels:
+//  1. tile_prep_kernel turns the Q8_1 activations into the B operand once:
+//     fp16 hi rows [t_pad][k], then lo rows [t_pad][k], and the per-token
+//     scales 2^e_t, in a scratch buffer taken from a library-owned,
+//     stream-ordered memory pool (no synchronisation; capturable in CUDA
+//     graphs).  Padding tokens are zero.
+//  2. tile_kernel: one tile = 128 weight rows (TMEM lanes) x TOK tokens; K
+//     advances in stages of 64 (a quarter of a 256-block).
+//     * a weight producer thread brings, per 256-block, the packed weights of
+//       all 128 rows into a shared-memory ring with one 2-D TMA copy (an
+//       80-byte, 16-byte-aligned window around each row's 54-byte block;
+//       rows past n arrive as zeros);
+//     * a B producer thread copies each stage's hi and lo rows (128-byte
+//       swizzled, K-major: the MMA's operand layout) with 2-D TMA;
+//     * A warps 0-15: group g = w/4 expands whole blocks g, g+4, g+8, ...
+//       for rows 32*(w%4) .. +31 into fp16 +-d_w and stores each quarter
+//       straight into tensor memory (tcgen05.st; a warp may only reach its
+//       own quarter of the TMEM lanes, which is exactly its rows), so the
+//       16-bit A operand never touches shared memory;
+//     * epilogue warps 16-19: TMEM -> registers -> y (or split-K partials);
+//     * warp 20: TMEM allocation; its lane 0 issues the MMAs (A from TMEM).
+//     The four groups work on four blocks at once; the MMA takes their
+//     stages round-robin (block 4i + g, quarter q at position 16i + 4q + g of
+//     the tile's K order), so every ring slot belongs to one group and every
+//     mbarrier parity wait is answered by the phase it waits for.
+// Small T (decode batches) cannot fill the GPU with 128-row tiles alone, so a
+// tile's K range is split over a cluster of S CTAs; each rank leaves its fp32
+// partial tile in shared memory and, after a cluster barrier, each rank sums
+// a slice of rows over all ranks in rank order through distributed shared
+// memory (deterministic).  Larger T runs persistent CTAs over tiles with two
+// TMEM accumulators, so the epilogue of one tile overlaps the next.  Every
+// wait is bounded; the first timeout sets a shared abort flag that releases
+// every other wait, the status word records it, and the CTA lets its issued
+// copies and MMAs finish before it leaves.
+//
+// Requires the weight row stride (k/256 * 54 bytes) to be a multiple of 16
+// (k a multiple of 2048): the launcher returns TQ1_ERR_UNSUPPORTED otherwise
+// and the caller uses the dp4a kernels.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/tq1.h"
+#include "tq1_device.cuh"
+#include "tq1_internal.h"
+
+namespace tq1 {
+
+namespace {
+
+constexpr int kTileRows = 128;  // weight rows per tile = TMEM lanes
+constexpr int kStageK = 64;     // K per stage
+constexpr int kWinBytes = 80;   // raw weight window per row and block (16-byte aligned)
+constexpr uint32_t kWRawBytes = kTileRows * kWinBytes;
+constexpr int kWSlotsPerGroup = 2;
+constexpr int kRW = 4 * kWSlotsPerGroup;  // raw weight ring: two blocks per A warp group
+constexpr int kAWarps = 16, kEWarps = 4;
+constexpr int kEWarp0 = kAWarps, kMWarp = kEWarp0 + kEWarps, kPWarpW = kMWarp + 1, kPWarpB = kMWarp + 2;
+constexpr int kTThreads = (kPWarpB + 1) * 32;
+constexpr int kMaxSplit = 8;
+constexpr int kPrepThreads = 256;
+
+template <int TOK>
+struct TileCfg {
+  static constexpr int N = 2 * TOK;                      // B rows: hi of TOK tokens, then lo
+  static constexpr uint32_t kBTile = N * 128;            // bytes per stage
+  // A stages live in tensor memory, B stages in shared memory, each ring as
+  // deep as its memory allows (multiples of 4: one slot column per group).
+  static constexpr int kStagesA = TOK <= 32 ? 12 : 8;
+  static constexpr int kStagesB = TOK <= 32 ? 12 : 8;
+  static_assert(kStagesA % 4 == 0 && kStagesB % 4 == 0, "stage rings must be multiples of the 4 A warp groups");
+  static constexpr int kAccCols = N < 32 ? 32 : N;       // TMEM columns per accumulator
+  static constexpr int kA0 = 2 * kAccCols;               // first TMEM column of the A stages
+  static constexpr int kTmemCols = 512;
+  static_assert(kA0 + kStagesA * 32 <= kTmemCols, "tensor memory budget");
+  static constexpr bool kSplitOk = TOK <= 32;            // split-K partials fit the B ring
+  static_assert(!kSplitOk || kStagesB * kBTile >= kTileRows * TOK * 4, "split-K partials");
+  static constexpr uint32_t kOffW = kStagesB * kBTile;
+  static constexpr uint32_t kSmem = kOffW + kRW * kWRawBytes + 1024;
+  // Instruction descriptor: D fp32, A and B fp16, K-major, N, M = 128.
+  static constexpr uint32_t kIdesc =
+      (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(kTileRows) >> 4) << 24);
+  static constexpr int kChunk = TOK < 32 ? TOK : 32;     // TMEM columns per epilogue load
+};
+
+struct TileArgs {
+  const float* scale;  // per-token 2^e_t (prep kernel output)
+  float* y;
+  unsigned* status;
+  int n, k, t, t_pad;
+  int tiles_m, tiles_n;
+  int split;  // S: CTAs (one cluster) sharing one tile's K range; 1 = persistent over tiles
+};
+
+// ------------------------------------------------------------- helpers --
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.  The
+// waiting thread sleeps in the barrier (suspend-time hint) rather than spin,
+// so the warps doing the work keep the issue slots.
+constexpr uint32_t kAbortPollNs = 20000;  // how often a sleeping waiter looks at the abort flag
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kAbortPollNs)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Lane 0 waits; the verdict is broadcast and the warp re-converges, which
+// orders the other lanes' later accesses after the wait.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                  // leading offset (unused: K fits one atom row)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride between 8-row groups
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// D (TMEM) += A (TMEM: lane = row, two fp16 per column) * B (shared memory).
+__device__ __forceinline__ void umma_ts(uint32_t dtmem, uint32_t atmem, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dtmem),
+      "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 2-D tiled TMA load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+template <int NC>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[NC]);
+
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr));
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// fp32 at the same shared-memory offset as `local`, in cluster CTA `rank`.
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+// P_k = floor(b * 3^k / 256) of the four bytes held in 16-bit lanes lo
+// (bytes 0, 2) and hi (bytes 1, 3); digit k = P_{k+1} - 3 P_k.
+template <int K>
+__device__ __forceinline__ uint32_t pk(uint32_t lo, uint32_t hi) {
+  return __byte_perm(lo * pow3(K), hi * pow3(K), 0x7351u);
+}
+
+// Four fp16 values (digit - 1) * d_w from one digit word: a byte permute reads
+// them from the table {-d_w, 0, +d_w}; the selector of a digit pair (D0, D1)
+// is 34 * (D0 + 256 * D1) + 0x1010, both pairs from one multiply-add.
+__device__ __forceinline__ void digits_to_f16(uint32_t D, uint32_t tlo, uint32_t thi, uint32_t& v0, uint32_t& v1) {
+  const uint32_t sel = D * 34u + 0x10101010u;
+  v0 = __byte_perm(tlo, thi, sel);
+  v1 = __byte_perm(tlo, thi, sel >> 16);
+}
+
+// Expand quarter `Q` of one block row into its 64 K values (fp16 +-d_w),
+// two per 32-bit word in K order: out[i] holds elements 2i, 2i+1 of the
+// stage.  Element order (issue #139, "Current behavior", continued over
+// qs[32..47] and qh): chunk j < 5 = digit j of qs words 0..7; chunk 5 / 6 =
+// digits 0,1 / 2,3 of qs words 8..11 (word i -> chunk words i and 4 + i);
+// chunk 7 = digit 4 of qs words 8..11, then the qh word's digits 0..3.  Stage
+// quarter Q holds chunks 2Q and 2Q + 1: chunk word wd of chunk j lands at
+// out[16 * (j - 2Q) + 2 * wd].
+template <int Q>
+__device__ __forceinline__ void expand_quarter(const uint32_t (&wv)[13], uint32_t tlo, uint32_t thi,
+                                               uint32_t (&out)[32]) {
+  auto put = [&](int j, int wd, uint32_t D) {
+    digits_to_f16(D, tlo, thi, out[16 * (j - 2 * Q) + 2 * wd], out[16 * (j - 2 * Q) + 2 * wd + 1]);
+  };
+  auto split = [&](uint32_t x, uint32_t& lo, uint32_t& hi) {
+    lo = __byte_perm(x, 0u, 0x4240u);
+    hi = __byte_perm(x, 0u, 0x4341u);
+  };
+  if (Q == 0) {
+#pragma unroll
+    for (int wd = 0; wd < 8; ++wd) {
+      uint32_t l, h;
+      split(wv[wd], l, h);
+      const uint32_t p1 = pk<1>(l, h), p2 = pk<2>(l, h);
+      put(0, wd, p1);
+      put(1, wd, p2 - 3u * p1);
+    }
+  } else if (Q == 1) {
+#pragma unroll
+    for (int wd = 0; wd < 8; ++wd) {
+      uint32_t l, h;
+      split(wv[wd], l, h);
+      const uint32_t p2 = pk<2>(l, h), p3 = pk<3>(l, h), p4 = pk<4>(l, h);
+      put(2, wd, p3 - 3u * p2);
+      put(3, wd, p4 - 3u * p3);
+    }
+  } else if (Q == 2) {
+#pragma unroll
+    for (int wd = 0; wd < 8; ++wd) {  // chunk 4: digit 4 of qs words 0..7
+      uint32_t l, h;
+      split(wv[wd], l, h);
+      put(4, wd, pk<5>(l, h) - 3u * pk<4>(l, h));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // chunk 5: digits 0 / 1 of qs words 8..11
+      uint32_t l, h;
+      split(wv[8 + i], l, h);
+      const uint32_t p1 = pk<1>(l, h), p2 = pk<2>(l, h);
+      put(5, i, p1);
+      put(5, 4 + i, p2 - 3u * p1);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // chunks 6, 7: digits 2, 3, 4 of qs words 8..11
+      uint32_t l, h;
+      split(wv[8 + i], l, h);
+      const uint32_t p2 = pk<2>(l, h), p3 = pk<3>(l, h), p4 = pk<4>(l, h), p5 = pk<5>(l, h);
+      put(6, i, p3 - 3u * p2);
+      put(6, 4 + i, p4 - 3u * p3);
+      put(7, i, p5 - 3u * p4);
+    }
+    {  // chunk 7, words 4..7: the qh digits
+      uint32_t l, h;
+      split(wv[12], l, h);
+      const uint32_t p1 = pk<1>(l, h), p2 = pk<2>(l, h), p3 = pk<3>(l, h), p4 = pk<4>(l, h);
+      put(7, 4, p1);
+      put(7, 5, p2 - 3u * p1);
+      put(7, 6, p3 - 3u * p2);
+      put(7, 7, p4 - 3u * p3);
+    }
+  }
+}
+
+// The 13 logical words of a block and its fp16 scale from the row's raw
+// window W (20 words), where the block starts 4*J0 + sh/8 bytes in.
+template <int J0>
+__device__ __forceinline__ void realign(const uint32_t (&W)[20], uint32_t sh, uint32_t (&wv)[13], uint32_t& h) {
+#pragma unroll
+  for (int m = 0; m < 13; ++m) wv[m] = __funnelshift_r(W[J0 + m], W[J0 + m + 1], sh);
+  h = (W[J0 + 13] >> sh) & 0xFFFFu;
+}
+
+// Eight int8 activations (two words) times fp16 d -> fp16 hi and lo parts.
+__device__ __forceinline__ void acts_to_hilo(uint32_t q0, uint32_t q1, __half2 d2, uint4& hv, uint4& lv) {
+  const __half2 c1152 = __float2half2_rn(1152.0f);
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    // int8 q -> exact fp16: bias to 0..255, place under the exponent of 1024
+    // (0x64xx), subtract 1024 + 128.
+    const uint32_t x = (u ? q1 : q0) ^ 0x80808080u;
+    const uint32_t m01 = __byte_perm(x, 0x64646464u, 0x5150u);
+    const uint32_t m23 = __byte_perm(x, 0x64646464u, 0x5352u);
+    const __half2 v01 = __hsub2(*reinterpret_cast<const __half2*>(&m01), c1152);
+    const __half2 v23 = __hsub2(*reinterpret_cast<const __half2*>(&m23), c1152);
+    const __half2 h01 = __hmul2(v01, d2), h23 = __hmul2(v23, d2);
+    const __half2 l01 = __hfma2(v01, d2, __hneg2(h01)), l23 = __hfma2(v23, d2, __hneg2(h23));
+    h[2 * u] = *reinterpret_cast<const uint32_t*>(&h01);
+    h[2 * u + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+    l[2 * u] = *reinterpret_cast<const uint32_t*>(&l01);
+    l[2 * u + 1] = *reinterpret_cast<const uint32_t*>(&l23);
+  }
+  hv = make_uint4(h[0], h[1], h[2], h[3]);
+  lv = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+
+// Position, in a tile's K order, of quarter q of the tile's block bi (of
+// nblk): blocks go in rounds of four, one per A warp group; within a round
+// the stages are taken quarter by quarter, group by group.
+__device__ __forceinline__ int stage_of(int bi, int q, int nblk) {
+  const int i = bi >> 2, g = bi & 3;
+  const int groups = min(4, nblk - 4 * i);
+  return 16 * i + q * groups + g;
+}
+
+}  // namespace
+
+// Q8_1 activations -> B operand: fp16 hi rows [t_pad][k], lo rows
+// [t_pad][k], per-token scale 2^e_t.  One CTA per (padded) token.
+__global__ void __launch_bounds__(kPrepThreads) tile_prep_kernel(const uint8_t* q8, int t, int k, int t_pad,
+                                                                 uint16_t* hilo, float* scale) {
+  __shared__ float s_red[kPrepThreads / 32];
+  __shared__ float s_inv;
+  pdl_launch_dependents();
+  pdl_wait();  // the activations may come from the previous kernel
+  const int tok = blockIdx.x, tid = threadIdx.x;
+  const int nq = k / kQK8;
+  uint16_t* hrow = hilo + static_cast<size_t>(tok) * k;
+  uint16_t* lrow = hilo + (static_cast<size_t>(t_pad) + tok) * k;
+  if (tok >= t) {
+    for (int i = tid; i < k / 8; i += kPrepThreads) {
+      reinterpret_cast<uint4*>(hrow)[i] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(lrow)[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (tid == 0) scale[tok] = 1.0f;
+    return;
+  }
+  const uint8_t* qr = q8 + static_cast<int64_t>(tok) * nq * kQ8Bytes;
+  float m = 0.0f;
+  for (int j = tid; j < nq; j += kPrepThreads)
+    m = fmaxf(m, fabsf(__half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(qr + j * kQ8Bytes))))));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((tid & 31) == 0) s_red[tid >> 5] = m;
+  __syncthreads();
+  if (tid == 0) {
+    float v = 0.0f;
+    for (int w = 0; w < kPrepThreads / 32; ++w) v = fmaxf(v, s_red[w]);
+    int ex = 0;
+    (void)frexpf(v * 127.0f, &ex);  // 127 * max d < 2^ex
+    const int e = max(0, ex - 14);
+    scale[tok] = ldexpf(1.0f, e);
+    s_inv = ldexpf(1.0f, -e);
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  for (int j = tid; j < nq; j += kPrepThreads) {
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(qr + j * kQ8Bytes);
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(__ldg(b) & 0xFFFFu))) * inv;
+    const __half2 d2 = __float2half2_rn(d);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint4 hv, lv;
+      acts_to_hilo(__ldg(b + 1 + 2 * g), __ldg(b + 2 + 2 * g), d2, hv, lv);
+      reinterpret_cast<uint4*>(hrow + kQK8 * j)[g] = hv;
+      reinterpret_cast<uint4*>(lrow + kQK8 * j)[g] = lv;
+    }
+  }
+}
+
+template <int TOK>
+__global__ void __launch_bounds__(kTThreads, 1)
+    tile_kernel(const TileArgs a, const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmb) {
+  using C = TileCfg<TOK>;
+  extern __shared__ __align__(1024) uint8_t tsmem_raw[];
+  __shared__ __align__(8) uint64_t afull_bar[C::kStagesA], aempty_bar[C::kStagesA];
+  __shared__ __align__(8) uint64_t bfull_bar[C::kStagesB], bempty_bar[C::kStagesB];
+  __shared__ __align__(8) uint64_t wfull_bar[kRW], wempty_bar[kRW];
+  __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  volatile int* abort_flag = &s_abort;
+
+  const uint32_t raw = smem_addr(tsmem_raw);
+  uint8_t* sm = tsmem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = smem_addr(sm);
+  uint8_t* wraw = sm + C::kOffW;
+  float* red = reinterpret_cast<float*>(sm);  // split-K partials reuse the B stages after the last MMA
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = a.k / kQK;
+  const int S = a.split;
+  const int ntiles = a.tiles_m * a.tiles_n;
+  const int rank = S > 1 ? static_cast<int>(blockIdx.x % S) : 0;
+  const int kb0 = S > 1 ? (nb * rank) / S : 0;
+  const int kb1 = S > 1 ? (nb * (rank + 1)) / S : nb;
+  const int nblk = kb1 - kb0;  // blocks per tile (the same for every tile of this CTA)
+  const int nst = 4 * nblk;    // stages per tile
+  auto unit_tile = [&](int u) -> int {
+    if (S > 1) return u == 0 ? static_cast<int>(blockIdx.x / S) : ntiles;
+    return static_cast<int>(blockIdx.x) + u * static_cast<int>(gridDim.x);
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < C::kStagesA; ++i) {
+      mbar_init(&afull_bar[i], 4);  // the 4 warps of the stage's A group
+      mbar_init(&aempty_bar[i], 1);
+    }
+    for (int i = 0; i < C::kStagesB; ++i) {
+      mbar_init(&bfull_bar[i], 1);
+      mbar_init(&bempty_bar[i], 1);
+    }
+    for (int i = 0; i < kRW; ++i) {
+      mbar_init(&wfull_bar[i], 1);
+      mbar_init(&wempty_bar[i], 4);  // the 4 warps of the slot's A group
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf_bar[i], 1);
+      mbar_init(&acce_bar[i], kEWarps);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_tmem)),
+                 "r"(C::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  pdl_launch_dependents();
+
+  if (warp < kAWarps) {
+    // ---------------------------------------------------------------- A --
+    const int g = warp >> 2;       // blocks g, g + 4, ... of every tile
+    const int quarter = warp & 3;  // TMEM lane quarter = rows 32*quarter ..
+    const int rl = (quarter << 5) | lane;
+    uint32_t c = 0;  // this group's blocks so far (raw weight ring position)
+    bool ok = true;
+    for (int u = 0; ok; ++u) {
+      const int tile = unit_tile(u);
+      if (tile >= ntiles) break;
+      for (int bi = g; bi < nblk; bi += 4, ++c) {
+        const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
+        if (!warp_wait(&wfull_bar[ws], (c / kWSlotsPerGroup) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint32_t W[20];
+        const uint4* src = reinterpret_cast<const uint4*>(wraw + ws * kWRawBytes + rl * kWinBytes);
+#pragma unroll
+        for (int cc = 0; cc < 5; ++cc) {
+          const uint4 v = src[cc];
+          W[4 * cc] = v.x;
+          W[4 * cc + 1] = v.y;
+          W[4 * cc + 2] = v.z;
+          W[4 * cc + 3] = v.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty_bar[ws]);
+        const uint32_t off = static_cast<uint32_t>((kb0 + bi) * kBlockBytes) & 15u;
+        const uint32_t sh = (off & 2u) * 8u;
+        uint32_t wv[13], h;
+        switch (off >> 2) {
+          case 0: realign<0>(W, sh, wv, h); break;
+          case 1: realign<1>(W, sh, wv, h); break;
+          case 2: realign<2>(W, sh, wv, h); break;
+          default: realign<3>(W, sh, wv, h); break;
+        }
+        const uint32_t tlo = h ^ 0x8000u;  // bytes 0-1: -d_w, bytes 2-3: 0
+        const uint32_t thi = h;            // bytes 4-5: +d_w
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t m = static_cast<uint32_t>(u * nst + stage_of(bi, q, nblk));
+          const uint32_t slot = m % C::kStagesA;
+          if (!warp_wait(&aempty_bar[slot], ((m / C::kStagesA) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t out[32];
+          if (q == 0) expand_quarter<0>(wv, tlo, thi, out);
+          else if (q == 1) expand_quarter<1>(wv, tlo, thi, out);
+          else if (q == 2) expand_quarter<2>(wv, tlo, thi, out);
+          else expand_quarter<3>(wv, tlo, thi, out);
+          tmem_st32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kA0 + slot * 32u, out);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull_bar[slot]);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp < kMWarp) {
+    // --------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may read
+    const int rl = quarter * 32 + lane;
+    pdl_wait();  // the scales are written by the prep kernel
+    for (int u = 0;; ++u) {
+      const int tile = unit_tile(u);
+      if (tile >= ntiles) break;
+      const int row = (tile / a.tiles_n) * kTileRows + rl;
+      const int tok0 = (tile % a.tiles_n) * TOK;
+      const int acc = u & 1;
+      if (!warp_wait(&accf_bar[acc], (u >> 1) & 1u, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
+#pragma unroll 1
+      for (int c0 = 0; c0 < TOK; c0 += C::kChunk) {
+        uint32_t vh[C::kChunk], vl[C::kChunk];
+        tmem_ld<C::kChunk>(tbase + c0, vh);
+        tmem_ld<C::kChunk>(tbase + TOK + c0, vl);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int jj = 0; jj < C::kChunk; ++jj) {
+          const int tl = c0 + jj, tok = tok0 + tl;
+          const float v = (__uint_as_float(vh[jj]) + __uint_as_float(vl[jj])) * __ldg(a.scale + tok);
+          if (S > 1) {
+            red[tl * kTileRows + rl] = v;
+          } else if (row < a.n && tok < a.t) {
+            a.y[static_cast<int64_t>(tok) * a.n + row] = v;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[acc]);
+    }
+  } else if (warp == kMWarp) {
+    // -------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      bool issued = false, ok = true;
+      uint64_t* last_bar = nullptr;
+      uint32_t last_ph = 0;
+      for (int u = 0; ok; ++u) {
+        const int tile = unit_tile(u);
+        if (tile >= ntiles) break;
+        const int acc = u & 1;
+        if (!wait_or_abort(&acce_bar[acc], ((u >> 1) & 1u) ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + static_cast<uint32_t>(acc * C::kAccCols);
+        for (int st = 0; st < nst; ++st) {
+          const uint32_t m = static_cast<uint32_t>(u * nst + st);
+          const uint32_t sa = m % C::kStagesA, pa = (m / C::kStagesA) & 1u;
+          const uint32_t sbs = m % C::kStagesB, pb = (m / C::kStagesB) & 1u;
+          if (!wait_or_abort(&afull_bar[sa], pa, abort_flag) || !wait_or_abort(&bfull_bar[sbs], pb, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t at = tmem + C::kA0 + sa * 32u;
+          const uint32_t sb = sbase + sbs * C::kBTile;
+#pragma unroll
+          for (int ks = 0; ks < kStageK / 16; ++ks)
+            umma_ts(dt, at + 8u * ks, umma_desc_sw128(sb + 32u * ks), C::kIdesc, (st > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&aempty_bar[sa]);
+          umma_commit(&bempty_bar[sbs]);
+          issued = true;
+          last_bar = &bempty_bar[sbs];
+          last_ph = pb;
+        }
+        if (!ok) break;
+        umma_commit(&accf_bar[acc]);
+      }
+      // After an abort, let the MMAs already issued finish (bounded) before
+      // the tensor memory is released.
+      if (*abort_flag && issued) (void)mbar_wait(last_bar, last_ph);
+    }
+  } else if (warp == kPWarpW) {
+    // ---------------------------------------------------- weight copies --
+    if (lane == 0) {
+      uint32_t cnt[4] = {0, 0, 0, 0};
+      int last_slot = -1;
+      uint32_t last_ph = 0;
+      for (int u = 0;; ++u) {
+        const int tile = unit_tile(u);
+        if (tile >= ntiles) break;
+        const int row0 = (tile / a.tiles_n) * kTileRows;
+        bool ok = true;
+        for (int bi = 0; bi < nblk; ++bi) {
+          const int g = bi & 3;
+          const uint32_t c = cnt[g]++;
+          const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
+          const uint32_t ph = (c / kWSlotsPerGroup) & 1u;
+          if (!wait_or_abort(&wempty_bar[ws], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&wfull_bar[ws], kWRawBytes);
+          tma_load_2d(wraw + ws * kWRawBytes, &tmw, ((kb0 + bi) * kBlockBytes) & ~15, row0, &wfull_bar[ws]);
+          last_slot = static_cast<int>(ws);
+          last_ph = ph;
+        }
+        if (!ok) break;
+      }
+      // Copies still in flight must land before the CTA leaves.
+      if (*abort_flag && last_slot >= 0) (void)mbar_wait(&wfull_bar[last_slot], last_ph);
+    }
+  } else {
+    // ------------------------------------------------ activation copies --
+    if (lane == 0) {
+      pdl_wait();  // the B operand is written by the prep kernel
+      int last_slot = -1;
+      uint32_t last_ph = 0;
+      for (int u = 0;; ++u) {
+        const int tile = unit_tile(u);
+        if (tile >= ntiles) break;
+        const int tok0 = (tile % a.tiles_n) * TOK;
+        bool ok = true;
+        // Stages in the MMA's order: rounds of four blocks, quarter by quarter.
+        for (int i = 0; 4 * i < nblk && ok; ++i) {
+          const int groups = min(4, nblk - 4 * i);
+          for (int q = 0; q < 4 && ok; ++q)
+            for (int gg = 0; gg < groups; ++gg) {
+              const uint32_t m = static_cast<uint32_t>(u * nst + 16 * i + q * groups + gg);
+              const uint32_t sbs = m % C::kStagesB, pb = (m / C::kStagesB) & 1u;
+              if (!wait_or_abort(&bempty_bar[sbs], pb ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const int kx = (kb0 + 4 * i + gg) * kQK + q * kStageK;
+              uint8_t* dst = sm + sbs * C::kBTile;
+              mbar_arrive_expect_tx(&bfull_bar[sbs], C::kBTile);
+              tma_load_2d(dst, &tmb, kx, tok0, &bfull_bar[sbs]);
+              tma_load_2d(dst + TOK * 128, &tmb, kx, a.t_pad + tok0, &bfull_bar[sbs]);
+              last_slot = static_cast<int>(sbs);
+              last_ph = pb;
+            }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag && last_slot >= 0) (void)mbar_wait(&bfull_bar[last_slot], last_ph);
+    }
+  }
+
+  __syncthreads();
+  if (tid == 0 && *abort_flag) raise_status(a.status, kStatusTimeout);
+  if (S > 1) {
+    __syncwarp();
+    cluster_sync_all();  // every rank's partial tile is in its shared memory
+    if (!*abort_flag && warp >= kEWarp0 && warp < kMWarp) {
+      const int tile = static_cast<int>(blockIdx.x / S);
+      const int row0 = (tile / a.tiles_n) * kTileRows, tok0 = (tile % a.tiles_n) * TOK;
+      const int r_lo = (kTileRows * rank) / S, r_hi = (kTileRows * (rank + 1)) / S;
+      const int nr = r_hi - r_lo;
+      for (int i = tid - kEWarp0 * 32; i < nr * TOK; i += kEWarps * 32) {
+        const int tl = i / nr, rl = r_lo + (i - (i / nr) * nr);
+        const int row = row0 + rl, tok = tok0 + tl;
+        if (row < a.n && tok < a.t) {
+          float part[kMaxSplit];
+#pragma unroll
+          for (int s = 0; s < kMaxSplit; ++s)
+            part[s] = s < S ? ld_peer(&red[tl * kTileRows + rl], static_cast<uint32_t>(s)) : 0.0f;
+          float v = 0.0f;
+#pragma unroll
+          for (int s = 0; s < kMaxSplit; ++s) v += s < S ? part[s] : 0.0f;  // rank order
+          a.y[static_cast<int64_t>(tok) * a.n + row] = v;
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();  // no rank leaves while others still read its partials
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMWarp) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+  }
+}
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major 2-D map over `rows` x `row_elems` elements with a `box` window.
+bool make_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, const void* base, uint64_t row_elems,
+              uint64_t rows, uint32_t box_x, uint32_t box_y, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {row_elems, rows};
+  const cuuint64_t strides[1] = {row_elems * esize};
+  const cuuint32_t box[2] = {box_x, box_y};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Library-owned pool for the prep kernel's scratch: stream-ordered
+// allocations that keep their memory cached between calls.
+cudaMemPool_t scratch_pool(int dev) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t p = nullptr;
+    if (!cuda_ok(cudaMemPoolCreate(&p, &props))) return nullptr;
+    uint64_t keep = ~uint64_t{0};
+    if (!cuda_ok(cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep))) return nullptr;
+    pools[dev] = p;
+  }
+  return pools[dev];
+}
+
+template <int TOK>
+int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms, cudaStream_t s) {
+  using C = TileCfg<TOK>;
+  const DeviceInfo& di = device_info();
+  static bool configured[64] = {};
+  if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
+  if (C::kSmem + 2048 > di.max_smem_optin) return TQ1_ERR_UNSUPPORTED;
+  if (!configured[di.device]) {
+    if (!cuda_ok(cudaFuncSetAttribute(tile_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(C::kSmem))))
+      return TQ1_ERR_CUDA;
+    configured[di.device] = true;
+  }
+  a.tiles_m = (a.n + kTileRows - 1) / kTileRows;
+  a.tiles_n = (a.t + TOK - 1) / TOK;
+  a.t_pad = a.tiles_n * TOK;
+  const int nb = a.k / kQK;
+  const uint64_t rowbytes = static_cast<uint64_t>(nb) * kBlockBytes;
+  const size_t hilo_bytes = 2 * static_cast<size_t>(a.t_pad) * a.k * sizeof(uint16_t);
+  const size_t ws_bytes = hilo_bytes + static_cast<size_t>(a.t_pad) * sizeof(float);
+
+  CUtensorMap tmw;
+  if (!make_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, rowbytes, static_cast<uint64_t>(a.n), kWinBytes, kTileRows,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return TQ1_ERR_UNSUPPORTED;
+  cudaMemPool_t pool = scratch_pool(di.device);
+  if (!pool) return TQ1_ERR_CUDA;
+  void* ws = nullptr;
+  if (!cuda_ok(cudaMallocFromPoolAsync(&ws, ws_bytes, pool, s))) return TQ1_ERR_CUDA;
+  uint16_t* hilo = static_cast<uint16_t*>(ws);
+  float* scale = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + hilo_bytes);
+  a.scale = scale;
+  int rc = TQ1_OK;
+  CUtensorMap tmb;
+  if (!make_map(&tmb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hilo, static_cast<uint64_t>(a.k),
+                2 * static_cast<uint64_t>(a.t_pad), kStageK, TOK, CU_TENSOR_MAP_SWIZZLE_128B))
+    rc = TQ1_ERR_UNSUPPORTED;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  if (rc == TQ1_OK) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.t_pad));
+    cfg.blockDim = dim3(kPrepThreads);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (!cuda_ok(cudaLaunchKernelEx(&cfg, tile_prep_kernel, q8, a.t, a.k, a.t_pad, hilo, scale))) rc = TQ1_ERR_CUDA;
+  }
+  if (rc == TQ1_OK) {
+    const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
+    int split = 1;
+    if (C::kSplitOk && 2 * tiles <= num_sms)
+      split = static_cast<int>(std::min<int64_t>({kMaxSplit, nb, num_sms / tiles}));
+    a.split = split;
+    const int64_t grid = split > 1 ? tiles * split : std::min<int64_t>(tiles, num_sms);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kTThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0] = pdl[0];
+    int na = 1;
+    if (split > 1) {
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = static_cast<unsigned>(split);
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    if (!cuda_ok(cudaLaunchKernelEx(&cfg, tile_kernel<TOK>, a, tmw, tmb))) rc = TQ1_ERR_CUDA;
+  }
+  // The scratch goes back to the pool once the kernels above have finished.
+  if (!cuda_ok(cudaFreeAsync(ws, s)) && rc == TQ1_OK) rc = TQ1_ERR_CUDA;
+  return rc;
+}
+
+}  // namespace
+
+int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
+                unsigned* status) {
+  if (n > (int64_t{1} << 30) || t > (int64_t{1} << 24) || k > (int64_t{1} << 30)) return TQ1_ERR_UNSUPPORTED;
+  // The weight map's row stride must be a multiple of 16 bytes.
+  if (((k / kQK) * kBlockBytes) % 16 != 0) return TQ1_ERR_UNSUPPORTED;
+  const DeviceInfo& di = device_info();
+  TileArgs a = {};
+  a.y = y;
+  a.status = status;
+  a.n = static_cast<int>(n);
+  a.k = static_cast<int>(k);
+  a.t = static_cast<int>(t);
+  if (t <= 8) return launch_tile_tok<8>(w, q8, a, di.num_sms, s);
+  if (t <= 16) return launch_tile_tok<16>(w, q8, a, di.num_sms, s);
+  if (t <= 32) return launch_tile_tok<32>(w, q8, a, di.num_sms, s);
+  return launch_tile_tok<64>(w, q8, a, di.num_sms, s);
+}
+
+}  // namespace tq1

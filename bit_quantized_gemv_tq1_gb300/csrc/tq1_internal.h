@@ -41,9 +41,10 @@ int launch_moe_compact(const int32_t* ids, int64_t t, int64_t top_k, int64_t n_e
 int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float* y, int64_t n, int64_t k,
                   int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status);
 
-// Dense prefill (t >= 256) on the tensor cores.
-int launch_prefill(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, void* ws,
-                   size_t ws_bytes, cudaStream_t s, unsigned* status);
+// y[c][r] for any t on the tensor cores (tcgen05): 128-row tiles, split-K
+// over a thread-block cluster when the tiles alone cannot fill the GPU.
+int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
+                unsigned* status);
 
 // Workspace layout of the routing table (int32 words):
 //   [0]                 n_active
