@@ -17,9 +17,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxK = 62720;  // activation records of one column must fit the staging budget
 // Columns from which tq1_mmv runs on the tensor cores; fewer columns take the
-// dp4a decode kernel.
+// dp4a kernels (measured crossover on GB300 at N=5120, K=6144: the dp4a
+// kernel's cost grows with every column, the tile path's barely does).
 #ifndef TQ1_TILE_MIN_T
-#define TQ1_TILE_MIN_T 5
+#define TQ1_TILE_MIN_T 11
 #endif
 constexpr int64_t kTileMinT = TQ1_TILE_MIN_T;
 std::mutex g_mu;
@@ -197,10 +198,18 @@ int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, con
   if (!st) return TQ1_ERR_CUDA;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* table = static_cast<int32_t*>(ws);
-  rc = launch_moe_compact(ids, t, top_k, n_experts, table, s, st);
+  const uint8_t* w = static_cast<const uint8_t*>(expert_blocks);
+  const uint8_t* a = static_cast<const uint8_t*>(q8);
+  MoePlan plan{};
+  const bool small = moe_small_plan(n, k, t * top_k, n_experts, &plan);
+  rc = launch_moe_compact(ids, t, top_k, n_experts, small ? plan.chunk : 1, small ? plan.row_blocks : 1, table, s,
+                          st);
   if (rc != TQ1_OK) return rc;
-  return launch_mmv_id(static_cast<const uint8_t*>(expert_blocks), n_experts, static_cast<const uint8_t*>(q8), y,
-                       n, k, t, top_k, table, s, st);
+  if (small) {
+    rc = launch_moe_small(w, a, y, n, k, top_k, n_experts, t * top_k, plan, table, s, st);
+    if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
+  }
+  return launch_mmv_id(w, n_experts, a, y, n, k, t, top_k, table, s, st);
 }
 
 int tq1_sync_status(void* stream) {

@@ -12,7 +12,7 @@
 // fixed-size array that is part of the library image.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
-// library holds it (about 72 KiB) until the process exits.  Its device address
+// library holds it (about 76 KiB) until the process exits.  Its device address
 // is looked up once per device, with that device current, on the first call;
 // that first call should therefore be made before any stream capture begins.
 // All calls on a device share the one array and it keeps the previous call's
@@ -32,7 +32,8 @@ constexpr int64_t kMaxExperts = 1024;
 constexpr int64_t kMaxPairs = 16384;  // tokens * top_k
 // Routing-table words for the largest accepted call, rounded up to whole
 // 256-byte units (the size tq1_mmv_id asks of its workspace).
-constexpr size_t kWords = (1 + static_cast<size_t>(kMaxExperts + 1) + kMaxExperts + kMaxPairs + 63) & ~size_t(63);
+constexpr size_t kWords =
+    (1 + static_cast<size_t>(kMaxExperts + 1) + kMaxExperts + kMaxPairs + (kMaxExperts + 1) + 63) & ~size_t(63);
 constexpr int kMaxDevices = 64;
 
 std::mutex g_mu;

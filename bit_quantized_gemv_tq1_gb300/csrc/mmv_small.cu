@@ -37,6 +37,7 @@
 #include <algorithm>
 
 #include "../../include/tq1.h"
+#include "packed.cuh"
 #include "tq1_device.cuh"
 #include "tq1_internal.h"
 
@@ -44,16 +45,9 @@ namespace tq1 {
 
 namespace {
 
-constexpr int kRowsPerTask = 4;
-constexpr int kLanesPerRow = 8;  // = blocks per task chunk
-constexpr int kMaxGroups = 64;   // row groups (mbarriers) per round
+using namespace packed;
 
-// Shared-memory bytes reserved per 4-row group: up to 15 bytes of alignment
-// slack before the rows, the rows, and the decoder's over-read after them;
-// a multiple of 16 so every group's bulk-copy destination is 16-byte aligned.
-__host__ __device__ __forceinline__ uint32_t group_stride(uint32_t rowbytes) {
-  return (kRowsPerTask * rowbytes + 32u + 15u) & ~15u;
-}
+constexpr int kMaxGroups = 64;   // row groups (mbarriers) per round
 
 // Per column count: threads per CTA, tasks pre-expanded per warp (held in
 // registers across the wait), and the weight-slab budget.
@@ -92,112 +86,6 @@ struct SmallArgs {
   uint32_t slab_bytes;  // shared memory for weight rows (rounds of rows_round rows)
   uint32_t nkc_magic;   // ceil(2^32 / nkc) for nkc > 1: task / nkc == umulhi(task, magic)
 };
-
-// Activation record of one column over one 256-block (word-major so that the
-// four activation words meeting one packed register are contiguous):
-//   words 8w + j  (w, j < 8): int8x4 word w of Q8_1 chunk j
-//   words 64 + j:  chunk j's fp32 scale divided by 4^(j mod 4)
-//   words 72 + j:  -4^(j mod 4) * sum of chunk j's int8 values
-constexpr int kPRec = 100;  // stride: 16-byte aligned, 4 banks apart
-
-struct Packed {
-  uint32_t a[8];  // slots 0..3: chunks 0..3, activation word w
-  uint32_t b[8];  // slots 0..3: chunks 4..7, activation word w
-  float dw;
-};
-
-// Expand the block at byte offset `off` (even) of shared memory `slab` into
-// packed digits.  Element order (PrismML-Eng/llama.cpp issue #139, "Current
-// behavior", continued over the last 16 qs bytes and the 4 qh bytes):
-//   qs word w < 8,  digit j      -> chunk j,         word w
-//   qs word 8 + i,  digit 0 / 1  -> chunk 5,         word i / 4 + i
-//                   digit 2 / 3  -> chunk 6,         word i / 4 + i
-//                   digit 4      -> chunk 7,         word i
-//   qh word,        digit k      -> chunk 7,         word 4 + k
-__device__ __forceinline__ void expand_pack(const uint8_t* slab, uint32_t off, Packed& P) {
-  const uint32_t* p = reinterpret_cast<const uint32_t*>(slab + (off & ~3u));
-  const uint32_t sh = (off & 2u) * 8u;
-  uint32_t w[14];
-#pragma unroll
-  for (int m = 0; m < 14; ++m) w[m] = p[m];
-  // Chunks 5..7 first (slots 1..3 of the b registers).
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t d[5];
-    expand_digits<5>(__funnelshift_r(w[8 + i], w[9 + i], sh), d);
-    P.b[i] = (d[0] << 2) | (d[2] << 4) | (d[4] << 6);
-    P.b[4 + i] = (d[1] << 2) | (d[3] << 4);
-  }
-  {
-    uint32_t d[4];
-    expand_digits<4>(__funnelshift_r(w[12], w[13], sh), d);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) P.b[4 + k] |= d[k] << 6;
-  }
-  // Chunks 0..4.
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t d[5];
-    expand_digits<5>(__funnelshift_r(w[i], w[i + 1], sh), d);
-    P.a[i] = d[0] | (d[1] << 2) | (d[2] << 4) | (d[3] << 6);
-    P.b[i] |= d[4];
-  }
-  P.dw = __half2float(__ushort_as_half(static_cast<unsigned short>((w[13] >> sh) & 0xFFFFu)));
-}
-
-__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-// d_w * sum_j d_a[j] * I_j for one packed block against one column record.
-__device__ __forceinline__ float packed_dot(const Packed& P, const uint32_t* rec) {
-  const int4 s0 = *reinterpret_cast<const int4*>(rec + 72);
-  const int4 s1 = *reinterpret_cast<const int4*>(rec + 76);
-  int I0 = s0.x, I1 = s0.y, I2 = s0.z, I3 = s0.w, I4 = s1.x, I5 = s1.y, I6 = s1.z, I7 = s1.w;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const uint4 qa = *reinterpret_cast<const uint4*>(rec + 8 * w);
-    const uint4 qb = *reinterpret_cast<const uint4*>(rec + 8 * w + 4);
-    I0 = dp4a_us(P.a[w] & 0x03030303u, qa.x, I0);
-    I1 = dp4a_us(P.a[w] & 0x0C0C0C0Cu, qa.y, I1);
-    I2 = dp4a_us(P.a[w] & 0x30303030u, qa.z, I2);
-    I3 = dp4a_us(P.a[w] & 0xC0C0C0C0u, qa.w, I3);
-    I4 = dp4a_us(P.b[w] & 0x03030303u, qb.x, I4);
-    I5 = dp4a_us(P.b[w] & 0x0C0C0C0Cu, qb.y, I5);
-    I6 = dp4a_us(P.b[w] & 0x30303030u, qb.z, I6);
-    I7 = dp4a_us(P.b[w] & 0xC0C0C0C0u, qb.w, I7);
-  }
-  const float4 a0 = *reinterpret_cast<const float4*>(rec + 64);
-  const float4 a1 = *reinterpret_cast<const float4*>(rec + 68);
-  float s = a0.x * static_cast<float>(I0);
-  s = fmaf(a0.y, static_cast<float>(I1), s);
-  s = fmaf(a0.z, static_cast<float>(I2), s);
-  s = fmaf(a0.w, static_cast<float>(I3), s);
-  s = fmaf(a1.x, static_cast<float>(I4), s);
-  s = fmaf(a1.y, static_cast<float>(I5), s);
-  s = fmaf(a1.z, static_cast<float>(I6), s);
-  s = fmaf(a1.w, static_cast<float>(I7), s);
-  return s * P.dw;
-}
-
-// Build one chunk (j) of one column's record from its Q8_1 block (global).
-__device__ __forceinline__ void fill_precord_chunk(const uint8_t* blk, uint32_t* rec, int j) {
-  const uint32_t* s = reinterpret_cast<const uint32_t*>(blk);
-  const uint32_t ds = __ldg(s);
-  int sum = 0;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const uint32_t q = __ldg(s + 1 + w);
-    rec[8 * w + j] = q;
-    sum = __dp4a(static_cast<int>(q), 0x01010101, sum);
-  }
-  const int slot = j & 3;
-  const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(ds & 0xFFFFu)));
-  rec[64 + j] = __float_as_uint(d * __int_as_float((127 - 2 * slot) << 23));  // d / 4^slot, exact
-  rec[72 + j] = static_cast<uint32_t>(-(sum << (2 * slot)));
-}
 
 }  // namespace
 

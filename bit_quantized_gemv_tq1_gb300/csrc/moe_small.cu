@@ -1,0 +1,270 @@
+// moe_small.cu -- expert-routed TQ1_0 x Q8_1 mat-vec for decode batches
+// (mul_mat_id): the packed-digit decode kernel applied to the experts the
+// routing selected.
+//
+// AMD-Ecosystem/llama.cpp PR #76 ("Summary"): mul_mat_id compacts the ids
+// into per-expert bounds and runs a grid over the compacted list, so each
+// expert's weights are read once for all the tokens routed to it.  Here a
+// task is (active expert, a chunk of up to kChunk of its (token, slot)
+// pairs, a range of its rows); the compaction kernel lays the tasks of each
+// active expert out contiguously and records where they start.  Persistent
+// CTAs walk the tasks: per task they request the rows' packed weights with
+// one 1-D bulk copy (TMA engine) per 4-row group, stage the chunk's
+// activation records, and run the decode kernel's expansion and dot products
+// (packed 2-bit digits, masked dp4a) for every pair of the chunk, so each
+// packed weight byte is expanded once per chunk.  Outputs go to
+// y[pair][row]; sums run in a fixed order (bitwise deterministic).
+#include <algorithm>
+
+#include "../../include/tq1.h"
+#include "packed.cuh"
+#include "tq1_device.cuh"
+#include "tq1_internal.h"
+
+namespace tq1 {
+
+namespace {
+
+using namespace packed;
+
+constexpr int kMThreads = 256;
+constexpr int kMWarps = kMThreads / 32;
+constexpr int kChunk = 4;        // pairs per task
+constexpr int kMaxRows = 128;    // rows per task
+constexpr int kMaxGroupsM = kMaxRows / kRowsPerTask;
+constexpr uint32_t kSlabBudget = 96 * 1024;
+constexpr size_t kMoeSmemBudget = 112 * 1024;  // two CTAs per SM
+
+struct MoeArgs {
+  const uint8_t* w;      // expert 0's first weight block
+  const uint8_t* q8;     // Q8_1 activations [t][k/32]
+  float* y;              // [t * top_k][n]
+  unsigned* status;
+  const int32_t* table;  // compacted routing table (layout in tq1_internal.h)
+  int64_t n;
+  int n_experts, top_k, nb, nkc;
+  int rows;              // rows per task (multiple of 4)
+  int row_blocks;        // row ranges per expert
+  int64_t pairs;         // t * top_k
+  uint32_t slab_bytes;
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(kMThreads, 2) moe_small_kernel(const MoeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nb = a.nb, nkc = a.nkc;
+  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBlockBytes;
+  const uint32_t gstride = group_stride(rowbytes);
+  uint8_t* slab = smem;
+  uint32_t* recs = reinterpret_cast<uint32_t*>(smem + a.slab_bytes);
+  const uint32_t rstride = static_cast<uint32_t>(nb) * kPRec;  // words per pair record
+  float* part = reinterpret_cast<float*>(recs + static_cast<size_t>(kChunk) * rstride);
+  __shared__ __align__(8) uint64_t bars[kMaxGroupsM];
+  __shared__ int s_abort;
+  __shared__ int s_pair[kChunk];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = lane >> 3, s = lane & 7;
+  const int ngroups_max = a.rows / kRowsPerTask;
+  if (tid == 0) {
+    for (int g = 0; g < ngroups_max; ++g) mbar_init(&bars[g], 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();  // the routing table is written by the compaction kernel
+
+  const int32_t* bounds = a.table + 1;
+  const int32_t* active = bounds + (a.n_experts + 1);
+  const int32_t* plist = active + a.n_experts;
+  const int32_t* tstart = plist + a.pairs;
+  const int n_active = a.table[0];
+  const int total = tstart[n_active];
+  const uint64_t policy = l2_evict_first_policy();
+  uint32_t iter = 0;  // tasks done by this CTA: every group barrier completes one phase per task
+
+  for (int task = blockIdx.x; task < total; task += gridDim.x, ++iter) {
+    // Active expert of this task: the last slot whose first task is <= task.
+    int lo = 0, hi = n_active - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tstart[mid] <= task) lo = mid;
+      else hi = mid - 1;
+    }
+    const int e = active[lo];
+    const int local = task - tstart[lo];
+    const int chunk = local / a.row_blocks, rb = local - (local / a.row_blocks) * a.row_blocks;
+    const int cnt = bounds[e + 1] - bounds[e];
+    const int pc = min(kChunk, cnt - chunk * kChunk);  // pairs of this task
+    const int64_t r0 = static_cast<int64_t>(rb) * a.rows;
+    const int rows = static_cast<int>(a.n - r0 < a.rows ? a.n - r0 : a.rows);
+    const int ngroups = (rows + kRowsPerTask - 1) / kRowsPerTask;
+    const uint8_t* wtask = a.w + (static_cast<int64_t>(e) * a.n + r0) * rowbytes;
+    const uint32_t wlow = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(wtask));
+
+    if (tid == 0) {
+      // One bulk copy per 4-row group, from the 16-byte boundary at or below
+      // the group; the bytes past the last 16-byte boundary with plain loads.
+      // Groups past this task's rows complete their phase with no bytes, so
+      // every barrier advances once per task.
+      for (int g = 0; g < ngroups_max; ++g) {
+        if (g < ngroups) {
+          const int grows = min(kRowsPerTask, rows - g * kRowsPerTask);
+          const uint8_t* src = wtask + static_cast<int64_t>(g) * kRowsPerTask * rowbytes;
+          const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
+          const uint32_t tot = delta + static_cast<uint32_t>(grows) * rowbytes;
+          const uint32_t main = tot & ~15u;
+          uint8_t* dst = slab + static_cast<uint32_t>(g) * gstride;
+          for (uint32_t i = main; i < tot; ++i) dst[i] = __ldg(src - delta + i);
+          mbar_arrive_expect_tx(&bars[g], main);
+          if (main) bulk_g2s(dst, src - delta, main, &bars[g], policy);
+        } else {
+          mbar_arrive_expect_tx(&bars[g], 0);
+        }
+      }
+    }
+    if (tid < kChunk) s_pair[tid] = tid < pc ? plist[bounds[e] + chunk * kChunk + tid] : 0;
+    __syncthreads();
+    // Activation records of the task's pairs (token = pair / top_k).
+    {
+      const int nchunks = pc * nb * 8;
+      for (int i = tid; i < nchunks; i += kMThreads) {
+        const int c = i / (nb * 8);
+        const int rem = i - c * nb * 8;
+        const int b = rem >> 3, j = rem & 7;
+        const int64_t token = s_pair[c] / a.top_k;
+        fill_precord_chunk(a.q8 + (token * nb * 8 + b * 8 + j) * kQ8Bytes, recs + c * rstride + b * kPRec, j);
+      }
+    }
+    __syncthreads();
+
+    // Warp tasks: 4 rows x 8 blocks; lane (row r, block s).
+    const int wtasks = ngroups * nkc;
+    bool ok = true;
+    for (int wt = warp; wt < wtasks; wt += kMWarps) {
+      const int g = wt / nkc, kc = wt - (wt / nkc) * nkc;
+      const int row = g * kRowsPerTask + r;
+      const int b = kc * kLanesPerRow + s;
+      if (!mbar_wait(&bars[g], iter & 1u)) {
+        ok = false;
+        break;
+      }
+      float acc[kChunk] = {0.f, 0.f, 0.f, 0.f};
+      if (row < rows && b < nb) {
+        Packed P;
+        const uint32_t off = static_cast<uint32_t>(g) * gstride + ((wlow + static_cast<uint32_t>(g) * kRowsPerTask * rowbytes) & 15u) +
+                             static_cast<uint32_t>(r) * rowbytes + static_cast<uint32_t>(b) * kBlockBytes;
+        expand_pack(slab, off, P);
+#pragma unroll
+        for (int c = 0; c < kChunk; ++c)
+          if (c < pc) acc[c] = packed_dot(P, recs + c * rstride + b * kPRec);
+      }
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        float v = acc[c];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        acc[c] = v;
+      }
+      if (s == 0 && row < rows) {
+#pragma unroll
+        for (int c = 0; c < kChunk; ++c) part[(row * nkc + kc) * kChunk + c] = acc[c];
+      }
+    }
+    if (!ok) s_abort = 1;
+    __syncthreads();
+    if (s_abort) {
+      if (tid == 0) {
+        raise_status(a.status, kStatusTimeout);
+        // Let this task's copies still in flight land (bounded).
+        for (int g = 0; g < ngroups_max; ++g) (void)mbar_wait(&bars[g], iter & 1u);
+      }
+      return;
+    }
+    // y[pair][r0 + row]: sum over the 8-block chunks, in order.
+    for (int i = tid; i < rows * pc; i += kMThreads) {
+      const int c = i / rows, row = i - (i / rows) * rows;
+      float v = 0.0f;
+      for (int kc = 0; kc < nkc; ++kc) v += part[(row * nkc + kc) * kChunk + c];
+      a.y[static_cast<int64_t>(s_pair[c]) * a.n + r0 + row] = v;
+    }
+    __syncthreads();  // slab, records and partials free for the next task
+  }
+}
+
+// Rows per task and row blocks per expert: enough tasks for about two per
+// CTA slot when every routed pair lands on its own expert, within the shared
+// memory budget (two CTAs per SM).
+bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoePlan* plan) {
+  const DeviceInfo& di = device_info();
+  const int nb = static_cast<int>(k / kQK);
+  const int nkc = (nb + kLanesPerRow - 1) / kLanesPerRow;
+  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBlockBytes;
+  const int64_t chunks = std::min<int64_t>(pairs, n_experts + pairs / kChunk);
+  const int64_t want_tasks = 2 * static_cast<int64_t>(std::max(1, di.num_sms));
+  int64_t rows = (n * std::max<int64_t>(chunks, 1) + want_tasks - 1) / want_tasks;
+  rows = std::max<int64_t>(16, std::min<int64_t>(kMaxRows, rows));
+  const int64_t fit = kRowsPerTask * static_cast<int64_t>(kSlabBudget / group_stride(rowbytes));
+  rows = std::min(rows, fit);
+  rows = (rows / kRowsPerTask) * kRowsPerTask;
+  if (rows < kRowsPerTask) return false;
+  const size_t smem = static_cast<size_t>(rows / kRowsPerTask) * group_stride(rowbytes) +
+                      static_cast<size_t>(kChunk) * nb * kPRec * 4 + static_cast<size_t>(rows) * nkc * kChunk * 4;
+  if (smem > kMoeSmemBudget) return false;
+  plan->chunk = kChunk;
+  plan->rows = static_cast<int>(rows);
+  plan->row_blocks = static_cast<int>((n + rows - 1) / rows);
+  return true;
+}
+
+int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
+                     int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
+                     unsigned* status) {
+  const DeviceInfo& di = device_info();
+  MoeArgs a = {};
+  a.w = w;
+  a.q8 = q8;
+  a.y = y;
+  a.status = status;
+  a.table = ws;
+  a.n = n;
+  a.n_experts = static_cast<int>(n_experts);
+  a.top_k = static_cast<int>(top_k);
+  a.nb = static_cast<int>(k / kQK);
+  a.nkc = (a.nb + kLanesPerRow - 1) / kLanesPerRow;
+  a.rows = plan.rows;
+  a.row_blocks = plan.row_blocks;
+  a.pairs = pairs;
+  const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * kBlockBytes;
+  a.slab_bytes = static_cast<uint32_t>(plan.rows / kRowsPerTask) * group_stride(rowbytes);
+  const size_t smem = a.slab_bytes + static_cast<size_t>(kChunk) * a.nb * kPRec * 4 +
+                      static_cast<size_t>(plan.rows) * a.nkc * kChunk * 4;
+  static bool configured[64] = {};
+  if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
+  if (!configured[di.device]) {
+    if (!cuda_ok(cudaFuncSetAttribute(moe_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kMoeSmemBudget))))
+      return TQ1_ERR_CUDA;
+    configured[di.device] = true;
+  }
+  // Upper bound on the tasks: every pair on its own expert.
+  const int64_t max_tasks = std::min<int64_t>(pairs, n_experts) * plan.row_blocks +
+                            (pairs / kChunk) * plan.row_blocks;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(2 * di.num_sms, max_tasks));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kMThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, moe_small_kernel, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+}
+
+}  // namespace tq1

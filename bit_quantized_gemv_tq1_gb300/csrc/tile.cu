@@ -87,18 +87,19 @@ template <int TOK>
 struct TileCfg {
   static constexpr int N = 2 * TOK;                      // B rows: hi of TOK tokens, then lo
   static constexpr uint32_t kBTile = N * 128;            // bytes per stage
-  // A stages live in tensor memory, B stages in shared memory, each ring as
-  // deep as its memory allows (multiples of 4: one slot column per group).
-  static constexpr int kStagesA = TOK <= 32 ? 12 : 8;
-  static constexpr int kStagesB = TOK <= 32 ? 12 : 8;
-  static_assert(kStagesA % 4 == 0 && kStagesB % 4 == 0, "stage rings must be multiples of the 4 A warp groups");
+  // Stage ring: the A half of a slot lives in tensor memory, the B half in
+  // shared memory; one full barrier per half, one empty barrier per slot
+  // (a single MMA commit frees both).  Its length is a multiple of 4, so a
+  // slot only ever holds stages of one A warp group.
+  static constexpr int kStages = TOK <= 32 ? 12 : 8;
+  static_assert(kStages % 4 == 0, "stage ring must be a multiple of the 4 A warp groups");
   static constexpr int kAccCols = N < 32 ? 32 : N;       // TMEM columns per accumulator
   static constexpr int kA0 = 2 * kAccCols;               // first TMEM column of the A stages
   static constexpr int kTmemCols = 512;
-  static_assert(kA0 + kStagesA * 32 <= kTmemCols, "tensor memory budget");
+  static_assert(kA0 + kStages * 32 <= kTmemCols, "tensor memory budget");
   static constexpr bool kSplitOk = TOK <= 32;            // split-K partials fit the B ring
-  static_assert(!kSplitOk || kStagesB * kBTile >= kTileRows * TOK * 4, "split-K partials");
-  static constexpr uint32_t kOffW = kStagesB * kBTile;
+  static_assert(!kSplitOk || kStages * kBTile >= kTileRows * TOK * 4, "split-K partials");
+  static constexpr uint32_t kOffW = kStages * kBTile;
   static constexpr uint32_t kSmem = kOffW + kRW * kWRawBytes + 1024;
   // Instruction descriptor: D fp32, A and B fp16, K-major, N, M = 128.
   static constexpr uint32_t kIdesc =
@@ -148,6 +149,23 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     if (global_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
       return false;
+    }
+  }
+}
+
+// The same bounded wait, spinning: for the single thread that issues the
+// MMAs, whose reaction time sets the pace of the whole pipeline.
+__device__ __forceinline__ bool spin_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((spin & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        return false;
+      }
     }
   }
 }
@@ -445,8 +463,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     tile_kernel(const TileArgs a, const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmb) {
   using C = TileCfg<TOK>;
   extern __shared__ __align__(1024) uint8_t tsmem_raw[];
-  __shared__ __align__(8) uint64_t afull_bar[C::kStagesA], aempty_bar[C::kStagesA];
-  __shared__ __align__(8) uint64_t bfull_bar[C::kStagesB], bempty_bar[C::kStagesB];
+  __shared__ __align__(8) uint64_t afull_bar[C::kStages], bfull_bar[C::kStages], empty_bar[C::kStages];
   __shared__ __align__(8) uint64_t wfull_bar[kRW], wempty_bar[kRW];
   __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
   __shared__ uint32_t s_tmem;
@@ -474,13 +491,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
   };
 
   if (tid == 0) {
-    for (int i = 0; i < C::kStagesA; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&afull_bar[i], 4);  // the 4 warps of the stage's A group
-      mbar_init(&aempty_bar[i], 1);
-    }
-    for (int i = 0; i < C::kStagesB; ++i) {
-      mbar_init(&bfull_bar[i], 1);
-      mbar_init(&bempty_bar[i], 1);
+      mbar_init(&bfull_bar[i], 1);  // the B copy's transaction count
+      mbar_init(&empty_bar[i], 1);  // the MMA commit
     }
     for (int i = 0; i < kRW; ++i) {
       mbar_init(&wfull_bar[i], 1);
@@ -546,8 +560,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint32_t m = static_cast<uint32_t>(u * nst + stage_of(bi, q, nblk));
-          const uint32_t slot = m % C::kStagesA;
-          if (!warp_wait(&aempty_bar[slot], ((m / C::kStagesA) & 1u) ^ 1u, abort_flag)) {
+          const uint32_t slot = m % C::kStages;
+          if (!warp_wait(&empty_bar[slot], ((m / C::kStages) & 1u) ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -616,23 +630,22 @@ __global__ void __launch_bounds__(kTThreads, 1)
         const uint32_t dt = tmem + static_cast<uint32_t>(acc * C::kAccCols);
         for (int st = 0; st < nst; ++st) {
           const uint32_t m = static_cast<uint32_t>(u * nst + st);
-          const uint32_t sa = m % C::kStagesA, pa = (m / C::kStagesA) & 1u;
-          const uint32_t sbs = m % C::kStagesB, pb = (m / C::kStagesB) & 1u;
-          if (!wait_or_abort(&afull_bar[sa], pa, abort_flag) || !wait_or_abort(&bfull_bar[sbs], pb, abort_flag)) {
+          const uint32_t slot = m % C::kStages, ph = (m / C::kStages) & 1u;
+          if (!spin_wait_or_abort(&afull_bar[slot], ph, abort_flag) ||
+              !spin_wait_or_abort(&bfull_bar[slot], ph, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t at = tmem + C::kA0 + sa * 32u;
-          const uint32_t sb = sbase + sbs * C::kBTile;
+          const uint32_t at = tmem + C::kA0 + slot * 32u;
+          const uint32_t sb = sbase + slot * C::kBTile;
 #pragma unroll
           for (int ks = 0; ks < kStageK / 16; ++ks)
             umma_ts(dt, at + 8u * ks, umma_desc_sw128(sb + 32u * ks), C::kIdesc, (st > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&aempty_bar[sa]);
-          umma_commit(&bempty_bar[sbs]);
+          umma_commit(&empty_bar[slot]);
           issued = true;
-          last_bar = &bempty_bar[sbs];
-          last_ph = pb;
+          last_bar = &empty_bar[slot];
+          last_ph = ph;
         }
         if (!ok) break;
         umma_commit(&accf_bar[acc]);
@@ -688,8 +701,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
           for (int q = 0; q < 4 && ok; ++q)
             for (int gg = 0; gg < groups; ++gg) {
               const uint32_t m = static_cast<uint32_t>(u * nst + 16 * i + q * groups + gg);
-              const uint32_t sbs = m % C::kStagesB, pb = (m / C::kStagesB) & 1u;
-              if (!wait_or_abort(&bempty_bar[sbs], pb ^ 1u, abort_flag)) {
+              const uint32_t sbs = m % C::kStages, pb = (m / C::kStages) & 1u;
+              if (!wait_or_abort(&empty_bar[sbs], pb ^ 1u, abort_flag)) {
                 ok = false;
                 break;
               }

@@ -35,9 +35,8 @@ int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
                      unsigned* status);
 
-// Expert-routed mat-vec over a compacted routing table in `ws`.
-int launch_moe_compact(const int32_t* ids, int64_t t, int64_t top_k, int64_t n_experts, int32_t* ws,
-                       cudaStream_t s, unsigned* status);
+// Expert-routed mat-vec over a compacted routing table in `ws` (general
+// dp4a kernel).
 int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float* y, int64_t n, int64_t k,
                   int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status);
 
@@ -47,11 +46,33 @@ int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_
                 unsigned* status);
 
 // Workspace layout of the routing table (int32 words):
-//   [0]                 n_active
-//   [1, 1+E+1)          expert bounds (exclusive prefix sum of counts)
-//   [E+2, E+2+E)        active expert ids, ascending
-//   [2E+2, 2E+2+P)      pair indices (token*top_k + slot) sorted by expert,
-//                       stable within an expert
-inline size_t moe_ws_words(int64_t n_experts, int64_t pairs) { return 1 + (size_t)(n_experts + 1) + n_experts + pairs; }
+//   [0]                   n_active
+//   [1, 1+E+1)            expert bounds (exclusive prefix sum of counts)
+//   [E+2, E+2+E)          active expert ids, ascending
+//   [2E+2, 2E+2+P)        pair indices (token*top_k + slot) sorted by expert,
+//                         stable within an expert
+//   [2E+2+P, 3E+3+P)      task offsets of the active experts (exclusive
+//                         prefix sum of ceil(count / chunk) * row_blocks;
+//                         entry n_active holds the total)
+inline size_t moe_ws_words(int64_t n_experts, int64_t pairs) {
+  return 1 + (size_t)(n_experts + 1) + n_experts + pairs + (n_experts + 1);
+}
+
+// Routing-table compaction; `chunk` (pairs per task) and `row_blocks`
+// (row ranges per expert) define the task offsets of the expert-routed
+// decode kernel.
+int launch_moe_compact(const int32_t* ids, int64_t t, int64_t top_k, int64_t n_experts, int chunk, int row_blocks,
+                       int32_t* ws, cudaStream_t s, unsigned* status);
+
+// Expert-routed decode kernel over the compacted table.  Returns
+// TQ1_ERR_UNSUPPORTED (launching nothing) when the shape does not fit its
+// staging; `plan` gives the chunk and row-block counts the compaction needs.
+struct MoePlan {
+  int chunk, rows, row_blocks;
+};
+bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoePlan* plan);
+int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
+                     int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
+                     unsigned* status);
 
 }  // namespace tq1

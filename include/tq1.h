@@ -143,7 +143,7 @@ int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, con
  * device memory (inside a stream capture, under a fixed memory budget, in a
  * latency-critical loop, or from plain C with no allocator at hand).  The
  * routing table lives in a fixed array that is part of the library image
- * (about 72 KiB on every GPU that loads the library, held until exit).
+ * (about 76 KiB on every GPU that loads the library, held until exit).
  * Limits: n_experts <= 1024 and t * top_k <= 16384; larger calls return
  * TQ1_ERR_WORKSPACE and launch nothing.  Same arguments, layouts, results
  * and errors as tq1_mmv_id otherwise.
