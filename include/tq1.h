@@ -24,9 +24,11 @@
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller and must be
- *     16-byte aligned (TQ1_ERR_ALIGN otherwise).  The library allocates no
- *     memory and never synchronises; work is enqueued on `stream` (a
- *     cudaStream_t, NULL for the legacy default stream) on the current device.
+ *     16-byte aligned (TQ1_ERR_ALIGN otherwise).  The library never
+ *     synchronises; work is enqueued on `stream` (a cudaStream_t, NULL for
+ *     the legacy default stream) on the current device.  The only memory it
+ *     takes is tq1_mmv's scratch for t >= 11, stream-ordered from its own
+ *     memory pool (see tq1_mmv).
  *   - Arguments are checked on the host before anything is launched; a
  *     failed check returns its negative code and launches nothing.
  *   - Shapes: k must be a positive multiple of 256; n, t >= 0 (0 means there
@@ -97,9 +99,14 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
  * w = d_w * trit and x = d_a * q, accumulated as
  *   sum_blocks d_w * sum_{chunks j} d_a[j] * I_j,   I_j = sum (trit * q) (exact int32)
  * in fp32.  blocks [n][k/256] TQ1_0, q8 [t][k/32] Q8_1, y fp32 [t][n].
- * t <= 32 runs the byte-major dp4a kernel laddered at 1/2/4/8/16/32 columns;
- * 32 < t < 256 runs it on 32-column slices; t >= 256 runs the tensor-core
- * prefill kernel.  Deterministic: repeated calls give identical bits.
+ * t <= 10 runs the byte-major dp4a kernels laddered at 1/2/4/8/16 columns;
+ * t >= 11 (prefill included) runs the tensor-core path: a prep kernel splits
+ * the activations into exact fp16 hi/lo parts in scratch taken from a
+ * library-owned stream-ordered memory pool (cudaMallocFromPoolAsync /
+ * cudaFreeAsync on `stream`: no synchronisation, capturable), then a tcgen05
+ * kernel contracts them with the expanded weights (k a multiple of 2048;
+ * other k stay on the dp4a kernels).  Deterministic: repeated calls give
+ * identical bits.
  * Source: PrismML-Eng/llama.cpp issue #139, "Proposed approach" (a dedicated
  * whole-block kernel that iterates over packed bytes); laddered column
  * counts: Neroued/ninfer issue #293.
