@@ -72,34 +72,35 @@ namespace tq1 {
 namespace {
 
 constexpr int kTileRows = 128;  // weight rows per tile = TMEM lanes
-constexpr int kStageK = 64;     // K per stage
+constexpr int kStageK = 64;     // K per MMA stage (a quarter of a 256-block)
 constexpr int kWinBytes = 80;   // raw weight window per row and block (16-byte aligned)
 constexpr uint32_t kWRawBytes = kTileRows * kWinBytes;
+constexpr int kGroups = 3;      // A warp groups = tensor-memory block slots
 constexpr int kWSlotsPerGroup = 2;
-constexpr int kRW = 4 * kWSlotsPerGroup;  // raw weight ring: two blocks per A warp group
-constexpr int kAWarps = 16, kEWarps = 4;
+constexpr int kRW = kGroups * kWSlotsPerGroup;  // raw weight ring: two blocks per A group
+constexpr int kAWarps = 4 * kGroups, kEWarps = 4;
 constexpr int kEWarp0 = kAWarps, kMWarp = kEWarp0 + kEWarps, kPWarpW = kMWarp + 1, kPWarpB = kMWarp + 2;
 constexpr int kTThreads = (kPWarpB + 1) * 32;
 constexpr int kMaxSplit = 8;
 constexpr int kPrepThreads = 256;
+constexpr int kBlockCols = 4 * 32;  // TMEM columns of one block of A (4 quarters x 32)
 
 template <int TOK>
 struct TileCfg {
   static constexpr int N = 2 * TOK;                      // B rows: hi of TOK tokens, then lo
-  static constexpr uint32_t kBTile = N * 128;            // bytes per stage
-  // Stage ring: the A half of a slot lives in tensor memory, the B half in
-  // shared memory; one full barrier per half, one empty barrier per slot
-  // (a single MMA commit frees both).  Its length is a multiple of 4, so a
-  // slot only ever holds stages of one A warp group.
-  static constexpr int kStages = TOK <= 32 ? 12 : 8;
-  static_assert(kStages % 4 == 0, "stage ring must be a multiple of the 4 A warp groups");
-  static constexpr int kAccCols = N < 32 ? 32 : N;       // TMEM columns per accumulator
-  static constexpr int kA0 = 2 * kAccCols;               // first TMEM column of the A stages
+  static constexpr uint32_t kBTile = N * 128;            // bytes of one quarter (K = 64) of B
+  static constexpr uint32_t kBBlock = 4 * kBTile;        // bytes of one block of B
+  // A block slots live in tensor memory (one per A warp group, so a slot has
+  // a single owner), B block slots in shared memory (a plain ring).
+  static constexpr int kRB = TOK >= 64 ? 2 : 3;
+  static constexpr int kAccs = TOK >= 64 ? 1 : 2;        // TMEM accumulators
+  static constexpr int kAccCols = N < 32 ? 32 : N;
+  static constexpr int kA0 = kAccs * kAccCols;           // first TMEM column of the A slots
   static constexpr int kTmemCols = 512;
-  static_assert(kA0 + kStages * 32 <= kTmemCols, "tensor memory budget");
+  static_assert(kA0 + kGroups * kBlockCols <= kTmemCols, "tensor memory budget");
   static constexpr bool kSplitOk = TOK <= 32;            // split-K partials fit the B ring
-  static_assert(!kSplitOk || kStages * kBTile >= kTileRows * TOK * 4, "split-K partials");
-  static constexpr uint32_t kOffW = kStages * kBTile;
+  static_assert(!kSplitOk || kRB * kBBlock >= kTileRows * TOK * 4, "split-K partials");
+  static constexpr uint32_t kOffW = kRB * kBBlock;
   static constexpr uint32_t kSmem = kOffW + kRW * kWRawBytes + 1024;
   // Instruction descriptor: D fp32, A and B fp16, K-major, N, M = 128.
   static constexpr uint32_t kIdesc =
@@ -394,15 +395,6 @@ __device__ __forceinline__ void acts_to_hilo(uint32_t q0, uint32_t q1, __half2 d
 }
 
 
-// Position, in a tile's K order, of quarter q of the tile's block bi (of
-// nblk): blocks go in rounds of four, one per A warp group; within a round
-// the stages are taken quarter by quarter, group by group.
-__device__ __forceinline__ int stage_of(int bi, int q, int nblk) {
-  const int i = bi >> 2, g = bi & 3;
-  const int groups = min(4, nblk - 4 * i);
-  return 16 * i + q * groups + g;
-}
-
 }  // namespace
 
 // Q8_1 activations -> B operand: fp16 hi rows [t_pad][k], lo rows
@@ -463,7 +455,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
     tile_kernel(const TileArgs a, const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmb) {
   using C = TileCfg<TOK>;
   extern __shared__ __align__(1024) uint8_t tsmem_raw[];
-  __shared__ __align__(8) uint64_t afull_bar[C::kStages], bfull_bar[C::kStages], empty_bar[C::kStages];
+  __shared__ __align__(8) uint64_t afull_bar[kGroups], aempty_bar[kGroups];
+  __shared__ __align__(8) uint64_t bfull_bar[C::kRB], bempty_bar[C::kRB];
   __shared__ __align__(8) uint64_t wfull_bar[kRW], wempty_bar[kRW];
   __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
   __shared__ uint32_t s_tmem;
@@ -474,7 +467,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   uint8_t* sm = tsmem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_addr(sm);
   uint8_t* wraw = sm + C::kOffW;
-  float* red = reinterpret_cast<float*>(sm);  // split-K partials reuse the B stages after the last MMA
+  float* red = reinterpret_cast<float*>(sm);  // split-K partials reuse the B ring after the last MMA
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = a.k / kQK;
@@ -484,17 +477,24 @@ __global__ void __launch_bounds__(kTThreads, 1)
   const int kb0 = S > 1 ? (nb * rank) / S : 0;
   const int kb1 = S > 1 ? (nb * (rank + 1)) / S : nb;
   const int nblk = kb1 - kb0;  // blocks per tile (the same for every tile of this CTA)
-  const int nst = 4 * nblk;    // stages per tile
+  // Tile of this CTA's unit u (>= ntiles: no more units).  Block j of the
+  // CTA (counted over all its units) is block j % nblk of unit j / nblk.
   auto unit_tile = [&](int u) -> int {
     if (S > 1) return u == 0 ? static_cast<int>(blockIdx.x / S) : ntiles;
     return static_cast<int>(blockIdx.x) + u * static_cast<int>(gridDim.x);
   };
+  int nunits = 0;
+  while (unit_tile(nunits) < ntiles) ++nunits;
+  const uint32_t nall = static_cast<uint32_t>(nunits * nblk);  // blocks of this CTA
 
   if (tid == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&afull_bar[i], 4);  // the 4 warps of the stage's A group
-      mbar_init(&bfull_bar[i], 1);  // the B copy's transaction count
-      mbar_init(&empty_bar[i], 1);  // the MMA commit
+    for (int i = 0; i < kGroups; ++i) {
+      mbar_init(&afull_bar[i], 4);  // the 4 warps of the slot's A group
+      mbar_init(&aempty_bar[i], 1);
+    }
+    for (int i = 0; i < C::kRB; ++i) {
+      mbar_init(&bfull_bar[i], 1);
+      mbar_init(&bempty_bar[i], 1);
     }
     for (int i = 0; i < kRW; ++i) {
       mbar_init(&wfull_bar[i], 1);
@@ -520,78 +520,68 @@ __global__ void __launch_bounds__(kTThreads, 1)
 
   if (warp < kAWarps) {
     // ---------------------------------------------------------------- A --
-    const int g = warp >> 2;       // blocks g, g + 4, ... of every tile
+    // Group g expands blocks j = g, g + 3, ... of the CTA into A slot g.
+    const int g = warp >> 2;
     const int quarter = warp & 3;  // TMEM lane quarter = rows 32*quarter ..
     const int rl = (quarter << 5) | lane;
-    uint32_t c = 0;  // this group's blocks so far (raw weight ring position)
-    bool ok = true;
-    for (int u = 0; ok; ++u) {
-      const int tile = unit_tile(u);
-      if (tile >= ntiles) break;
-      for (int bi = g; bi < nblk; bi += 4, ++c) {
-        const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
-        if (!warp_wait(&wfull_bar[ws], (c / kWSlotsPerGroup) & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint32_t W[20];
-        const uint4* src = reinterpret_cast<const uint4*>(wraw + ws * kWRawBytes + rl * kWinBytes);
+    const uint32_t tslot = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kA0 + g * kBlockCols;
+    uint32_t c = 0;  // this group's blocks so far
+    for (uint32_t j = g; j < nall; j += kGroups, ++c) {
+      const int bi = static_cast<int>(j % nblk);
+      const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
+      if (!warp_wait(&wfull_bar[ws], (c / kWSlotsPerGroup) & 1u, abort_flag)) break;
+      uint32_t W[20];
+      const uint4* src = reinterpret_cast<const uint4*>(wraw + ws * kWRawBytes + rl * kWinBytes);
 #pragma unroll
-        for (int cc = 0; cc < 5; ++cc) {
-          const uint4 v = src[cc];
-          W[4 * cc] = v.x;
-          W[4 * cc + 1] = v.y;
-          W[4 * cc + 2] = v.z;
-          W[4 * cc + 3] = v.w;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty_bar[ws]);
-        const uint32_t off = static_cast<uint32_t>((kb0 + bi) * kBlockBytes) & 15u;
-        const uint32_t sh = (off & 2u) * 8u;
-        uint32_t wv[13], h;
-        switch (off >> 2) {
-          case 0: realign<0>(W, sh, wv, h); break;
-          case 1: realign<1>(W, sh, wv, h); break;
-          case 2: realign<2>(W, sh, wv, h); break;
-          default: realign<3>(W, sh, wv, h); break;
-        }
-        const uint32_t tlo = h ^ 0x8000u;  // bytes 0-1: -d_w, bytes 2-3: 0
-        const uint32_t thi = h;            // bytes 4-5: +d_w
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t m = static_cast<uint32_t>(u * nst + stage_of(bi, q, nblk));
-          const uint32_t slot = m % C::kStages;
-          if (!warp_wait(&empty_bar[slot], ((m / C::kStages) & 1u) ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          uint32_t out[32];
-          if (q == 0) expand_quarter<0>(wv, tlo, thi, out);
-          else if (q == 1) expand_quarter<1>(wv, tlo, thi, out);
-          else if (q == 2) expand_quarter<2>(wv, tlo, thi, out);
-          else expand_quarter<3>(wv, tlo, thi, out);
-          tmem_st32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kA0 + slot * 32u, out);
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&afull_bar[slot]);
-        }
-        if (!ok) break;
+      for (int cc = 0; cc < 5; ++cc) {
+        const uint4 v = src[cc];
+        W[4 * cc] = v.x;
+        W[4 * cc + 1] = v.y;
+        W[4 * cc + 2] = v.z;
+        W[4 * cc + 3] = v.w;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wempty_bar[ws]);
+      const uint32_t off = static_cast<uint32_t>((kb0 + bi) * kBlockBytes) & 15u;
+      const uint32_t sh = (off & 2u) * 8u;
+      uint32_t wv[13], h;
+      switch (off >> 2) {
+        case 0: realign<0>(W, sh, wv, h); break;
+        case 1: realign<1>(W, sh, wv, h); break;
+        case 2: realign<2>(W, sh, wv, h); break;
+        default: realign<3>(W, sh, wv, h); break;
+      }
+      const uint32_t tlo = h ^ 0x8000u;  // bytes 0-1: -d_w, bytes 2-3: 0
+      const uint32_t thi = h;            // bytes 4-5: +d_w
+      // The slot is free once the MMAs of this group's previous block are done.
+      if (!warp_wait(&aempty_bar[g], (c & 1u) ^ 1u, abort_flag)) break;
+      tc_fence_after();
+      uint32_t out[32];
+      expand_quarter<0>(wv, tlo, thi, out);
+      tmem_st32(tslot + 0 * 32, out);
+      expand_quarter<1>(wv, tlo, thi, out);
+      tmem_st32(tslot + 1 * 32, out);
+      expand_quarter<2>(wv, tlo, thi, out);
+      tmem_st32(tslot + 2 * 32, out);
+      expand_quarter<3>(wv, tlo, thi, out);
+      tmem_st32(tslot + 3 * 32, out);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull_bar[g]);
     }
   } else if (warp < kMWarp) {
     // --------------------------------------------------------- epilogue --
     const int quarter = warp & 3;  // TMEM lane quarter this warp may read
     const int rl = quarter * 32 + lane;
     pdl_wait();  // the scales are written by the prep kernel
-    for (int u = 0;; ++u) {
+    for (int u = 0; u < nunits; ++u) {
       const int tile = unit_tile(u);
-      if (tile >= ntiles) break;
       const int row = (tile / a.tiles_n) * kTileRows + rl;
       const int tok0 = (tile % a.tiles_n) * TOK;
-      const int acc = u & 1;
-      if (!warp_wait(&accf_bar[acc], (u >> 1) & 1u, abort_flag)) break;
+      const int acc = u % C::kAccs;
+      const uint32_t aph = static_cast<uint32_t>(u / C::kAccs) & 1u;
+      if (!warp_wait(&accf_bar[acc], aph, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
 #pragma unroll 1
@@ -621,31 +611,35 @@ __global__ void __launch_bounds__(kTThreads, 1)
       bool issued = false, ok = true;
       uint64_t* last_bar = nullptr;
       uint32_t last_ph = 0;
-      for (int u = 0; ok; ++u) {
-        const int tile = unit_tile(u);
-        if (tile >= ntiles) break;
-        const int acc = u & 1;
-        if (!wait_or_abort(&acce_bar[acc], ((u >> 1) & 1u) ^ 1u, abort_flag)) break;
+      uint32_t j = 0;
+      for (int u = 0; u < nunits && ok; ++u) {
+        const int acc = u % C::kAccs;
+        const uint32_t aph = static_cast<uint32_t>(u / C::kAccs) & 1u;
+        if (!spin_wait_or_abort(&acce_bar[acc], aph ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t dt = tmem + static_cast<uint32_t>(acc * C::kAccCols);
-        for (int st = 0; st < nst; ++st) {
-          const uint32_t m = static_cast<uint32_t>(u * nst + st);
-          const uint32_t slot = m % C::kStages, ph = (m / C::kStages) & 1u;
-          if (!spin_wait_or_abort(&afull_bar[slot], ph, abort_flag) ||
-              !spin_wait_or_abort(&bfull_bar[slot], ph, abort_flag)) {
+        for (int bi = 0; bi < nblk; ++bi, ++j) {
+          const uint32_t ga = j % kGroups, pa = (j / kGroups) & 1u;
+          const uint32_t rb = j % C::kRB, pb = (j / C::kRB) & 1u;
+          if (!spin_wait_or_abort(&afull_bar[ga], pa, abort_flag) ||
+              !spin_wait_or_abort(&bfull_bar[rb], pb, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t at = tmem + C::kA0 + slot * 32u;
-          const uint32_t sb = sbase + slot * C::kBTile;
+          const uint32_t at = tmem + C::kA0 + ga * kBlockCols;
+          const uint32_t sb = sbase + rb * C::kBBlock;
 #pragma unroll
-          for (int ks = 0; ks < kStageK / 16; ++ks)
-            umma_ts(dt, at + 8u * ks, umma_desc_sw128(sb + 32u * ks), C::kIdesc, (st > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&empty_bar[slot]);
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int ks = 0; ks < kStageK / 16; ++ks)
+              umma_ts(dt, at + 32u * q + 8u * ks, umma_desc_sw128(sb + q * C::kBTile + 32u * ks), C::kIdesc,
+                      (bi > 0 || q > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&aempty_bar[ga]);
+          umma_commit(&bempty_bar[rb]);
           issued = true;
-          last_bar = &empty_bar[slot];
-          last_ph = ph;
+          last_bar = &bempty_bar[rb];
+          last_ph = pb;
         }
         if (!ok) break;
         umma_commit(&accf_bar[acc]);
@@ -657,29 +651,21 @@ __global__ void __launch_bounds__(kTThreads, 1)
   } else if (warp == kPWarpW) {
     // ---------------------------------------------------- weight copies --
     if (lane == 0) {
-      uint32_t cnt[4] = {0, 0, 0, 0};
+      uint32_t cnt[kGroups] = {};
       int last_slot = -1;
       uint32_t last_ph = 0;
-      for (int u = 0;; ++u) {
-        const int tile = unit_tile(u);
-        if (tile >= ntiles) break;
-        const int row0 = (tile / a.tiles_n) * kTileRows;
-        bool ok = true;
-        for (int bi = 0; bi < nblk; ++bi) {
-          const int g = bi & 3;
-          const uint32_t c = cnt[g]++;
-          const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
-          const uint32_t ph = (c / kWSlotsPerGroup) & 1u;
-          if (!wait_or_abort(&wempty_bar[ws], ph ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&wfull_bar[ws], kWRawBytes);
-          tma_load_2d(wraw + ws * kWRawBytes, &tmw, ((kb0 + bi) * kBlockBytes) & ~15, row0, &wfull_bar[ws]);
-          last_slot = static_cast<int>(ws);
-          last_ph = ph;
-        }
-        if (!ok) break;
+      for (uint32_t j = 0; j < nall; ++j) {
+        const int g = static_cast<int>(j % kGroups);
+        const int bi = static_cast<int>(j % nblk);
+        const int row0 = (unit_tile(static_cast<int>(j / nblk)) / a.tiles_n) * kTileRows;
+        const uint32_t c = cnt[g]++;
+        const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
+        const uint32_t ph = (c / kWSlotsPerGroup) & 1u;
+        if (!wait_or_abort(&wempty_bar[ws], ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(&wfull_bar[ws], kWRawBytes);
+        tma_load_2d(wraw + ws * kWRawBytes, &tmw, ((kb0 + bi) * kBlockBytes) & ~15, row0, &wfull_bar[ws]);
+        last_slot = static_cast<int>(ws);
+        last_ph = ph;
       }
       // Copies still in flight must land before the CTA leaves.
       if (*abort_flag && last_slot >= 0) (void)mbar_wait(&wfull_bar[last_slot], last_ph);
@@ -690,32 +676,21 @@ __global__ void __launch_bounds__(kTThreads, 1)
       pdl_wait();  // the B operand is written by the prep kernel
       int last_slot = -1;
       uint32_t last_ph = 0;
-      for (int u = 0;; ++u) {
-        const int tile = unit_tile(u);
-        if (tile >= ntiles) break;
-        const int tok0 = (tile % a.tiles_n) * TOK;
-        bool ok = true;
-        // Stages in the MMA's order: rounds of four blocks, quarter by quarter.
-        for (int i = 0; 4 * i < nblk && ok; ++i) {
-          const int groups = min(4, nblk - 4 * i);
-          for (int q = 0; q < 4 && ok; ++q)
-            for (int gg = 0; gg < groups; ++gg) {
-              const uint32_t m = static_cast<uint32_t>(u * nst + 16 * i + q * groups + gg);
-              const uint32_t sbs = m % C::kStages, pb = (m / C::kStages) & 1u;
-              if (!wait_or_abort(&empty_bar[sbs], pb ^ 1u, abort_flag)) {
-                ok = false;
-                break;
-              }
-              const int kx = (kb0 + 4 * i + gg) * kQK + q * kStageK;
-              uint8_t* dst = sm + sbs * C::kBTile;
-              mbar_arrive_expect_tx(&bfull_bar[sbs], C::kBTile);
-              tma_load_2d(dst, &tmb, kx, tok0, &bfull_bar[sbs]);
-              tma_load_2d(dst + TOK * 128, &tmb, kx, a.t_pad + tok0, &bfull_bar[sbs]);
-              last_slot = static_cast<int>(sbs);
-              last_ph = pb;
-            }
+      for (uint32_t j = 0; j < nall; ++j) {
+        const int bi = static_cast<int>(j % nblk);
+        const int tok0 = (unit_tile(static_cast<int>(j / nblk)) % a.tiles_n) * TOK;
+        const uint32_t rb = j % C::kRB, pb = (j / C::kRB) & 1u;
+        if (!wait_or_abort(&bempty_bar[rb], pb ^ 1u, abort_flag)) break;
+        uint8_t* dst = sm + rb * C::kBBlock;
+        mbar_arrive_expect_tx(&bfull_bar[rb], C::kBBlock);
+        const int kx = (kb0 + bi) * kQK;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          tma_load_2d(dst + q * C::kBTile, &tmb, kx + q * kStageK, tok0, &bfull_bar[rb]);
+          tma_load_2d(dst + q * C::kBTile + TOK * 128, &tmb, kx + q * kStageK, a.t_pad + tok0, &bfull_bar[rb]);
         }
-        if (!ok) break;
+        last_slot = static_cast<int>(rb);
+        last_ph = pb;
       }
       if (*abort_flag && last_slot >= 0) (void)mbar_wait(&bfull_bar[last_slot], last_ph);
     }
