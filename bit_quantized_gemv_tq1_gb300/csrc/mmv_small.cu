@@ -55,7 +55,7 @@ template <int C>
 struct SmallCfg;
 template <>
 struct SmallCfg<1> {
-  static constexpr int kThreads = 512;
+  static constexpr int kThreads = 448;  // 14 warps (measured: 3% faster than 16 at N=5120, K=6144)
   static constexpr int kHeld = 2;
   static constexpr uint32_t kSlab = 96 * 1024;
 };
@@ -105,7 +105,6 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
   const uint32_t rstride = static_cast<uint32_t>(nb) * kPRec;  // words per column
   float* part = reinterpret_cast<float*>(recs + static_cast<size_t>(C) * rstride);
   uint64_t* bars = reinterpret_cast<uint64_t*>(part + ((static_cast<size_t>(a.rows_cta) * nkc * C + 1) & ~size_t(1)));
-  __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = lane >> 3, s = lane & 7;
@@ -160,8 +159,8 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
   };
 
   if (tid == 0) {
-    s_abort = 0;
-    for (int g = 0; g < kMaxGroups; ++g) mbar_init(&bars[g], 1);
+    const int nbars = min(kMaxGroups, (a.rows_round + kRowsPerTask - 1) / kRowsPerTask);
+    for (int g = 0; g < nbars; ++g) mbar_init(&bars[g], 1);
     fence_mbar_init();
     if (nrounds > 0) issue_round(0);  // weights: before waiting on the previous kernel
   }
@@ -185,17 +184,17 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
   pdl_wait();
 
   // Phase 2: activation records of the C columns, then the dot products.
+  // A failed wait anywhere in the CTA aborts it; the vote rides on the
+  // barrier that publishes the records (a flag in shared memory read after
+  // the barrier measurably slowed the dot phase).
   {
-    const int nchunks = a.t * nb * 8;
+    const int per_col = nb * 8, nchunks = a.t * per_col;
     for (int i = tid; i < nchunks; i += kThreads) {
-      const int c = i / (nb * 8);
-      const int rem = i - c * nb * 8;
-      const int b = rem >> 3, j = rem & 7;
-      fill_precord_chunk(a.q8 + static_cast<int64_t>(i) * kQ8Bytes, recs + c * rstride + b * kPRec, j);
+      const int c = i / per_col, rem = i - c * per_col;
+      fill_precord_chunk(a.q8 + static_cast<int64_t>(i) * kQ8Bytes, recs + c * rstride + (rem >> 3) * kPRec, rem & 7);
     }
   }
-  if (!ok) s_abort = 1;
-  __syncthreads();
+  bool abort = __syncthreads_or(!ok) != 0;
 
   // Reduce a task's per-lane partials over the row's 8 lanes and store them.
   auto finish_task = [&](const TaskPos& T, float (&acc)[C]) {
@@ -225,14 +224,15 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
     finish_task(T, acc);
   };
 
-  if (!s_abort) {
+  if (!abort) {
 #pragma unroll
     for (int h = 0; h < kHeld; ++h) {
       const int task = warp + h * kWarps;
       if (task < ntasks0) dot_task(task_pos(0, task), held[h]);
     }
   }
-  for (int rd = 0; rd < nrounds && !s_abort; ++rd) {
+  int rd = 0;
+  for (; rd < nrounds && !abort; ++rd) {
     const int rs = rd * a.rows_round;
     const int ngroups = (min(a.rows_round, rows - rs) + kRowsPerTask - 1) / kRowsPerTask;
     const int ntasks = ngroups * nkc;
@@ -248,36 +248,29 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
       if (T.live) expand_pack(slab, T.off, P);
       dot_task(T, P);
     }
-    if (!ok) {
-      raise_status(a.status, kStatusTimeout);
-      s_abort = 1;
-    }
-    __syncthreads();  // slab free, all tasks of the round done
-    if (s_abort) {
-      // Let this round's copies that are still in flight land (bounded)
-      // before the CTA gives its shared memory back.
-      if (tid == 0)
-        for (int g = 0; g < ngroups; ++g) (void)mbar_wait(&bars[g], parity);
-      return;
-    }
+    abort = __syncthreads_or(!ok) != 0;  // slab free, all tasks of the round done
+    if (abort) break;
     if (tid == 0 && rd + 1 < nrounds) issue_round(rd + 1);
   }
-  if (s_abort) {
+  if (abort) {
+    // Let the copies of the round that failed (still in flight, perhaps)
+    // land, bounded, before the CTA gives its shared memory back.
     if (tid == 0) {
       raise_status(a.status, kStatusTimeout);
-      const int ngroups = (min(a.rows_round, rows) + kRowsPerTask - 1) / kRowsPerTask;
-      for (int g = 0; g < ngroups; ++g) (void)mbar_wait(&bars[g], 0);
+      const int rdw = min(rd, nrounds - 1);
+      const int ngroups = (min(a.rows_round, rows - rdw * a.rows_round) + kRowsPerTask - 1) / kRowsPerTask;
+      for (int g = 0; g < ngroups; ++g) (void)mbar_wait(&bars[g], static_cast<uint32_t>(rdw & 1));
     }
     return;
   }
 
   // y[c][r0 + row] = sum over block chunks, in order.
-  for (int i = tid; i < rows * a.t; i += kThreads) {
-    const int c = i / rows, row = i - (i / rows) * rows;
-    float v = 0.0f;
-    for (int kc = 0; kc < nkc; ++kc) v += part[(static_cast<size_t>(row) * nkc + kc) * C + c];
-    a.y[static_cast<int64_t>(c) * a.n + r0 + row] = v;
-  }
+  for (int c = 0; c < a.t; ++c)
+    for (int row = tid; row < rows; row += kThreads) {
+      float v = 0.0f;
+      for (int kc = 0; kc < nkc; ++kc) v += part[(static_cast<size_t>(row) * nkc + kc) * C + c];
+      a.y[static_cast<int64_t>(c) * a.n + r0 + row] = v;
+    }
 }
 
 template <int C>
@@ -302,6 +295,10 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
     const size_t lim = di.max_smem_optin - fa.sharedSizeBytes;
     if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(lim))))
+      return TQ1_ERR_CUDA;
+    // Two CTAs of consecutive calls share an SM: ask for the largest
+    // shared-memory carveout so the L1 split never limits residency.
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
       return TQ1_ERR_CUDA;
     max_dyn[di.device] = lim;
   }

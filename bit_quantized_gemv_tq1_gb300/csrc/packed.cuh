@@ -42,6 +42,31 @@ struct Packed {
   float dw;
 };
 
+// P_k(b) = floor(b * 3^k / 256) for the four bytes of `x` and k = 1..ND, as
+// u8x4 words (P[0] = 0).  b * 3^5 < 2^16, so bytes 0,2 and bytes 1,3 are
+// multiplied in 16-bit lanes of two words without interacting and a byte
+// permute gathers the high byte of every lane.  The first three powers are
+// shift-and-add chains (integer ALU pipe), the last two multiplies (FMA-heavy
+// pipe), which keeps the two integer pipes balanced.
+template <int ND>
+__device__ __forceinline__ void pow3_floors(uint32_t x, uint32_t (&P)[ND + 1]) {
+  const uint32_t L0 = x & 0x00FF00FFu;
+  const uint32_t H0 = __byte_perm(x, 0u, 0x4341u);
+  uint32_t L = L0, H = H0;
+  P[0] = 0;
+#pragma unroll
+  for (int k = 1; k <= ND; ++k) {
+    if (k <= 3) {
+      L = times3(L);
+      H = times3(H);
+    } else {
+      L = L0 * pow3(k);
+      H = H0 * pow3(k);
+    }
+    P[k] = __byte_perm(L, H, 0x7351u);
+  }
+}
+
 // Expand the block at byte offset `off` (even) of shared memory `slab` into
 // packed digits.  Element order (PrismML-Eng/llama.cpp issue #139, "Current
 // behavior", continued over the last 16 qs bytes and the 4 qh bytes):
@@ -50,35 +75,46 @@ struct Packed {
 //                   digit 2 / 3  -> chunk 6,         word i / 4 + i
 //                   digit 4      -> chunk 7,         word i
 //   qh word,        digit k      -> chunk 7,         word 4 + k
-__device__ __forceinline__ void expand_pack(const uint8_t* slab, uint32_t off, Packed& P) {
+//
+// The specification's digit k of byte b, ((uint8)(b*3^k)*3) >> 8, equals
+// P_{k+1}(b) - 3 P_k(b) (the carry out of 3 * (b*3^k mod 256)).  A packed
+// register sum_s 4^s * digit_s is therefore an integer combination of the
+// u8x4 words P_k; every byte lane of the result lies in [0, 170], so the
+// combination computed in wrapping 32-bit arithmetic has no carries or
+// borrows between lanes and equals the packed register exactly.  For a qs
+// word of the first 32 bytes, slots 0..3 hold digits 0..3:
+//   d0 + 4 d1 + 16 d2 + 64 d3 = 64 P4 - 11 P1 - 44 P2 - 176 P3
+// and digit 4 (slot 0 of the b register) is P5 - 3 P4.
+__device__ __forceinline__ void expand_pack(const uint8_t* slab, uint32_t off, Packed& Q) {
   const uint32_t* p = reinterpret_cast<const uint32_t*>(slab + (off & ~3u));
   const uint32_t sh = (off & 2u) * 8u;
   uint32_t w[14];
 #pragma unroll
   for (int m = 0; m < 14; ++m) w[m] = p[m];
-  // Chunks 5..7 first (slots 1..3 of the b registers).
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t d[5];
-    expand_digits<5>(__funnelshift_r(w[8 + i], w[9 + i], sh), d);
-    P.b[i] = (d[0] << 2) | (d[2] << 4) | (d[4] << 6);
-    P.b[4 + i] = (d[1] << 2) | (d[3] << 4);
-  }
-  {
-    uint32_t d[4];
-    expand_digits<4>(__funnelshift_r(w[12], w[13], sh), d);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) P.b[4 + k] |= d[k] << 6;
-  }
-  // Chunks 0..4.
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    uint32_t d[5];
-    expand_digits<5>(__funnelshift_r(w[i], w[i + 1], sh), d);
-    P.a[i] = d[0] | (d[1] << 2) | (d[2] << 4) | (d[3] << 6);
-    P.b[i] |= d[4];
+    uint32_t P[6];
+    pow3_floors<5>(__funnelshift_r(w[i], w[i + 1], sh), P);
+    Q.a[i] = P[4] * 64u - P[1] * 11u - P[2] * 44u - P[3] * 176u;
+    Q.b[i] = P[5] - 3u * P[4];
   }
-  P.dw = __half2float(__ushort_as_half(static_cast<unsigned short>((w[13] >> sh) & 0xFFFFu)));
+  // qs word 8 + i: slots 1, 2, 3 of b[i] take digits 0, 2, 4; slots 1, 2 of
+  // b[4 + i] take digits 1, 3.
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t P[6];
+    pow3_floors<5>(__funnelshift_r(w[8 + i], w[9 + i], sh), P);
+    Q.b[i] += P[1] * 4u - P[2] * 48u + P[3] * 16u - P[4] * 192u + P[5] * 64u;
+    Q.b[4 + i] += P[2] * 4u - P[1] * 12u - P[3] * 48u + P[4] * 16u;
+  }
+  // qh word: digit k goes to slot 3 of b[4 + k].
+  {
+    uint32_t P[5];
+    pow3_floors<4>(__funnelshift_r(w[12], w[13], sh), P);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) Q.b[4 + k] += P[k + 1] * 64u - P[k] * 192u;
+  }
+  Q.dw = __half2float(__ushort_as_half(static_cast<unsigned short>((w[13] >> sh) & 0xFFFFu)));
 }
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
