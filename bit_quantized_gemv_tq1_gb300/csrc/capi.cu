@@ -20,7 +20,7 @@ constexpr int64_t kMaxK = 62720;  // activation records of one column must fit t
 // dp4a kernels (measured crossover on GB300 at N=5120, K=6144: the dp4a
 // kernel's cost grows with every column, the tile path's barely does).
 #ifndef TQ1_TILE_MIN_T
-#define TQ1_TILE_MIN_T 11
+#define TQ1_TILE_MIN_T 7
 #endif
 constexpr int64_t kTileMinT = TQ1_TILE_MIN_T;
 std::mutex g_mu;

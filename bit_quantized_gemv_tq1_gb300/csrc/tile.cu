@@ -76,8 +76,8 @@ constexpr int kStageK = 64;     // K per MMA stage (a quarter of a 256-block)
 constexpr int kWinBytes = 80;   // raw weight window per row and block (16-byte aligned)
 constexpr uint32_t kWRawBytes = kTileRows * kWinBytes;
 constexpr int kGroups = 3;      // A warp groups = tensor-memory block slots
-constexpr int kWSlotsPerGroup = 2;
-constexpr int kRW = kGroups * kWSlotsPerGroup;  // raw weight ring: two blocks per A group
+constexpr int kWSlotsPerGroup = 3;
+constexpr int kRW = kGroups * kWSlotsPerGroup;  // raw weight ring: three blocks per A group
 constexpr int kAWarps = 4 * kGroups, kEWarps = 4;
 constexpr int kEWarp0 = kAWarps, kMWarp = kEWarp0 + kEWarps, kPWarpW = kMWarp + 1, kPWarpB = kMWarp + 2;
 constexpr int kTThreads = (kPWarpB + 1) * 32;
@@ -93,15 +93,27 @@ struct TileCfg {
   // A block slots live in tensor memory (one per A warp group, so a slot has
   // a single owner), B block slots in shared memory (a plain ring).
   static constexpr int kRB = TOK >= 64 ? 2 : 3;
-  static constexpr int kAccs = TOK >= 64 ? 1 : 2;        // TMEM accumulators
+  static constexpr int kAccs = TOK >= 64 ? 1 : 2;        // TMEM accumulators (tiles in flight)
   static constexpr int kAccCols = N < 32 ? 32 : N;
-  static constexpr int kA0 = kAccs * kAccCols;           // first TMEM column of the A slots
+  // Independent partial accumulators per tile: consecutive MMAs alternate
+  // between them, so an MMA need not wait for the previous one's result
+  // (at small N the chain through one accumulator, not the tensor pipe,
+  // sets the pace).  The epilogue adds them.
+  static constexpr int kPart = N <= 32 ? 2 : 1;
+  static constexpr int kAccStride = kPart * kAccCols;     // TMEM columns per tile accumulator
+  static constexpr int kA0 = kAccs * kAccStride;         // first TMEM column of the A slots
   static constexpr int kTmemCols = 512;
   static_assert(kA0 + kGroups * kBlockCols <= kTmemCols, "tensor memory budget");
   static constexpr bool kSplitOk = TOK <= 32;            // split-K partials fit the B ring
   static_assert(!kSplitOk || kRB * kBBlock >= kTileRows * TOK * 4, "split-K partials");
   static constexpr uint32_t kOffW = kRB * kBBlock;
-  static constexpr uint32_t kSmem = kOffW + kRW * kWRawBytes + 1024;
+  // Split-K partials pushed by every rank into the rank that owns the rows:
+  // [source rank][row of the owner's slice][token], at most ceil(128 / S)
+  // rows per slice.
+  static constexpr uint32_t kOffRed = kOffW + kRW * kWRawBytes;
+  static constexpr uint32_t kRedBytes = kSplitOk ? (kTileRows + kMaxSplit) * TOK * 4 : 0;
+  static constexpr uint32_t kSmem = kOffRed + kRedBytes + 1024;
+  static_assert(kSmem + 2048 <= 232448, "shared memory budget");
   // Instruction descriptor: D fp32, A and B fp16, K-major, N, M = 128.
   static constexpr uint32_t kIdesc =
       (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(kTileRows) >> 4) << 24);
@@ -261,15 +273,6 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// fp32 at the same shared-memory offset as `local`, in cluster CTA `rank`.
-__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-  return v;
 }
 
 // P_k = floor(b * 3^k / 256) of the four bytes held in 16-bit lanes lo
@@ -463,11 +466,18 @@ __global__ void __launch_bounds__(kTThreads, 1)
   __shared__ int s_abort;
   volatile int* abort_flag = &s_abort;
 
+  if (threadIdx.x == 0) {
+    // Fetch both tensor-map descriptors now: the first copy through a map
+    // otherwise waits for its descriptor.
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmb)) : "memory");
+  }
   const uint32_t raw = smem_addr(tsmem_raw);
   uint8_t* sm = tsmem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_addr(sm);
   uint8_t* wraw = sm + C::kOffW;
-  float* red = reinterpret_cast<float*>(sm);  // split-K partials reuse the B ring after the last MMA
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);  // split-K partials (owner side)
+  __shared__ float s_tscale[kEWarps][TOK];  // per-token scales, one copy per epilogue warp
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = a.k / kQK;
@@ -486,6 +496,15 @@ __global__ void __launch_bounds__(kTThreads, 1)
   int nunits = 0;
   while (unit_tile(nunits) < ntiles) ++nunits;
   const uint32_t nall = static_cast<uint32_t>(nunits * nblk);  // blocks of this CTA
+  // Block j goes to A group j % kGroups as that group's block c = j / kGroups;
+  // its raw weights use ring slot g * kWSlotsPerGroup + c % kWSlotsPerGroup.
+  auto issue_weights = [&](uint32_t j, uint32_t ws) {
+    const int bi = static_cast<int>(j % nblk);
+    const int row0 = (unit_tile(static_cast<int>(j / nblk)) / a.tiles_n) * kTileRows;
+    mbar_arrive_expect_tx(&wfull_bar[ws], kWRawBytes);
+    tma_load_2d(wraw + ws * kWRawBytes, &tmw, ((kb0 + bi) * kBlockBytes) & ~15, row0, &wfull_bar[ws]);
+  };
+  const uint32_t nfirst = nall < static_cast<uint32_t>(kRW) ? nall : static_cast<uint32_t>(kRW);
 
   if (tid == 0) {
     for (int i = 0; i < kGroups; ++i) {
@@ -507,6 +526,13 @@ __global__ void __launch_bounds__(kTThreads, 1)
     s_abort = 0;
     fence_mbar_init();
   }
+  // The weights do not depend on the previous kernel: the first ring's worth
+  // of copies goes out at once, one per lane of warp 0.
+  if (warp == 0) {
+    __syncwarp();
+    const uint32_t j = static_cast<uint32_t>(lane);
+    if (j < nfirst) issue_weights(j, (j % kGroups) * kWSlotsPerGroup + (j / kGroups) % kWSlotsPerGroup);
+  }
   if (warp == kMWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_tmem)),
                  "r"(C::kTmemCols));
@@ -526,8 +552,13 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const int rl = (quarter << 5) | lane;
     const uint32_t tslot = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kA0 + g * kBlockCols;
     uint32_t c = 0;  // this group's blocks so far
+    int bi = g;      // j % nblk, advanced without a division
+    while (bi >= nblk && nblk > 0) bi -= nblk;
     for (uint32_t j = g; j < nall; j += kGroups, ++c) {
-      const int bi = static_cast<int>(j % nblk);
+      if (c > 0) {
+        bi += kGroups;
+        while (bi >= nblk) bi -= nblk;
+      }
       const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
       if (!warp_wait(&wfull_bar[ws], (c / kWSlotsPerGroup) & 1u, abort_flag)) break;
       uint32_t W[20];
@@ -574,6 +605,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
     // --------------------------------------------------------- epilogue --
     const int quarter = warp & 3;  // TMEM lane quarter this warp may read
     const int rl = quarter * 32 + lane;
+    float* tsc = s_tscale[warp - kEWarp0];
+    // Split-K: the value of (row rl, token tl) goes to the rank owning row
+    // rl's slice, into that rank's partials at [this rank][row in slice][tl].
+    const int owner = ((rl + 1) * S - 1) / kTileRows;
+    const int slice_max = (kTileRows + S - 1) / S;
+    uint32_t red_dst = 0;
+    if (S > 1) {
+      const int oslot = (rank * slice_max + (rl - (kTileRows * owner) / S)) * TOK;
+      uint32_t la = smem_addr(red + oslot);
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(red_dst) : "r"(la), "r"(owner));
+    }
     pdl_wait();  // the scales are written by the prep kernel
     for (int u = 0; u < nunits; ++u) {
       const int tile = unit_tile(u);
@@ -581,23 +623,48 @@ __global__ void __launch_bounds__(kTThreads, 1)
       const int tok0 = (tile % a.tiles_n) * TOK;
       const int acc = u % C::kAccs;
       const uint32_t aph = static_cast<uint32_t>(u / C::kAccs) & 1u;
+      // Scales of this tile's tokens, fetched while the MMAs run.
+      __syncwarp();
+      for (int tl = lane; tl < TOK; tl += 32) tsc[tl] = __ldg(a.scale + tok0 + tl);
+      __syncwarp();
       if (!warp_wait(&accf_bar[acc], aph, abort_flag)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * C::kAccStride);
 #pragma unroll 1
       for (int c0 = 0; c0 < TOK; c0 += C::kChunk) {
         uint32_t vh[C::kChunk], vl[C::kChunk];
         tmem_ld<C::kChunk>(tbase + c0, vh);
         tmem_ld<C::kChunk>(tbase + TOK + c0, vl);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (C::kPart == 2) {
+          uint32_t wh[C::kChunk], wl[C::kChunk];
+          tmem_ld<C::kChunk>(tbase + C::kAccCols + c0, wh);
+          tmem_ld<C::kChunk>(tbase + C::kAccCols + TOK + c0, wl);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int jj = 0; jj < C::kChunk; ++jj) {
-          const int tl = c0 + jj, tok = tok0 + tl;
-          const float v = (__uint_as_float(vh[jj]) + __uint_as_float(vl[jj])) * __ldg(a.scale + tok);
-          if (S > 1) {
-            red[tl * kTileRows + rl] = v;
-          } else if (row < a.n && tok < a.t) {
-            a.y[static_cast<int64_t>(tok) * a.n + row] = v;
+          for (int jj = 0; jj < C::kChunk; ++jj) {
+            vh[jj] = __float_as_uint(__uint_as_float(vh[jj]) + __uint_as_float(wh[jj]));
+            vl[jj] = __float_as_uint(__uint_as_float(vl[jj]) + __uint_as_float(wl[jj]));
+          }
+        }
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (S > 1) {
+          // Four tokens per 16-byte store into the owner's partials.
+#pragma unroll
+          for (int jj = 0; jj < C::kChunk; jj += 4) {
+            const int tl = c0 + jj;
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = (__uint_as_float(vh[jj + e]) + __uint_as_float(vl[jj + e])) * tsc[tl + e];
+            asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red_dst + 4u * tl), "f"(v[0]),
+                         "f"(v[1]), "f"(v[2]), "f"(v[3])
+                         : "memory");
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < C::kChunk; ++jj) {
+            const int tl = c0 + jj, tok = tok0 + tl;
+            const float v = (__uint_as_float(vh[jj]) + __uint_as_float(vl[jj])) * tsc[tl];
+            if (row < a.n && tok < a.t) a.y[static_cast<int64_t>(tok) * a.n + row] = v;
           }
         }
       }
@@ -611,16 +678,18 @@ __global__ void __launch_bounds__(kTThreads, 1)
       bool issued = false, ok = true;
       uint64_t* last_bar = nullptr;
       uint32_t last_ph = 0;
-      uint32_t j = 0;
+      // Everything but the waits is precomputed: the B descriptors of a slot
+      // differ from the ring's first descriptor only in the address field
+      // (address >> 4, 14 bits, no carry for shared-memory addresses).
+      const uint64_t d0 = umma_desc_sw128(sbase);
+      uint32_t ga = 0, pa = 0, rb = 0, pb = 0;  // A group slot, B ring slot and their phases
       for (int u = 0; u < nunits && ok; ++u) {
         const int acc = u % C::kAccs;
         const uint32_t aph = static_cast<uint32_t>(u / C::kAccs) & 1u;
         if (!spin_wait_or_abort(&acce_bar[acc], aph ^ 1u, abort_flag)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + static_cast<uint32_t>(acc * C::kAccCols);
-        for (int bi = 0; bi < nblk; ++bi, ++j) {
-          const uint32_t ga = j % kGroups, pa = (j / kGroups) & 1u;
-          const uint32_t rb = j % C::kRB, pb = (j / C::kRB) & 1u;
+        const uint32_t dt = tmem + static_cast<uint32_t>(acc * C::kAccStride);
+        for (int bi = 0; bi < nblk; ++bi) {
           if (!spin_wait_or_abort(&afull_bar[ga], pa, abort_flag) ||
               !spin_wait_or_abort(&bfull_bar[rb], pb, abort_flag)) {
             ok = false;
@@ -628,18 +697,23 @@ __global__ void __launch_bounds__(kTThreads, 1)
           }
           tc_fence_after();
           const uint32_t at = tmem + C::kA0 + ga * kBlockCols;
-          const uint32_t sb = sbase + rb * C::kBBlock;
+          const uint64_t db = d0 + ((rb * C::kBBlock) >> 4);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int ks = 0; ks < kStageK / 16; ++ks)
-              umma_ts(dt, at + 32u * q + 8u * ks, umma_desc_sw128(sb + q * C::kBTile + 32u * ks), C::kIdesc,
-                      (bi > 0 || q > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < kStageK / 16; ++ks) {
+              const int step = q * (kStageK / 16) + ks;  // 0..15 within the block
+              const uint32_t part = static_cast<uint32_t>(step % C::kPart);
+              umma_ts(dt + part * C::kAccCols, at + 32u * q + 8u * ks, db + ((q * C::kBTile + 32u * ks) >> 4),
+                      C::kIdesc, (bi > 0 || step >= C::kPart) ? 1u : 0u);
+            }
           umma_commit(&aempty_bar[ga]);
           umma_commit(&bempty_bar[rb]);
           issued = true;
           last_bar = &bempty_bar[rb];
           last_ph = pb;
+          if (++ga == kGroups) { ga = 0; pa ^= 1u; }
+          if (++rb == C::kRB) { rb = 0; pb ^= 1u; }
         }
         if (!ok) break;
         umma_commit(&accf_bar[acc]);
@@ -651,78 +725,82 @@ __global__ void __launch_bounds__(kTThreads, 1)
   } else if (warp == kPWarpW) {
     // ---------------------------------------------------- weight copies --
     if (lane == 0) {
-      uint32_t cnt[kGroups] = {};
       int last_slot = -1;
       uint32_t last_ph = 0;
-      for (uint32_t j = 0; j < nall; ++j) {
-        const int g = static_cast<int>(j % kGroups);
-        const int bi = static_cast<int>(j % nblk);
-        const int row0 = (unit_tile(static_cast<int>(j / nblk)) / a.tiles_n) * kTileRows;
-        const uint32_t c = cnt[g]++;
-        const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
+      for (uint32_t j = nfirst; j < nall; ++j) {
+        const uint32_t g = j % kGroups, c = j / kGroups;
+        const uint32_t ws = g * kWSlotsPerGroup + (c % kWSlotsPerGroup);
         const uint32_t ph = (c / kWSlotsPerGroup) & 1u;
         if (!wait_or_abort(&wempty_bar[ws], ph ^ 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(&wfull_bar[ws], kWRawBytes);
-        tma_load_2d(wraw + ws * kWRawBytes, &tmw, ((kb0 + bi) * kBlockBytes) & ~15, row0, &wfull_bar[ws]);
+        issue_weights(j, ws);
         last_slot = static_cast<int>(ws);
         last_ph = ph;
       }
       // Copies still in flight must land before the CTA leaves.
       if (*abort_flag && last_slot >= 0) (void)mbar_wait(&wfull_bar[last_slot], last_ph);
+      else if (*abort_flag && nfirst > 0) {
+        for (uint32_t j = 0; j < nfirst; ++j)
+          (void)mbar_wait(&wfull_bar[(j % kGroups) * kWSlotsPerGroup + (j / kGroups) % kWSlotsPerGroup], 0);
+      }
     }
   } else {
     // ------------------------------------------------ activation copies --
-    if (lane == 0) {
-      pdl_wait();  // the B operand is written by the prep kernel
-      int last_slot = -1;
-      uint32_t last_ph = 0;
-      for (uint32_t j = 0; j < nall; ++j) {
-        const int bi = static_cast<int>(j % nblk);
-        const int tok0 = (unit_tile(static_cast<int>(j / nblk)) % a.tiles_n) * TOK;
-        const uint32_t rb = j % C::kRB, pb = (j / C::kRB) & 1u;
-        if (!wait_or_abort(&bempty_bar[rb], pb ^ 1u, abort_flag)) break;
-        uint8_t* dst = sm + rb * C::kBBlock;
-        mbar_arrive_expect_tx(&bfull_bar[rb], C::kBBlock);
-        const int kx = (kb0 + bi) * kQK;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          tma_load_2d(dst + q * C::kBTile, &tmb, kx + q * kStageK, tok0, &bfull_bar[rb]);
-          tma_load_2d(dst + q * C::kBTile + TOK * 128, &tmb, kx + q * kStageK, a.t_pad + tok0, &bfull_bar[rb]);
-        }
-        last_slot = static_cast<int>(rb);
-        last_ph = pb;
+    // Lane 0 waits for a free slot and posts the byte count; lanes 0-7 then
+    // issue the block's eight copies (4 quarters x hi/lo rows) at once.
+    pdl_wait();  // the B operand is written by the prep kernel
+    int last_slot = -1;
+    uint32_t last_ph = 0, rb = 0, pb = 0;
+    int bi = 0, u = 0;
+    int tok0 = nunits > 0 ? (unit_tile(0) % a.tiles_n) * TOK : 0;
+    for (uint32_t j = 0; j < nall; ++j) {
+      int ok = 1;
+      if (lane == 0) {
+        ok = wait_or_abort(&bempty_bar[rb], pb ^ 1u, abort_flag) ? 1 : 0;
+        if (ok) mbar_arrive_expect_tx(&bfull_bar[rb], C::kBBlock);
       }
-      if (*abort_flag && last_slot >= 0) (void)mbar_wait(&bfull_bar[last_slot], last_ph);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane < 8) {
+        const int q = lane >> 1, hl = lane & 1;
+        tma_load_2d(sm + rb * C::kBBlock + q * C::kBTile + hl * TOK * 128, &tmb, (kb0 + bi) * kQK + q * kStageK,
+                    hl * a.t_pad + tok0, &bfull_bar[rb]);
+      }
+      __syncwarp();
+      last_slot = static_cast<int>(rb);
+      last_ph = pb;
+      if (++rb == C::kRB) { rb = 0; pb ^= 1u; }
+      if (++bi == nblk) {
+        bi = 0;
+        if (++u < nunits) tok0 = (unit_tile(u) % a.tiles_n) * TOK;
+      }
     }
+    if (lane == 0 && *abort_flag && last_slot >= 0) (void)mbar_wait(&bfull_bar[last_slot], last_ph);
   }
-
   __syncthreads();
   if (tid == 0 && *abort_flag) raise_status(a.status, kStatusTimeout);
   if (S > 1) {
     __syncwarp();
-    cluster_sync_all();  // every rank's partial tile is in its shared memory
-    if (!*abort_flag && warp >= kEWarp0 && warp < kMWarp) {
+    cluster_sync_all();  // every rank's partials are in their owners' shared memory
+    if (!*abort_flag) {
+      // Every thread of the CTA sums a strided share of this rank's slice:
+      // thread -> (row of the slice, token) with the row fastest, so that
+      // the y stores of a warp are contiguous.
       const int tile = static_cast<int>(blockIdx.x / S);
       const int row0 = (tile / a.tiles_n) * kTileRows, tok0 = (tile % a.tiles_n) * TOK;
       const int r_lo = (kTileRows * rank) / S, r_hi = (kTileRows * (rank + 1)) / S;
-      const int nr = r_hi - r_lo;
-      for (int i = tid - kEWarp0 * 32; i < nr * TOK; i += kEWarps * 32) {
-        const int tl = i / nr, rl = r_lo + (i - (i / nr) * nr);
-        const int row = row0 + rl, tok = tok0 + tl;
-        if (row < a.n && tok < a.t) {
-          float part[kMaxSplit];
-#pragma unroll
-          for (int s = 0; s < kMaxSplit; ++s)
-            part[s] = s < S ? ld_peer(&red[tl * kTileRows + rl], static_cast<uint32_t>(s)) : 0.0f;
+      const int nr = r_hi - r_lo, slice_max = (kTileRows + S - 1) / S;
+      const int ntok = min(TOK, a.t - tok0), nrow = min(nr, a.n - (row0 + r_lo));
+      static_assert(kTThreads >= 512, "reduction mapping");
+      for (int ri = tid % 64; tid < 512 && ri < nrow; ri += 64) {
+        for (int tl = tid / 64; tl < ntok; tl += 8) {
           float v = 0.0f;
 #pragma unroll
-          for (int s = 0; s < kMaxSplit; ++s) v += s < S ? part[s] : 0.0f;  // rank order
-          a.y[static_cast<int64_t>(tok) * a.n + row] = v;
+          for (int src = 0; src < kMaxSplit; ++src)  // rank order
+            if (src < S) v += red[(src * slice_max + ri) * TOK + tl];
+          a.y[static_cast<int64_t>(tok0 + tl) * a.n + row0 + r_lo + ri] = v;
         }
       }
     }
-    __syncwarp();
-    cluster_sync_all();  // no rank leaves while others still read its partials
   }
   tc_fence_before();
   __syncthreads();

@@ -27,7 +27,7 @@
  *     16-byte aligned (TQ1_ERR_ALIGN otherwise).  The library never
  *     synchronises; work is enqueued on `stream` (a cudaStream_t, NULL for
  *     the legacy default stream) on the current device.  The only memory it
- *     takes is tq1_mmv's scratch for t >= 11, stream-ordered from its own
+ *     takes is tq1_mmv's scratch for t >= 7, stream-ordered from its own
  *     memory pool (see tq1_mmv).
  *   - Arguments are checked on the host before anything is launched; a
  *     failed check returns its negative code and launches nothing.
@@ -100,7 +100,7 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
  *   sum_blocks d_w * sum_{chunks j} d_a[j] * I_j,   I_j = sum (trit * q) (exact int32)
  * in fp32.  blocks [n][k/256] TQ1_0, q8 [t][k/32] Q8_1, y fp32 [t][n].
  * t <= 10 runs the byte-major dp4a kernels laddered at 1/2/4/8/16 columns;
- * t >= 11 (prefill included) runs the tensor-core path: a prep kernel splits
+ * t >= 7 (prefill included) runs the tensor-core path: a prep kernel splits
  * the activations into exact fp16 hi/lo parts in scratch taken from a
  * library-owned stream-ordered memory pool (cudaMallocFromPoolAsync /
  * cudaFreeAsync on `stream`: no synchronisation, capturable), then a tcgen05
