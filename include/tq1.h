@@ -99,7 +99,8 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
  * w = d_w * trit and x = d_a * q, accumulated as
  *   sum_blocks d_w * sum_{chunks j} d_a[j] * I_j,   I_j = sum (trit * q) (exact int32)
  * in fp32.  blocks [n][k/256] TQ1_0, q8 [t][k/32] Q8_1, y fp32 [t][n].
- * t <= 10 runs the byte-major dp4a kernels laddered at 1/2/4/8/16 columns;
+ * t <= 6 runs the byte-major dp4a kernels (rungs of 1/2/4 columns, then a
+ * general kernel with 8-column rungs);
  * t >= 7 (prefill included) runs the tensor-core path: a prep kernel splits
  * the activations into exact fp16 hi/lo parts in scratch taken from a
  * library-owned stream-ordered memory pool (cudaMallocFromPoolAsync /
