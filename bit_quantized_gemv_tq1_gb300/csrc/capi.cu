@@ -23,6 +23,9 @@ constexpr int64_t kMaxK = 62720;  // activation records of one column must fit t
 #define TQ1_TILE_MIN_T 7
 #endif
 constexpr int64_t kTileMinT = TQ1_TILE_MIN_T;
+// Routed pairs up to which tq1_mmv_id skips the routing table (each pair's
+// rows are then read once per pair, not once per distinct expert).
+constexpr int64_t kMoeDirectMaxPairs = 32;
 std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
@@ -201,6 +204,9 @@ int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, con
   const uint8_t* w = static_cast<const uint8_t*>(expert_blocks);
   const uint8_t* a = static_cast<const uint8_t*>(q8);
   MoePlan plan{};
+  // A few pairs (decode): no routing table, each CTA reads its pair's id.
+  if (t * top_k <= kMoeDirectMaxPairs && moe_direct_plan(n, k, t * top_k, &plan))
+    return launch_moe_direct(w, a, ids, y, n, k, top_k, n_experts, t * top_k, plan, s, st);
   const bool small = moe_small_plan(n, k, t * top_k, n_experts, &plan);
   rc = launch_moe_compact(ids, t, top_k, n_experts, small ? plan.chunk : 1, small ? plan.row_blocks : 1, table, s,
                           st);

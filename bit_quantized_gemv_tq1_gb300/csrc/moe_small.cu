@@ -195,6 +195,192 @@ __global__ void __launch_bounds__(kMThreads, 2) moe_small_kernel(const MoeArgs a
   }
 }
 
+// ----------------------------------------------------------- direct mode --
+// Few routed pairs (a decode step: t * top_k of a few tens): compacting the
+// routing table costs a kernel and two dependent round trips through L2 on
+// the critical path, for little weight reuse to gain.  Instead each CTA owns
+// one (pair, row range): it reads the pair's expert id itself once the
+// previous kernel has finished, requests that expert's rows, builds the
+// token's activation records while they arrive, and writes y[pair][rows].
+// A pair whose id is outside [0, n_experts) leaves its outputs untouched and
+// raises kStatusBadId.
+constexpr int kDThreads = 256;
+constexpr int kDWarps = kDThreads / 32;
+constexpr int kDMaxRows = 128;
+constexpr int kDMaxGroups = kDMaxRows / kRowsPerTask;
+constexpr size_t kDSmemBudget = 112 * 1024;  // two CTAs per SM
+
+struct DirectArgs {
+  const uint8_t* w;      // expert 0's first weight block
+  const uint8_t* q8;     // Q8_1 activations [t][k/32]
+  const int32_t* ids;    // [t][top_k]
+  float* y;              // [t * top_k][n]
+  unsigned* status;
+  int64_t n;
+  int n_experts, top_k, nb, nkc;
+  int rows;              // rows per CTA (multiple of 4)
+  int row_blocks;        // CTAs per pair
+  uint32_t slab_bytes;
+};
+
+__global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nb = a.nb, nkc = a.nkc;
+  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBlockBytes;
+  const uint32_t gstride = group_stride(rowbytes);
+  uint8_t* slab = smem;
+  uint32_t* recs = reinterpret_cast<uint32_t*>(smem + a.slab_bytes);
+  float* part = reinterpret_cast<float*>(recs + static_cast<size_t>(nb) * kPRec);
+  __shared__ __align__(8) uint64_t bars[kDMaxGroups];
+
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = lane >> 3, s = lane & 7;
+  const int pair = static_cast<int>(blockIdx.x) / a.row_blocks;
+  const int rb = static_cast<int>(blockIdx.x) - pair * a.row_blocks;
+  const int64_t r0 = static_cast<int64_t>(rb) * a.rows;
+  const int rows = static_cast<int>(a.n - r0 < a.rows ? a.n - r0 : a.rows);
+  const int ngroups = (rows + kRowsPerTask - 1) / kRowsPerTask;
+  if (tid == 0) {
+    for (int g = 0; g < ngroups; ++g) mbar_init(&bars[g], 1);
+    fence_mbar_init();
+  }
+  pdl_wait();  // ids and activations may come from the previous kernel
+  const int e = __ldg(a.ids + pair);
+  if (e < 0 || e >= a.n_experts) {
+    if (tid == 0 && rb == 0) raise_status(a.status, kStatusBadId);
+    return;  // no copy was issued
+  }
+  const uint8_t* wtask = a.w + (static_cast<int64_t>(e) * a.n + r0) * rowbytes;
+  const uint32_t wlow = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(wtask));
+  if (tid == 0) {
+    const uint64_t policy = l2_evict_first_policy();
+    for (int g = 0; g < ngroups; ++g) {
+      const int grows = min(kRowsPerTask, rows - g * kRowsPerTask);
+      const uint8_t* src = wtask + static_cast<int64_t>(g) * kRowsPerTask * rowbytes;
+      const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
+      const uint32_t tot = delta + static_cast<uint32_t>(grows) * rowbytes;
+      const uint32_t main = tot & ~15u;
+      uint8_t* dst = slab + static_cast<uint32_t>(g) * gstride;
+      for (uint32_t i = main; i < tot; ++i) dst[i] = __ldg(src - delta + i);
+      mbar_arrive_expect_tx(&bars[g], main);
+      if (main) bulk_g2s(dst, src - delta, main, &bars[g], policy);
+    }
+  }
+  // Activation records of the pair's token while the weights arrive.
+  const int64_t token = pair / a.top_k;
+  for (int i = tid; i < nb * 8; i += kDThreads)
+    fill_precord_chunk(a.q8 + (token * nb * 8 + i) * kQ8Bytes, recs + (i >> 3) * kPRec, i & 7);
+  __syncthreads();
+
+  // Warp tasks: 4 rows x 8 blocks; lane (row r, block s).
+  const int wtasks = ngroups * nkc;
+  bool ok = true;
+  for (int wt = warp; wt < wtasks; wt += kDWarps) {
+    const int g = wt / nkc, kc = wt - (wt / nkc) * nkc;
+    const int row = g * kRowsPerTask + r;
+    const int b = kc * kLanesPerRow + s;
+    if (!mbar_wait(&bars[g], 0)) {
+      ok = false;
+      break;
+    }
+    float v = 0.0f;
+    if (row < rows && b < nb) {
+      Packed P;
+      const uint32_t off = static_cast<uint32_t>(g) * gstride +
+                           ((wlow + static_cast<uint32_t>(g) * kRowsPerTask * rowbytes) & 15u) +
+                           static_cast<uint32_t>(r) * rowbytes + static_cast<uint32_t>(b) * kBlockBytes;
+      expand_pack(slab, off, P);
+      v = packed_dot(P, recs + b * kPRec);
+    }
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    if (s == 0 && row < rows) {
+      if (nkc == 1) a.y[static_cast<int64_t>(pair) * a.n + r0 + row] = v;
+      else part[row * nkc + kc] = v;
+    }
+  }
+  const bool abort = __syncthreads_or(!ok) != 0;
+  if (abort) {
+    if (tid == 0) {
+      raise_status(a.status, kStatusTimeout);
+      for (int g = 0; g < ngroups; ++g) (void)mbar_wait(&bars[g], 0);  // let copies land (bounded)
+    }
+    return;
+  }
+  if (nkc > 1) {
+    for (int row = tid; row < rows; row += kDThreads) {
+      float v = 0.0f;
+      for (int kc = 0; kc < nkc; ++kc) v += part[row * nkc + kc];  // in order
+      a.y[static_cast<int64_t>(pair) * a.n + r0 + row] = v;
+    }
+  }
+}
+
+// Rows per CTA so that pairs x row blocks is about one CTA per SM, within the
+// shared-memory budget; false if even four rows do not fit.
+bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan) {
+  const DeviceInfo& di = device_info();
+  const int nb = static_cast<int>(k / kQK);
+  const int nkc = (nb + kLanesPerRow - 1) / kLanesPerRow;
+  const uint32_t gs = group_stride(static_cast<uint32_t>(nb) * kBlockBytes);
+  int64_t rows = (n * pairs + di.num_sms - 1) / std::max(1, di.num_sms);
+  rows = ((std::max<int64_t>(rows, kRowsPerTask) + kRowsPerTask - 1) / kRowsPerTask) * kRowsPerTask;
+  rows = std::min<int64_t>(rows, kDMaxRows);
+  auto smem_of = [&](int64_t r) {
+    return static_cast<size_t>(r / kRowsPerTask) * gs + static_cast<size_t>(nb) * kPRec * 4 +
+           static_cast<size_t>(r) * nkc * 4;
+  };
+  while (rows > kRowsPerTask && smem_of(rows) > kDSmemBudget) rows -= kRowsPerTask;
+  if (smem_of(rows) > kDSmemBudget) return false;
+  plan->chunk = 1;
+  plan->rows = static_cast<int>(rows);
+  plan->row_blocks = static_cast<int>((n + rows - 1) / rows);
+  return pairs * plan->row_blocks < (int64_t{1} << 31);
+}
+
+int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
+                      int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
+                      unsigned* status) {
+  const DeviceInfo& di = device_info();
+  DirectArgs a = {};
+  a.w = w;
+  a.q8 = q8;
+  a.ids = ids;
+  a.y = y;
+  a.status = status;
+  a.n = n;
+  a.n_experts = static_cast<int>(n_experts);
+  a.top_k = static_cast<int>(top_k);
+  a.nb = static_cast<int>(k / kQK);
+  a.nkc = (a.nb + kLanesPerRow - 1) / kLanesPerRow;
+  a.rows = plan.rows;
+  a.row_blocks = plan.row_blocks;
+  const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * kBlockBytes;
+  a.slab_bytes = static_cast<uint32_t>(plan.rows / kRowsPerTask) * group_stride(rowbytes);
+  const size_t smem = a.slab_bytes + static_cast<size_t>(a.nb) * kPRec * 4 + static_cast<size_t>(plan.rows) * a.nkc * 4;
+  static bool configured[64] = {};
+  if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
+  if (!configured[di.device]) {
+    if (!cuda_ok(cudaFuncSetAttribute(moe_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kDSmemBudget))))
+      return TQ1_ERR_CUDA;
+    configured[di.device] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pairs * plan.row_blocks));
+  cfg.blockDim = dim3(kDThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, moe_direct_kernel, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+}
+
 // Rows per task and row blocks per expert: enough tasks for about two per
 // CTA slot when every routed pair lands on its own expert, within the shared
 // memory budget (two CTAs per SM).

@@ -71,6 +71,14 @@ struct MoePlan {
   int chunk, rows, row_blocks;
 };
 bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoePlan* plan);
+
+// Expert-routed mat-vec without a routing table, for few pairs: one CTA per
+// (pair, row range) reads its expert id itself.  `plan` gives the rows per
+// CTA and the row ranges per pair.
+bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan);
+int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
+                      int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
+                      unsigned* status);
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
                      unsigned* status);
