@@ -351,6 +351,7 @@ def run_ours(args, ws, rank, local):
     if not args.no_extra:
         extra["prefill_c5"] = prefill_bench(lib, L, synth, dev, stream, capture, args)
         extra["moe_c4"] = moe_bench(lib, L, synth, dev, stream, capture, args)
+        extra["dequant_c2"] = dequant_bench(lib, L, synth, dev, stream, capture, args)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -441,6 +442,43 @@ def prefill_bench(lib, L, synth, dev, stream, capture, args) -> dict:
             "peak_tflops": peak, "frac": round(flops / (ms * 1e-3) / 1e12 / peak, 4),
             "note": "tflops counts the method's MACs once; the kernel issues each twice (fp16 hi and lo "
                     "parts of the activations); peak = measured bf16 dense (fp16 runs at the same rate)"}
+
+
+def dequant_bench(lib, L, synth, dev, stream, capture, args) -> dict:
+    """Dequantisation of config 2's matrix (N=5120, K=6144) to fp32 and fp16,
+    cycling weight copies; bytes = packed weights read + values written."""
+    import torch
+
+    c2 = synth.CONFIGS["c2"]
+    n, k = c2["n"], c2["k"]
+    wbytes = n * (k // QK) * BLOCK_BYTES
+    copies = 20
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2000)
+    blocks = torch.empty(copies * wbytes, dtype=torch.uint8, device=dev)
+    for l in range(copies):
+        w = synth.device_weights(n, k, c2["p_zero"], c2["d_lo"], c2["d_hi"], gen, dev)
+        L.tq1_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+        del w
+    peak = float(measured_peaks()["hbm_gbs"])
+    out = {"workload": "c2 matrix N=5120 K=6144 -> fp32 / fp16 rows"}
+    for f16 in (False, True):
+        y = torch.empty((n, k), dtype=torch.float16 if f16 else torch.float32, device=dev)
+
+        def calls(s, y=y, f16=f16):
+            for l in range(copies):
+                assert lib.tq1_dequantize_rows(blocks.data_ptr() + l * wbytes, y.data_ptr(), n, k, int(f16), s) == 0
+
+        g = capture(calls)
+        ms = _time_graph(g, stream, 5) / copies
+        assert lib.tq1_sync_status(stream.cuda_stream) == 0
+        byts = wbytes + n * k * (2 if f16 else 4)
+        gbs = byts / (ms * 1e-3) / 1e9
+        out["f16" if f16 else "f32"] = {"us_per_call": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                                        "frac_of_measured_hbm": round(gbs / peak, 4)}
+        del g, y
+    del blocks
+    return out
 
 
 def moe_bench(lib, L, synth, dev, stream, capture, args) -> dict:

@@ -67,9 +67,11 @@ def library() -> ctypes.CDLL:
         lib.tq1_mmv_id_workspace_size.argtypes = [I64, I64, I64]
         lib.tq1_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq1_mmv_id_noalloc.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P]
+        lib.tq1_dequantize_rows.argtypes = [P, P, I64, I64, ctypes.c_int, P]
+        lib.tq1_get_rows.argtypes = [P, P, I64, P, I64, I64, ctypes.c_int, P]
         lib.tq1_sync_status.argtypes = [P]
         for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_partials", "tq1_mmv_id",
-                     "tq1_mmv_id_noalloc", "tq1_sync_status"):
+                     "tq1_mmv_id_noalloc", "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -147,6 +149,18 @@ def tq1_mmv_id_noalloc(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int
     any stream capture; calls that may overlap on the GPU race on the array."""
     _check(library().tq1_mmv_id_noalloc(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(y), n, k, t,
                                         top_k, _stream(stream)), "tq1_mmv_id_noalloc")
+
+
+def tq1_dequantize_rows(blocks, out, n: int, k: int, out_f16: bool = False, stream=None) -> None:
+    """out[n][k] (fp32, or fp16 when out_f16) = the values the TQ1_0 blocks encode."""
+    _check(library().tq1_dequantize_rows(_addr(blocks), _addr(out), n, k, int(bool(out_f16)), _stream(stream)),
+           "tq1_dequantize_rows")
+
+
+def tq1_get_rows(blocks, row_ids, n_ids: int, out, n: int, k: int, out_f16: bool = False, stream=None) -> None:
+    """out[i] = dequantised row row_ids[i] of the n x k TQ1_0 matrix."""
+    _check(library().tq1_get_rows(_addr(blocks), _addr(row_ids), n_ids, _addr(out), n, k, int(bool(out_f16)),
+                                  _stream(stream)), "tq1_get_rows")
 
 
 def tq1_sync_status(stream=None) -> int:

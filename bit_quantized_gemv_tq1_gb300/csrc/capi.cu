@@ -180,6 +180,31 @@ int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t 
   return mmv_common(blocks, q8, nullptr, part, n, k, t, stream);
 }
 
+int tq1_dequantize_rows(const void* blocks, void* out, int64_t n, int64_t k, int out_f16, void* stream) {
+  if (n < 0 || k <= 0 || (k % kQK) != 0) return TQ1_ERR_SHAPE;
+  if (n == 0) return TQ1_OK;
+  if (!blocks || !out) return TQ1_ERR_NULL;
+  if (misaligned(blocks) || misaligned(out)) return TQ1_ERR_ALIGN;
+  if (n > (int64_t{1} << 40) / k) return TQ1_ERR_UNSUPPORTED;
+  unsigned* st = status_ptr();
+  if (!st) return TQ1_ERR_CUDA;
+  return launch_dequant(static_cast<const uint8_t*>(blocks), nullptr, n, out, n, k, out_f16 != 0,
+                        static_cast<cudaStream_t>(stream), st);
+}
+
+int tq1_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n, int64_t k,
+                 int out_f16, void* stream) {
+  if (n < 0 || n_ids < 0 || k <= 0 || (k % kQK) != 0) return TQ1_ERR_SHAPE;
+  if (n_ids == 0) return TQ1_OK;
+  if (!blocks || !row_ids || !out) return TQ1_ERR_NULL;
+  if (misaligned(blocks) || misaligned(row_ids) || misaligned(out)) return TQ1_ERR_ALIGN;
+  if (n_ids > (int64_t{1} << 40) / k) return TQ1_ERR_UNSUPPORTED;
+  unsigned* st = status_ptr();
+  if (!st) return TQ1_ERR_CUDA;
+  return launch_dequant(static_cast<const uint8_t*>(blocks), row_ids, n_ids, out, n, k, out_f16 != 0,
+                        static_cast<cudaStream_t>(stream), st);
+}
+
 size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k) {
   if (n_experts < 0 || t < 0 || top_k < 0) return 0;
   const size_t words = moe_ws_words(n_experts, t * top_k);

@@ -1,0 +1,129 @@
+// dequant.cu -- TQ1_0 rows back to fp32 or fp16 values: whole-matrix
+// dequantisation and row gathers (get_rows, e.g. an embedding lookup).
+//
+// The CPU reference walks a 256-block once and amortises each packed byte
+// over its trits (PrismML-Eng/llama.cpp issue #139, "Current behavior"); the
+// Vulkan backend of the same format ships dequant and get_rows shaders next
+// to its mat-vec ("Upstream state").  Here one warp owns one 256-block of one
+// output row: lane l produces elements 8l .. 8l+7.  Those eight elements are
+// digit k of eight consecutive packed bytes (element order of the block:
+// e < 160 -> qs[e % 32] digit e/32; e < 240 -> qs[32 + (e-160) % 16] digit
+// (e-160)/16; else qh[(e-240) % 4] digit (e-240)/4), so each lane reads its
+// eight bytes once and expands them with the specification's digit formula
+// ((uint8)(b*3^k)*3) >> 8.  Stores are 16-byte vectors, a warp writing one
+// contiguous 1 KiB (fp32) or 512 B (fp16) span: the kernel is bound by the
+// output bytes written to HBM.
+#include <algorithm>
+
+#include "../../include/tq1.h"
+#include "tq1_device.cuh"
+#include "tq1_internal.h"
+
+namespace tq1 {
+
+namespace {
+
+constexpr int kDqThreads = 256;
+constexpr int kDqWarps = kDqThreads / 32;
+
+__device__ __forceinline__ uint32_t digit_of(uint32_t b, uint32_t k) {
+  const uint32_t p = static_cast<uint32_t>((kPow3Packed >> (8 * k)) & 0xFFu);
+  return (((b * p) & 0xFFu) * 3u) >> 8;
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __restrict__ blocks,
+                                                             const int32_t* __restrict__ row_ids, int64_t n_out,
+                                                             void* __restrict__ out, int64_t n, int nb,
+                                                             unsigned* status) {
+  pdl_wait();  // blocks and row ids may come from the previous kernel
+  const int lane = threadIdx.x & 31;
+  const int64_t units = n_out * nb;
+  const int64_t wstride = static_cast<int64_t>(gridDim.x) * kDqWarps;
+  // Byte offset of this lane's first byte within the block, and its digit(s).
+  int boff, dig;
+  if (lane < 20) {
+    boff = 8 * (lane & 3);
+    dig = lane >> 2;
+  } else if (lane < 30) {
+    boff = 32 + 8 * ((lane - 20) & 1);
+    dig = (lane - 20) >> 1;
+  } else {
+    boff = 48;              // qh[0..3], digits 2 (lane - 30) and 2 (lane - 30) + 1
+    dig = 2 * (lane - 30);
+  }
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * kDqWarps + (threadIdx.x >> 5); u < units; u += wstride) {
+    const int64_t orow = u / nb;
+    const int b = static_cast<int>(u - orow * nb);
+    int64_t srow = orow;
+    if (row_ids) {
+      srow = __ldg(row_ids + orow);
+      if (srow < 0 || srow >= n) {
+        if (lane == 0 && b == 0) raise_status(status, kStatusBadId);
+        continue;  // the output row is left untouched
+      }
+    }
+    const uint8_t* blk = blocks + (srow * nb + b) * kBlockBytes;  // 2-byte aligned
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
+    const float dw = __half2float(__ushort_as_half(__ldg(h + 26)));
+    uint32_t by[8];
+    if (lane < 30) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t v = __ldg(h + (boff >> 1) + i);
+        by[2 * i] = v & 0xFFu;
+        by[2 * i + 1] = v >> 8;
+      }
+    } else {
+      const uint32_t v0 = __ldg(h + 24), v1 = __ldg(h + 25);
+      by[0] = by[4] = v0 & 0xFFu;
+      by[1] = by[5] = v0 >> 8;
+      by[2] = by[6] = v1 & 0xFFu;
+      by[3] = by[7] = v1 >> 8;
+    }
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t k = lane < 30 ? static_cast<uint32_t>(dig) : static_cast<uint32_t>(dig + (i >> 2));
+      v[i] = static_cast<float>(static_cast<int>(digit_of(by[i], k)) - 1) * dw;  // exact: +-d or 0
+    }
+    const int64_t e0 = orow * static_cast<int64_t>(nb) * kQK + static_cast<int64_t>(b) * kQK + 8 * lane;
+    if (F16) {
+      uint4 o;
+      o.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0]))) | (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1]))) << 16);
+      o.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[2]))) | (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[3]))) << 16);
+      o.z = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[4]))) | (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[5]))) << 16);
+      o.w = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[6]))) | (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[7]))) << 16);
+      __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + e0), o);
+    } else {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + e0);
+      __stcs(o, make_float4(v[0], v[1], v[2], v[3]));
+      __stcs(o + 1, make_float4(v[4], v[5], v[6], v[7]));
+    }
+  }
+}
+
+}  // namespace
+
+int launch_dequant(const uint8_t* blocks, const int32_t* row_ids, int64_t n_out, void* out, int64_t n, int64_t k,
+                   bool f16, cudaStream_t s, unsigned* status) {
+  const DeviceInfo& di = device_info();
+  const int nb = static_cast<int>(k / kQK);
+  const int64_t warps = n_out * nb;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((warps + kDqWarps - 1) / kDqWarps,
+                                                               static_cast<int64_t>(di.num_sms) * 16));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kDqThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = f16 ? cudaLaunchKernelEx(&cfg, dequant_kernel<true>, blocks, row_ids, n_out, out, n, nb, status)
+                            : cudaLaunchKernelEx(&cfg, dequant_kernel<false>, blocks, row_ids, n_out, out, n, nb, status);
+  return cuda_ok(e) ? TQ1_OK : TQ1_ERR_CUDA;
+}
+
+}  // namespace tq1

@@ -45,6 +45,11 @@ int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float*
 int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
                 unsigned* status);
 
+// Rows of TQ1_0 blocks to fp32 (f16 = false) or fp16 values: out row i is
+// source row row_ids[i] (row_ids == nullptr: row i).
+int launch_dequant(const uint8_t* blocks, const int32_t* row_ids, int64_t n_out, void* out, int64_t n, int64_t k,
+                   bool f16, cudaStream_t s, unsigned* status);
+
 // Workspace layout of the routing table (int32 words):
 //   [0]                   n_active
 //   [1, 1+E+1)            expert bounds (exclusive prefix sum of counts)

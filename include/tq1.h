@@ -122,6 +122,30 @@ int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t 
                      void* stream);
 
 /*
+ * Dequantise TQ1_0 rows: out[r][j] = d_w(r, j/256) * trit(r, j), the value the
+ * block encodes (fp32 when out_f16 == 0, else fp16; both exact, since the
+ * scale is an fp16 value and the trit is -1, 0 or +1).
+ *   blocks: [n][k/256] TQ1_0;  out: [n][k] fp32 or fp16, 16-byte aligned.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Current behavior" (the CPU
+ * dequantize_row walk: each packed byte amortised over its trits, element
+ * order of the block) and "Upstream state" (the dequant shader that ships with
+ * the Vulkan mat-vec).
+ */
+int tq1_dequantize_rows(const void* blocks, void* out, int64_t n, int64_t k, int out_f16, void* stream);
+
+/*
+ * Gather dequantised rows (get_rows, e.g. an embedding lookup):
+ * out[i][:] = row row_ids[i] of the n x k TQ1_0 matrix, i < n_ids, fp32 or
+ * fp16 as in tq1_dequantize_rows.  An id outside [0, n) leaves its output row
+ * untouched and sets TQ1_ERR_BAD_ID in the device status (tq1_sync_status).
+ *   row_ids: int32 [n_ids] (device);  out: [n_ids][k].
+ * Source: PrismML-Eng/llama.cpp issue #139, "Upstream state" (get_rows for the
+ * format next to its mat-vec).
+ */
+int tq1_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n, int64_t k,
+                 int out_f16, void* stream);
+
+/*
  * Workspace bytes tq1_mmv_id needs for n_experts experts and t*top_k routed pairs.
  */
 size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k);

@@ -127,6 +127,13 @@ def tq1_decode_rows(blocks: np.ndarray, n: int, k: int) -> tuple[np.ndarray, np.
     return trits, scales
 
 
+def tq1_dequantize_rows(blocks: np.ndarray, n: int, k: int) -> np.ndarray:
+    """Values the blocks encode, fp32 [n][k]: trit * d per element (the decode
+    above, scaled by its block's fp16 scale; exact in fp32)."""
+    trits, scales = tq1_decode_rows(blocks, n, k)
+    return (trits.astype(np.float32).reshape(n, k // QK, QK) * scales[:, :, None]).reshape(n, k)
+
+
 def q8_1_quantize(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     t, k = x.shape

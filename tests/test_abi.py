@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_id", "tq1_mmv_partials",
-                 "tq1_mmv_id_workspace_size", "tq1_sync_status", "tq1_status_string"):
+                 "tq1_mmv_id_workspace_size", "tq1_sync_status", "tq1_status_string", "tq1_dequantize_rows",
+                 "tq1_get_rows"):
         assert want in names
 
 
@@ -81,3 +82,15 @@ def test_other_host_checks(lib):
     assert lib.tq1_mmv_id(FAKE, 0, FAKE, FAKE, FAKE, 16, 256, 2, 2, FAKE, ws, None) == -2
     assert lib.tq1_mmv_id(FAKE, 8, FAKE, None, FAKE, 16, 256, 2, 2, FAKE, ws, None) == -1
     assert lib.tq1_mmv_id(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 0, 2, FAKE, ws, None) == 0
+
+
+def test_dequant_host_checks(lib):
+    assert lib.tq1_dequantize_rows(FAKE, FAKE, 4, 100, 0, None) == -2
+    assert lib.tq1_dequantize_rows(FAKE, FAKE, -1, 256, 0, None) == -2
+    assert lib.tq1_dequantize_rows(None, FAKE, 4, 256, 0, None) == -1
+    assert lib.tq1_dequantize_rows(FAKE, FAKE + 8, 4, 256, 1, None) == -3
+    assert lib.tq1_dequantize_rows(None, None, 0, 256, 0, None) == 0
+    assert lib.tq1_get_rows(FAKE, None, 3, FAKE, 4, 256, 0, None) == -1
+    assert lib.tq1_get_rows(FAKE, FAKE, -1, FAKE, 4, 256, 0, None) == -2
+    assert lib.tq1_get_rows(FAKE, FAKE + 4, 3, FAKE, 4, 256, 0, None) == -3
+    assert lib.tq1_get_rows(None, None, 0, None, 4, 256, 0, None) == 0

@@ -136,3 +136,12 @@ def test_f32_from_f16_all_patterns():
             assert np.isnan(got)
         else:
             assert got == r and np.signbit(got) == np.signbit(r), h
+
+
+@pytest.mark.parametrize("p_zero", [1.0 / 3.0, 0.4])
+def test_dequantize_returns_the_synthetic_weights(p_zero):
+    # The generator draws fp32 weights that are exactly fp16(d) * trit, so the
+    # values the blocks encode are those weights, element for element.
+    p = synth.matvec(19, 1024, 1, p_zero=p_zero, seed=17)
+    blocks = orc.tq1_encode_rows(p.w)
+    np.testing.assert_array_equal(orc.tq1_dequantize_rows(blocks, p.n, p.k), p.w)
