@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kDqThreads = 256;
 constexpr int kDqWarps = kDqThreads / 32;
+constexpr int kDqUnits = 2;  // 256-blocks per warp whose loads are in flight together (4: fewer resident warps, slower)
 
 __device__ __forceinline__ uint32_t digit_of(uint32_t b, uint32_t k) {
   const uint32_t p = static_cast<uint32_t>((kPow3Packed >> (8 * k)) & 0xFFu);
@@ -52,53 +53,75 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
     boff = 48;              // qh[0..3], digits 2 (lane - 30) and 2 (lane - 30) + 1
     dig = 2 * (lane - 30);
   }
-  for (int64_t u = static_cast<int64_t>(blockIdx.x) * kDqWarps + (threadIdx.x >> 5); u < units; u += wstride) {
-    const int64_t orow = u / nb;
-    const int b = static_cast<int>(u - orow * nb);
-    int64_t srow = orow;
-    if (row_ids) {
-      srow = __ldg(row_ids + orow);
-      if (srow < 0 || srow >= n) {
-        if (lane == 0 && b == 0) raise_status(status, kStatusBadId);
-        continue;  // the output row is left untouched
+  // kDqUnits units per iteration: their loads are in flight together.
+  for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * kDqWarps + (threadIdx.x >> 5); u0 < units;
+       u0 += kDqUnits * wstride) {
+    uint32_t hw[kDqUnits][5];  // per unit: 4 halfwords of the lane's bytes, the fp16 scale
+    int64_t orow[kDqUnits];
+    int bb[kDqUnits];
+    bool live[kDqUnits];
+#pragma unroll
+    for (int x = 0; x < kDqUnits; ++x) {
+      const int64_t u = u0 + x * wstride;
+      live[x] = u < units;
+      orow[x] = live[x] ? u / nb : 0;
+      bb[x] = static_cast<int>(u - orow[x] * nb);
+      int64_t srow = orow[x];
+      if (live[x] && row_ids) {
+        srow = __ldg(row_ids + orow[x]);
+        if (srow < 0 || srow >= n) {
+          if (lane == 0 && bb[x] == 0) raise_status(status, kStatusBadId);
+          live[x] = false;  // the output row is left untouched
+        }
+      }
+      if (live[x]) {
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(blocks + (srow * nb + bb[x]) * kBlockBytes);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hw[x][i] = __ldg(h + (boff >> 1) + i);
+        hw[x][4] = __ldg(h + 26);
       }
     }
-    const uint8_t* blk = blocks + (srow * nb + b) * kBlockBytes;  // 2-byte aligned
-    const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
-    const float dw = __half2float(__ushort_as_half(__ldg(h + 26)));
-    uint32_t by[8];
-    if (lane < 30) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t v = __ldg(h + (boff >> 1) + i);
-        by[2 * i] = v & 0xFFu;
-        by[2 * i + 1] = v >> 8;
+    for (int x = 0; x < kDqUnits; ++x) {
+      if (!live[x]) continue;
+      uint32_t by[8];
+      if (lane < 30) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          by[2 * i] = hw[x][i] & 0xFFu;
+          by[2 * i + 1] = hw[x][i] >> 8;
+        }
+      } else {  // qh[0..3] twice: digits dig and dig + 1
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          by[2 * i] = by[2 * i + 4] = hw[x][i] & 0xFFu;
+          by[2 * i + 1] = by[2 * i + 5] = hw[x][i] >> 8;
+        }
       }
-    } else {
-      const uint32_t v0 = __ldg(h + 24), v1 = __ldg(h + 25);
-      by[0] = by[4] = v0 & 0xFFu;
-      by[1] = by[5] = v0 >> 8;
-      by[2] = by[6] = v1 & 0xFFu;
-      by[3] = by[7] = v1 >> 8;
-    }
-    float v[8];
+      uint32_t dg[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t k = lane < 30 ? static_cast<uint32_t>(dig) : static_cast<uint32_t>(dig + (i >> 2));
-      v[i] = static_cast<float>(static_cast<int>(digit_of(by[i], k)) - 1) * dw;  // exact: +-d or 0
-    }
-    const int64_t e0 = orow * static_cast<int64_t>(nb) * kQK + static_cast<int64_t>(b) * kQK + 8 * lane;
-    if (F16) {
-      uint4 o;
-      o.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0]))) | (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1]))) << 16);
-      o.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[2]))) | (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[3]))) << 16);
-      o.z = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[4]))) | (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[5]))) << 16);
-      o.w = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[6]))) | (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[7]))) << 16);
-      __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + e0), o);
-    } else {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + e0);
-      __stcs(o, make_float4(v[0], v[1], v[2], v[3]));
-      __stcs(o + 1, make_float4(v[4], v[5], v[6], v[7]));
+      for (int i = 0; i < 8; ++i)
+        dg[i] = digit_of(by[i], lane < 30 ? static_cast<uint32_t>(dig) : static_cast<uint32_t>(dig + (i >> 2)));
+      const int64_t e0 = orow[x] * static_cast<int64_t>(nb) * kQK + static_cast<int64_t>(bb[x]) * kQK + 8 * lane;
+      const uint32_t h16 = hw[x][4];
+      if (F16) {
+        // fp16 values by byte permute from the table {-d, 0, +d}: a digit
+        // pair (a, b) selects bytes 2a, 2a+1, 2b, 2b+1 (selector
+        // 34 * (a + 256 b) + 0x1010).
+        const uint32_t tlo = h16 ^ 0x8000u, thi = h16;
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = __byte_perm(tlo, thi, (dg[2 * i] | (dg[2 * i + 1] << 8)) * 34u + 0x1010u);
+        __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + e0), make_uint4(o[0], o[1], o[2], o[3]));
+      } else {
+        const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(h16)));
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = dg[i] == 1u ? 0.0f : (dg[i] == 2u ? dw : -dw);  // exact
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + e0);
+        __stcs(o, make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(o + 1, make_float4(v[4], v[5], v[6], v[7]));
+      }
     }
   }
 }
