@@ -63,6 +63,7 @@ def library() -> ctypes.CDLL:
         lib.q8_1_quantize_acts.argtypes = [P, P, I64, I64, P]
         lib.tq1_mmv.argtypes = [P, P, P, I64, I64, I64, P]
         lib.tq1_mmv_partials.argtypes = [P, P, P, I64, I64, I64, P]
+        lib.tq1_mmv_add.argtypes = [P, P, P, P, I64, I64, I64, P]
         lib.tq1_mmv_id_workspace_size.restype = SZ
         lib.tq1_mmv_id_workspace_size.argtypes = [I64, I64, I64]
         lib.tq1_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
@@ -70,8 +71,8 @@ def library() -> ctypes.CDLL:
         lib.tq1_dequantize_rows.argtypes = [P, P, I64, I64, ctypes.c_int, P]
         lib.tq1_get_rows.argtypes = [P, P, I64, P, I64, I64, ctypes.c_int, P]
         lib.tq1_sync_status.argtypes = [P]
-        for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_partials", "tq1_mmv_id",
-                     "tq1_mmv_id_noalloc", "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status"):
+        for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_add", "tq1_mmv_partials",
+                     "tq1_mmv_id", "tq1_mmv_id_noalloc", "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -122,6 +123,12 @@ def q8_1_quantize_acts(x, q8, t: int, k: int, stream=None) -> None:
 
 def tq1_mmv(blocks, q8, y, n: int, k: int, t: int, stream=None) -> None:
     _check(library().tq1_mmv(_addr(blocks), _addr(q8), _addr(y), n, k, t, _stream(stream)), "tq1_mmv")
+
+
+def tq1_mmv_add(blocks, q8, res, y, n: int, k: int, t: int, stream=None) -> None:
+    """y = res + W x (res may be y itself)."""
+    _check(library().tq1_mmv_add(_addr(blocks), _addr(q8), _addr(res), _addr(y), n, k, t, _stream(stream)),
+           "tq1_mmv_add")
 
 
 def tq1_mmv_partials(blocks, q8, part, n: int, k: int, t: int, stream=None) -> None:

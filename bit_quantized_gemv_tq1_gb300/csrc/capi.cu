@@ -139,12 +139,13 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
 }
 
 static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* part, int64_t n, int64_t k,
-                      int64_t t, void* stream) {
+                      int64_t t, void* stream, const float* res = nullptr) {
   int rc = check_mmv_shape(n, k, t);
   if (rc != TQ1_OK) return rc;
   if (n == 0 || t == 0) return TQ1_OK;
   if (!blocks || !q8 || (!y && !part)) return TQ1_ERR_NULL;
-  if (misaligned(blocks) || misaligned(q8) || (y && misaligned(y)) || (part && misaligned(part)))
+  if (misaligned(blocks) || misaligned(q8) || (y && misaligned(y)) || (part && misaligned(part)) ||
+      (res && misaligned(res)))
     return TQ1_ERR_ALIGN;
   if (k > kMaxK) return TQ1_ERR_UNSUPPORTED;
   unsigned* st = status_ptr();
@@ -154,17 +155,17 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
   const uint8_t* a = static_cast<const uint8_t*>(q8);
   const int64_t q8_row = (k / kQK8) * kQ8Bytes;
   if (y && t >= kTileMinT) {
-    rc = launch_tile(w, a, y, n, k, t, s, st);
+    rc = launch_tile(w, a, y, n, k, t, s, st, res);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the dp4a kernels below
   }
   if (y && t <= 4) {
-    rc = launch_mmv_small(w, a, y, n, k, t, s, st);
+    rc = launch_mmv_small(w, a, y, n, k, t, s, st, res);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
   }
   for (int64_t c0 = 0; c0 < t; c0 += 32) {
     const int64_t tc = t - c0 < 32 ? t - c0 : 32;
     rc = launch_mmv(w, a + c0 * q8_row, y ? y + c0 * n : nullptr, part ? part + c0 * n * (k / kQK8) : nullptr, n,
-                    k, tc, s, st);
+                    k, tc, s, st, res ? res + c0 * n : nullptr);
     if (rc != TQ1_OK) return rc;
   }
   return TQ1_OK;
@@ -172,6 +173,12 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
 
 int tq1_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream) {
   return mmv_common(blocks, q8, y, nullptr, n, k, t, stream);
+}
+
+int tq1_mmv_add(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
+                void* stream) {
+  if (!res && n > 0 && t > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;
+  return mmv_common(blocks, q8, y, nullptr, n, k, t, stream, res);
 }
 
 int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,

@@ -44,6 +44,7 @@ struct MmvArgs {
   const uint8_t* w;   // weight blocks (MoE: expert 0's first block)
   const uint8_t* q8;  // Q8_1 activations [t][k/32]
   float* y;
+  const float* res;   // optional residual added to y (same layout), or nullptr
   int32_t* part;
   unsigned* status;
   int64_t n, k, t;
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const MmvArgs a) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(acc + a.rt * CMAX + ((a.rt * CMAX) & 1));
   __shared__ const uint8_t* s_qrow[CMAX];
   __shared__ float* s_yrow[CMAX];
+  __shared__ const float* s_rrow[CMAX];
   __shared__ int s_abort;
 
   const int tid = threadIdx.x;
@@ -273,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const MmvArgs a) {
         }
         s_qrow[tid] = a.q8 + token * nq * kQ8Bytes;
         s_yrow[tid] = (MODE == kModePartials) ? nullptr : a.y + orow * a.n + T.row0;
+        s_rrow[tid] = (MODE == kModeY && a.res) ? a.res + orow * a.n + T.row0 : nullptr;
       }
       for (int i = tid; i < a.rt * CMAX; i += kThreads) acc[i] = 0.0f;
       __syncthreads();
@@ -362,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const MmvArgs a) {
       for (int task = tid; task < rows * T.ncols; task += kThreads) {
         const int c = task / rows;
         const int r = task - c * rows;
-        s_yrow[c][r] = acc[r * CMAX + c];
+        s_yrow[c][r] = acc[r * CMAX + c] + (s_rrow[c] ? s_rrow[c][r] : 0.0f);
       }
       __syncthreads();
     }
@@ -439,12 +442,13 @@ static int rung_for(int64_t t) {
 }
 
 int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int64_t n, int64_t k, int64_t t,
-               cudaStream_t s, unsigned* status) {
+               cudaStream_t s, unsigned* status, const float* res) {
   const DeviceInfo& di = device_info();
   MmvArgs a = {};
   a.w = w;
   a.q8 = q8;
   a.y = y;
+  a.res = res;
   a.part = part;
   a.status = status;
   a.n = n;

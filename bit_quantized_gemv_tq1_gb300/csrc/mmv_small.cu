@@ -76,6 +76,7 @@ struct SmallArgs {
   const uint8_t* w;
   const uint8_t* q8;
   float* y;
+  const float* res;     // optional residual added to y (same layout), or nullptr
   unsigned* status;
   int64_t n;
   int t;                // active columns (<= C)
@@ -89,7 +90,7 @@ struct SmallArgs {
 
 }  // namespace
 
-template <int C>
+template <int C, bool RES>
 __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(const SmallArgs a) {
   constexpr int kThreads = SmallCfg<C>::kThreads;
   constexpr int kWarps = kThreads / 32;
@@ -269,7 +270,8 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
     for (int row = tid; row < rows; row += kThreads) {
       float v = 0.0f;
       for (int kc = 0; kc < nkc; ++kc) v += part[(static_cast<size_t>(row) * nkc + kc) * C + c];
-      a.y[static_cast<int64_t>(c) * a.n + r0 + row] = v;
+      const int64_t yi = static_cast<int64_t>(c) * a.n + r0 + row;
+      a.y[yi] = RES ? v + a.res[yi] : v;
     }
 }
 
@@ -283,7 +285,7 @@ static size_t small_smem(int nb, int rows_cta, uint32_t slab_bytes) {
   return b;
 }
 
-template <int C>
+template <int C, bool RES>
 static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   const DeviceInfo& di = device_info();
   const size_t bytes = small_smem<C>(a.nb, a.rows_cta, a.slab_bytes);
@@ -291,14 +293,14 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
   if (max_dyn[di.device] == 0) {
     cudaFuncAttributes fa{};
-    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C>))) return TQ1_ERR_CUDA;
+    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C, RES>))) return TQ1_ERR_CUDA;
     const size_t lim = di.max_smem_optin - fa.sharedSizeBytes;
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(lim))))
       return TQ1_ERR_CUDA;
     // Two CTAs of consecutive calls share an SM: ask for the largest
     // shared-memory carveout so the L1 split never limits residency.
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
       return TQ1_ERR_CUDA;
     max_dyn[di.device] = lim;
   }
@@ -313,19 +315,20 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_small_kernel<C>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_small_kernel<C, RES>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
 }
 
 // Returns TQ1_ERR_UNSUPPORTED (launching nothing) when the shape does not
 // fit this kernel's staging; the caller then uses the general kernel.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status) {
+                     unsigned* status, const float* res) {
   if (t < 1 || t > 4) return TQ1_ERR_UNSUPPORTED;
   const DeviceInfo& di = device_info();
   SmallArgs a = {};
   a.w = w;
   a.q8 = q8;
   a.y = y;
+  a.res = res;
   a.status = status;
   a.n = n;
   a.t = static_cast<int>(t);
@@ -346,9 +349,12 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.nkc_magic = a.nkc > 1 ? static_cast<uint32_t>(((uint64_t{1} << 32) + a.nkc - 1) / a.nkc) : 0u;
   if (static_cast<int64_t>(a.rows_round / kRowsPerTask) * a.nkc >= (int64_t{1} << 20)) return TQ1_ERR_UNSUPPORTED;
   switch (rung) {
-    case 1: return launch_small_rung<1>(a, static_cast<int>(grid), s);
-    case 2: return launch_small_rung<2>(a, static_cast<int>(grid), s);
-    default: return launch_small_rung<4>(a, static_cast<int>(grid), s);
+    case 1: return res ? launch_small_rung<1, true>(a, static_cast<int>(grid), s)
+                       : launch_small_rung<1, false>(a, static_cast<int>(grid), s);
+    case 2: return res ? launch_small_rung<2, true>(a, static_cast<int>(grid), s)
+                       : launch_small_rung<2, false>(a, static_cast<int>(grid), s);
+    default: return res ? launch_small_rung<4, true>(a, static_cast<int>(grid), s)
+                        : launch_small_rung<4, false>(a, static_cast<int>(grid), s);
   }
 }
 

@@ -123,6 +123,7 @@ struct TileCfg {
 struct TileArgs {
   const float* scale;  // per-token 2^e_t (prep kernel output)
   float* y;
+  const float* res;    // optional residual added to y (same layout), or nullptr
   unsigned* status;
   int n, k, t, t_pad;
   int tiles_m, tiles_n;
@@ -664,7 +665,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
           for (int jj = 0; jj < C::kChunk; ++jj) {
             const int tl = c0 + jj, tok = tok0 + tl;
             const float v = (__uint_as_float(vh[jj]) + __uint_as_float(vl[jj])) * tsc[tl];
-            if (row < a.n && tok < a.t) a.y[static_cast<int64_t>(tok) * a.n + row] = v;
+            if (row < a.n && tok < a.t) {
+              const int64_t yi = static_cast<int64_t>(tok) * a.n + row;
+              a.y[yi] = a.res ? v + a.res[yi] : v;
+            }
           }
         }
       }
@@ -797,7 +801,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
 #pragma unroll
           for (int src = 0; src < kMaxSplit; ++src)  // rank order
             if (src < S) v += red[(src * slice_max + ri) * TOK + tl];
-          a.y[static_cast<int64_t>(tok0 + tl) * a.n + row0 + r_lo + ri] = v;
+          const int64_t yi = static_cast<int64_t>(tok0 + tl) * a.n + row0 + r_lo + ri;
+          a.y[yi] = a.res ? v + a.res[yi] : v;
         }
       }
     }
@@ -947,13 +952,14 @@ int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms
 }  // namespace
 
 int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                unsigned* status) {
+                unsigned* status, const float* res) {
   if (n > (int64_t{1} << 30) || t > (int64_t{1} << 24) || k > (int64_t{1} << 30)) return TQ1_ERR_UNSUPPORTED;
   // The weight map's row stride must be a multiple of 16 bytes.
   if (((k / kQK) * kBlockBytes) % 16 != 0) return TQ1_ERR_UNSUPPORTED;
   const DeviceInfo& di = device_info();
   TileArgs a = {};
   a.y = y;
+  a.res = res;
   a.status = status;
   a.n = static_cast<int>(n);
   a.k = static_cast<int>(k);

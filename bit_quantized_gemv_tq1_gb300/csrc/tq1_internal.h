@@ -26,14 +26,14 @@ int launch_quantize_rows(const float* w, uint8_t* blocks, int64_t n, int64_t k, 
 int launch_quantize_acts(const float* x, uint8_t* q8, int64_t t, int64_t k, cudaStream_t s);
 
 // y[c][r] (y != nullptr) or int32 partials part[c][r][k/32] (part != nullptr)
-// for columns c < t <= 32.
+// for columns c < t <= 32.  `res` (optional, y's layout) is added to y.
 int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int64_t n, int64_t k, int64_t t,
-               cudaStream_t s, unsigned* status);
+               cudaStream_t s, unsigned* status, const float* res = nullptr);
 
 // Decode-path kernel for 1 <= t <= 4 columns.  Returns TQ1_ERR_UNSUPPORTED
 // without launching when the shape does not fit its staging.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status);
+                     unsigned* status, const float* res = nullptr);
 
 // Expert-routed mat-vec over a compacted routing table in `ws` (general
 // dp4a kernel).
@@ -43,7 +43,7 @@ int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float*
 // y[c][r] for any t on the tensor cores (tcgen05): 128-row tiles, split-K
 // over a thread-block cluster when the tiles alone cannot fill the GPU.
 int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                unsigned* status);
+                unsigned* status, const float* res = nullptr);
 
 // Rows of TQ1_0 blocks to fp32 (f16 = false) or fp16 values: out row i is
 // source row row_ids[i] (row_ids == nullptr: row i).

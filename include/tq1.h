@@ -115,6 +115,19 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
 int tq1_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream);
 
 /*
+ * Mat-vec with a residual added in the kernel's epilogue:
+ *   y[c][r] = res[c][r] + sum_k w[r][k] * x[c][k]
+ * (one fp32 add per output after the dot product; the same kernels, rungs and
+ * accumulation as tq1_mmv).  res: fp32 [t][n], device, 16-byte aligned; it may
+ * be y itself (in-place update).  Errors as tq1_mmv; res == NULL is
+ * TQ1_ERR_NULL.
+ * Source: Neroued/ninfer issue #293 (the linear_add rungs: a linear layer
+ * fused with its residual add).
+ */
+int tq1_mmv_add(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
+                void* stream);
+
+/*
  * Debug entry: the exact integer partials part[c][r][j] = I_j (int32,
  * [t][n][k/32]) that tq1_mmv scales.  t <= 32.  Bit-exact by construction.
  */

@@ -156,3 +156,22 @@ def test_empty_is_noop():
     L.tq1_mmv(0, 0, 0, 0, 256, 1)
     L.tq1_mmv(0, 0, 0, 7, 256, 0)
     assert L.tq1_sync_status() == 0
+
+
+@pytest.mark.parametrize("n,k,t", [(300, 2048, 1), (5120, 6144, 2), (77, 1024, 4), (257, 2048, 5), (129, 4096, 9),
+                                   (300, 2048, 40)])
+def test_mmv_add_residual(n, k, t):
+    # Every route (decode rungs, general kernel, tile path with split-K and
+    # persistent tiles): y = res + W x, separately and in place.
+    p = synth.matvec(n, k, t, p_zero=0.4, seed=n + 7 * t)
+    blocks, q8 = G.quantize_rows(p.w), G.quantize_acts(p.x)
+    res = np.random.default_rng(t).standard_normal((t, n)).astype(np.float32)
+    L, torch = G.lib(), G.torch()
+    y = torch.full((t, n), float("nan"), dtype=torch.float32, device="cuda")
+    r = G.dev(res)
+    L.tq1_mmv_add(blocks, q8, r, y, n, k, t)
+    ref = orc.mmv_f64(orc.tq1_encode_rows(p.w), orc.q8_1_quantize(p.x), n, k, t) + res.astype(np.float64)
+    G.assert_close(G.host(y), ref)
+    L.tq1_mmv_add(blocks, q8, r, r, n, k, t)  # in place
+    np.testing.assert_array_equal(G.host(r), G.host(y))
+    assert L.tq1_sync_status() == 0
