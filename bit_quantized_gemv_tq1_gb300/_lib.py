@@ -67,12 +67,14 @@ def library() -> ctypes.CDLL:
         lib.tq1_mmv_id_workspace_size.restype = SZ
         lib.tq1_mmv_id_workspace_size.argtypes = [I64, I64, I64]
         lib.tq1_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
+        lib.tq1_mmv_id_slots.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq1_mmv_id_noalloc.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P]
         lib.tq1_dequantize_rows.argtypes = [P, P, I64, I64, ctypes.c_int, P]
         lib.tq1_get_rows.argtypes = [P, P, I64, P, I64, I64, ctypes.c_int, P]
         lib.tq1_sync_status.argtypes = [P]
         for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_add", "tq1_mmv_partials",
-                     "tq1_mmv_id", "tq1_mmv_id_noalloc", "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status"):
+                     "tq1_mmv_id", "tq1_mmv_id_slots", "tq1_mmv_id_noalloc", "tq1_dequantize_rows", "tq1_get_rows",
+                     "tq1_sync_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -146,6 +148,15 @@ def tq1_mmv_id(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, t: int
         ws_bytes = ws.numel() * ws.element_size()
     _check(library().tq1_mmv_id(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(y), n, k, t, top_k,
                                 _addr(ws), ws_bytes, _stream(stream)), "tq1_mmv_id")
+
+
+def tq1_mmv_id_slots(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, t: int, top_k: int, ws,
+                     ws_bytes: int | None = None, stream=None) -> None:
+    """tq1_mmv_id with one Q8_1 activation row per (token, slot): q8 [t][top_k][k/32]."""
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size()
+    _check(library().tq1_mmv_id_slots(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(y), n, k, t,
+                                      top_k, _addr(ws), ws_bytes, _stream(stream)), "tq1_mmv_id_slots")
 
 
 def tq1_mmv_id_noalloc(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, t: int, top_k: int,

@@ -218,8 +218,11 @@ size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k) {
   return (words * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
 }
 
-int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
-               int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+static int mmv_id_common(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+                         int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream,
+                         bool per_slot) {
   int rc = check_mmv_shape(n, k, t);
   if (rc != TQ1_OK) return rc;
   if (n_experts <= 0 || top_k < 0) return TQ1_ERR_SHAPE;
@@ -235,19 +238,32 @@ int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, con
   int32_t* table = static_cast<int32_t*>(ws);
   const uint8_t* w = static_cast<const uint8_t*>(expert_blocks);
   const uint8_t* a = static_cast<const uint8_t*>(q8);
+  const int act_div = per_slot ? 1 : static_cast<int>(top_k);
   MoePlan plan{};
   // A few pairs (decode): no routing table, each CTA reads its pair's id.
   if (t * top_k <= kMoeDirectMaxPairs && moe_direct_plan(n, k, t * top_k, &plan))
-    return launch_moe_direct(w, a, ids, y, n, k, top_k, n_experts, t * top_k, plan, s, st);
+    return launch_moe_direct(w, a, ids, y, n, k, top_k, n_experts, t * top_k, plan, s, st, act_div);
   const bool small = moe_small_plan(n, k, t * top_k, n_experts, &plan);
   rc = launch_moe_compact(ids, t, top_k, n_experts, small ? plan.chunk : 1, small ? plan.row_blocks : 1, table, s,
                           st);
   if (rc != TQ1_OK) return rc;
   if (small) {
-    rc = launch_moe_small(w, a, y, n, k, top_k, n_experts, t * top_k, plan, table, s, st);
+    rc = launch_moe_small(w, a, y, n, k, top_k, n_experts, t * top_k, plan, table, s, st, act_div);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
   }
-  return launch_mmv_id(w, n_experts, a, y, n, k, t, top_k, table, s, st);
+  return launch_mmv_id(w, n_experts, a, y, n, k, t, top_k, table, s, st, act_div);
+}
+
+extern "C" {
+
+int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+               int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream) {
+  return mmv_id_common(expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, ws, ws_bytes, stream, false);
+}
+
+int tq1_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+                     int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream) {
+  return mmv_id_common(expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, ws, ws_bytes, stream, true);
 }
 
 int tq1_sync_status(void* stream) {

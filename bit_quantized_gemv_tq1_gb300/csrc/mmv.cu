@@ -52,6 +52,7 @@ struct MmvArgs {
   int cc;             // columns per activation staging chunk
   int rt;             // rows per tile
   int top_k;
+  int act_div;        // MoE: activation row of a pair = pair / act_div
   int64_t n_experts;
   const int32_t* table;  // MoE routing table (see tq1_internal.h)
 };
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const MmvArgs a) {
           const int32_t* pairs = active + a.n_experts;
           const int e = active[T.slot];
           const int64_t pair = pairs[bounds[e] + T.col0 + tid];
-          token = pair / a.top_k;
+          token = pair / a.act_div;
           orow = pair;
         } else {
           token = T.col0 + tid;
@@ -472,9 +473,10 @@ int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int
 }
 
 int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float* y, int64_t n, int64_t k,
-                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status) {
+                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status, int act_div) {
   const DeviceInfo& di = device_info();
   MmvArgs a = {};
+  a.act_div = act_div;
   a.w = w;
   a.q8 = q8;
   a.y = y;

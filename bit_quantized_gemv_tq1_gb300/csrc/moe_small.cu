@@ -43,6 +43,7 @@ struct MoeArgs {
   const int32_t* table;  // compacted routing table (layout in tq1_internal.h)
   int64_t n;
   int n_experts, top_k, nb, nkc;
+  int act_div;           // activation row of a pair = pair / act_div (top_k, or 1: one row per pair)
   int rows;              // rows per task (multiple of 4)
   int row_blocks;        // row ranges per expert
   int64_t pairs;         // t * top_k
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kMThreads, 2) moe_small_kernel(const MoeArgs a
         const int c = i / (nb * 8);
         const int rem = i - c * nb * 8;
         const int b = rem >> 3, j = rem & 7;
-        const int64_t token = s_pair[c] / a.top_k;
+        const int64_t token = s_pair[c] / a.act_div;
         fill_precord_chunk(a.q8 + (token * nb * 8 + b * 8 + j) * kQ8Bytes, recs + c * rstride + b * kPRec, j);
       }
     }
@@ -218,6 +219,7 @@ struct DirectArgs {
   unsigned* status;
   int64_t n;
   int n_experts, top_k, nb, nkc;
+  int act_div;           // activation row of a pair = pair / act_div (top_k, or 1: one row per pair)
   int rows;              // rows per CTA (multiple of 4)
   int row_blocks;        // CTAs per pair
   uint32_t slab_bytes;
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectAr
     }
   }
   // Activation records of the pair's token while the weights arrive.
-  const int64_t token = pair / a.top_k;
+  const int64_t token = pair / a.act_div;
   for (int i = tid; i < nb * 8; i += kDThreads)
     fill_precord_chunk(a.q8 + (token * nb * 8 + i) * kQ8Bytes, recs + (i >> 3) * kPRec, i & 7);
   __syncthreads();
@@ -342,9 +344,10 @@ bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan) {
 
 int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
                       int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
-                      unsigned* status) {
+                      unsigned* status, int act_div) {
   const DeviceInfo& di = device_info();
   DirectArgs a = {};
+  a.act_div = act_div;
   a.w = w;
   a.q8 = q8;
   a.ids = ids;
@@ -408,9 +411,10 @@ bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoeP
 
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
-                     unsigned* status) {
+                     unsigned* status, int act_div) {
   const DeviceInfo& di = device_info();
   MoeArgs a = {};
+  a.act_div = act_div;
   a.w = w;
   a.q8 = q8;
   a.y = y;

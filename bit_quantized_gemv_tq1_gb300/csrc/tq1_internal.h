@@ -37,8 +37,10 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
 
 // Expert-routed mat-vec over a compacted routing table in `ws` (general
 // dp4a kernel).
+// `act_div`: the activation row of routed pair p is p / act_div (top_k: one
+// row per token shared by its slots; 1: one row per (token, slot)).
 int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float* y, int64_t n, int64_t k,
-                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status);
+                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status, int act_div);
 
 // y[c][r] for any t on the tensor cores (tcgen05): 128-row tiles, split-K
 // over a thread-block cluster when the tiles alone cannot fill the GPU.
@@ -83,9 +85,9 @@ bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoeP
 bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan);
 int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
                       int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
-                      unsigned* status);
+                      unsigned* status, int act_div);
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
-                     unsigned* status);
+                     unsigned* status, int act_div);
 
 }  // namespace tq1

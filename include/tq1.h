@@ -184,6 +184,19 @@ int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, con
                int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Expert-routed mat-vec with one activation row per routed (token, slot) pair
+ * (the down-projection of an expert layer, whose input differs per slot):
+ *   y[c][s][r] = expert ids[c][s]'s matrix times activation row (c, s).
+ *   q8: [t][top_k][k/32] Q8_1.  Everything else, including the workspace and
+ * the error behaviour, as tq1_mmv_id.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Acceptance criteria" (MUL_MAT_ID
+ * cases); AMD-Ecosystem/llama.cpp PR #76, "Summary" (ids -> expert bounds ->
+ * compacted grid).
+ */
+int tq1_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+                     int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * tq1_mmv_id without a workspace argument, for callers that cannot allocate
  * device memory (inside a stream capture, under a fixed memory budget, in a
  * latency-critical loop, or from plain C with no allocator at hand).  The

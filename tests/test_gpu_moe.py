@@ -123,3 +123,27 @@ def test_deterministic_repeat():
     a, _ = _mmv_id(blocks, m, m.ids, q8)
     b, _ = _mmv_id(blocks, m, m.ids, q8)
     np.testing.assert_array_equal(G.host(a), G.host(b))
+
+
+@pytest.mark.parametrize("t,top_k,n_experts", [(1, 8, 16), (3, 4, 6), (40, 2, 5)])
+def test_per_slot_activations(t, top_k, n_experts):
+    # One activation row per (token, slot): direct mode (few pairs) and the
+    # compacted path (80 pairs).
+    m = synth.moe(n_experts, 160, 1024, t, top_k, seed=9 + t)
+    blocks = _experts_gpu(m)
+    x = np.random.default_rng(t).standard_normal((t * top_k, m.k)).astype(np.float32)
+    q8 = G.quantize_acts(x)
+    L, torch = G.lib(), G.torch()
+    ws_bytes = L.tq1_mmv_id_workspace_size(m.n_experts, t, top_k)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    y = torch.full((t, top_k, m.n), float("nan"), dtype=torch.float32, device="cuda")
+    L.tq1_mmv_id_slots(blocks, m.n_experts, q8, G.dev(m.ids.astype(np.int32)), y, m.n, m.k, t, top_k, ws)
+    assert L.tq1_sync_status() == 0
+    ob = _oracle_blocks(m, np.unique(m.ids))
+    oq = orc.q8_1_quantize(x).reshape(t * top_k, -1)
+    ref = np.zeros((t, top_k, m.n))
+    for c in range(t):
+        for s in range(top_k):
+            e = int(m.ids[c, s])
+            ref[c, s] = orc.mmv_f64(ob[e], oq[c * top_k + s], m.n, m.k, 1)[0]
+    G.assert_close(G.host(y), ref)
