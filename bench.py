@@ -352,6 +352,7 @@ def run_ours(args, ws, rank, local):
         extra["prefill_c5"] = prefill_bench(lib, L, synth, dev, stream, capture, args)
         extra["moe_c4"] = moe_bench(lib, L, synth, dev, stream, capture, args)
         extra["dequant_c2"] = dequant_bench(lib, L, synth, dev, stream, capture, args)
+        extra["decode_chain_c2"] = fused_chain_bench(lib, L, synth, dev, stream, capture, args)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -442,6 +443,49 @@ def prefill_bench(lib, L, synth, dev, stream, capture, args) -> dict:
             "peak_tflops": peak, "frac": round(flops / (ms * 1e-3) / 1e12 / peak, 4),
             "note": "tflops counts the method's MACs once; the kernel issues each twice (fp16 hi and lo "
                     "parts of the activations); peak = measured bf16 dense (fp16 runs at the same rate)"}
+
+
+def fused_chain_bench(lib, L, synth, dev, stream, capture, args) -> dict:
+    """A decode chain where every mat-vec has its own fp32 activation row
+    (config 2's shape, R weight copies): q8_1_quantize_acts + tq1_mmv per call
+    against tq1_mmv_f32 (quantisation inside the mat-vec kernel)."""
+    import torch
+
+    c2 = synth.CONFIGS["c2"]
+    n, k = c2["n"], c2["k"]
+    wbytes = n * (k // QK) * BLOCK_BYTES
+    qbytes = (k // QK8) * Q8_BYTES
+    copies = 82
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2200)
+    blocks = torch.empty(copies * wbytes, dtype=torch.uint8, device=dev)
+    for l in range(copies):
+        w = synth.device_weights(n, k, c2["p_zero"], c2["d_lo"], c2["d_hi"], gen, dev)
+        L.tq1_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+        del w
+    x = synth.device_activations((copies, k), gen, dev)
+    q8 = torch.empty(copies * qbytes, dtype=torch.uint8, device=dev)
+    y = torch.empty((copies, n), dtype=torch.float32, device=dev)
+    bp, xp, qp, yp = blocks.data_ptr(), x.data_ptr(), q8.data_ptr(), y.data_ptr()
+
+    def two_step(s):
+        for l in range(copies):
+            assert lib.q8_1_quantize_acts(xp + l * k * 4, qp + l * qbytes, 1, k, s) == 0
+            assert lib.tq1_mmv(bp + l * wbytes, qp + l * qbytes, yp + l * n * 4, n, k, 1, s) == 0
+
+    def fused(s):
+        for l in range(copies):
+            assert lib.tq1_mmv_f32(bp + l * wbytes, xp + l * k * 4, yp + l * n * 4, n, k, 1, s) == 0
+
+    out = {"workload": "c2 N=5120 K=6144 T=1, each call its own fp32 activation row, 82 calls per chain"}
+    for name, fn in (("quantise_then_mmv", two_step), ("fused_mmv_f32", fused)):
+        g = capture(fn)
+        us = _time_graph(g, stream, 10) * 1e3 / copies
+        assert lib.tq1_sync_status(stream.cuda_stream) == 0
+        out[name] = {"us_per_call": round(us, 3), "gbs": round(alg_bytes(n, k, 1) / (us * 1e-6) / 1e9, 1)}
+        del g
+    del blocks, x, q8, y
+    return out
 
 
 def dequant_bench(lib, L, synth, dev, stream, capture, args) -> dict:

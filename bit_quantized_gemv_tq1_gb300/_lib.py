@@ -64,6 +64,7 @@ def library() -> ctypes.CDLL:
         lib.tq1_mmv.argtypes = [P, P, P, I64, I64, I64, P]
         lib.tq1_mmv_partials.argtypes = [P, P, P, I64, I64, I64, P]
         lib.tq1_mmv_add.argtypes = [P, P, P, P, I64, I64, I64, P]
+        lib.tq1_mmv_f32.argtypes = [P, P, P, I64, I64, I64, P]
         lib.tq1_mmv_id_workspace_size.restype = SZ
         lib.tq1_mmv_id_workspace_size.argtypes = [I64, I64, I64]
         lib.tq1_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
@@ -72,9 +73,9 @@ def library() -> ctypes.CDLL:
         lib.tq1_dequantize_rows.argtypes = [P, P, I64, I64, ctypes.c_int, P]
         lib.tq1_get_rows.argtypes = [P, P, I64, P, I64, I64, ctypes.c_int, P]
         lib.tq1_sync_status.argtypes = [P]
-        for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_add", "tq1_mmv_partials",
-                     "tq1_mmv_id", "tq1_mmv_id_slots", "tq1_mmv_id_noalloc", "tq1_dequantize_rows", "tq1_get_rows",
-                     "tq1_sync_status"):
+        for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_add", "tq1_mmv_f32",
+                     "tq1_mmv_partials", "tq1_mmv_id", "tq1_mmv_id_slots", "tq1_mmv_id_noalloc",
+                     "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -125,6 +126,11 @@ def q8_1_quantize_acts(x, q8, t: int, k: int, stream=None) -> None:
 
 def tq1_mmv(blocks, q8, y, n: int, k: int, t: int, stream=None) -> None:
     _check(library().tq1_mmv(_addr(blocks), _addr(q8), _addr(y), n, k, t, _stream(stream)), "tq1_mmv")
+
+
+def tq1_mmv_f32(blocks, x, y, n: int, k: int, t: int, stream=None) -> None:
+    """Decode mat-vec from fp32 activations, quantised to Q8_1 inside the kernel (t <= 4)."""
+    _check(library().tq1_mmv_f32(_addr(blocks), _addr(x), _addr(y), n, k, t, _stream(stream)), "tq1_mmv_f32")
 
 
 def tq1_mmv_add(blocks, q8, res, y, n: int, k: int, t: int, stream=None) -> None:

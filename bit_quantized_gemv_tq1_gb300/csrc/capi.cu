@@ -175,6 +175,19 @@ int tq1_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, 
   return mmv_common(blocks, q8, y, nullptr, n, k, t, stream);
 }
 
+int tq1_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t, void* stream) {
+  int rc = check_mmv_shape(n, k, t);
+  if (rc != TQ1_OK) return rc;
+  if (n == 0 || t == 0) return TQ1_OK;
+  if (!blocks || !x || !y) return TQ1_ERR_NULL;
+  if (misaligned(blocks) || misaligned(x) || misaligned(y)) return TQ1_ERR_ALIGN;
+  if (t > 4 || k > kMaxK) return TQ1_ERR_UNSUPPORTED;
+  unsigned* st = status_ptr();
+  if (!st) return TQ1_ERR_CUDA;
+  return launch_mmv_small(static_cast<const uint8_t*>(blocks), nullptr, y, n, k, t, static_cast<cudaStream_t>(stream),
+                          st, nullptr, x);
+}
+
 int tq1_mmv_add(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
                 void* stream) {
   if (!res && n > 0 && t > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;

@@ -77,6 +77,7 @@ struct SmallArgs {
   const uint8_t* q8;
   float* y;
   const float* res;     // optional residual added to y (same layout), or nullptr
+  const float* x;       // fp32 activations [t][k] quantised in the prologue (F32IN), else unused
   unsigned* status;
   int64_t n;
   int t;                // active columns (<= C)
@@ -90,7 +91,7 @@ struct SmallArgs {
 
 }  // namespace
 
-template <int C, bool RES>
+template <int C, bool RES, bool F32IN>
 __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(const SmallArgs a) {
   constexpr int kThreads = SmallCfg<C>::kThreads;
   constexpr int kWarps = kThreads / 32;
@@ -190,9 +191,24 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
   // the barrier measurably slowed the dot phase).
   {
     const int per_col = nb * 8, nchunks = a.t * per_col;
-    for (int i = tid; i < nchunks; i += kThreads) {
-      const int c = i / per_col, rem = i - c * per_col;
-      fill_precord_chunk(a.q8 + static_cast<int64_t>(i) * kQ8Bytes, recs + c * rstride + (rem >> 3) * kPRec, rem & 7);
+    if (F32IN) {
+      // Q8_1 quantisation fused into the prologue: two lanes per 32-element
+      // chunk of the fp32 activations (each CTA quantises the whole row);
+      // whole warps iterate so the pair shuffles always have every lane.
+      for (int base = warp * 32; base < 2 * nchunks; base += kThreads) {
+        const int i2 = base + lane;
+        const bool live = i2 < 2 * nchunks;
+        const int i = live ? i2 >> 1 : 0;
+        const int c = i / per_col, rem = i - c * per_col;
+        quantize_precord_half(a.x + static_cast<int64_t>(i) * kQK8, recs + c * rstride + (rem >> 3) * kPRec, rem & 7,
+                              i2 & 1, live);
+      }
+    } else {
+      for (int i = tid; i < nchunks; i += kThreads) {
+        const int c = i / per_col, rem = i - c * per_col;
+        fill_precord_chunk(a.q8 + static_cast<int64_t>(i) * kQ8Bytes, recs + c * rstride + (rem >> 3) * kPRec,
+                           rem & 7);
+      }
     }
   }
   bool abort = __syncthreads_or(!ok) != 0;
@@ -285,7 +301,7 @@ static size_t small_smem(int nb, int rows_cta, uint32_t slab_bytes) {
   return b;
 }
 
-template <int C, bool RES>
+template <int C, bool RES, bool F32IN>
 static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   const DeviceInfo& di = device_info();
   const size_t bytes = small_smem<C>(a.nb, a.rows_cta, a.slab_bytes);
@@ -293,14 +309,14 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
   if (max_dyn[di.device] == 0) {
     cudaFuncAttributes fa{};
-    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C, RES>))) return TQ1_ERR_CUDA;
+    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C, RES, F32IN>))) return TQ1_ERR_CUDA;
     const size_t lim = di.max_smem_optin - fa.sharedSizeBytes;
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(lim))))
       return TQ1_ERR_CUDA;
     // Two CTAs of consecutive calls share an SM: ask for the largest
     // shared-memory carveout so the L1 split never limits residency.
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
       return TQ1_ERR_CUDA;
     max_dyn[di.device] = lim;
   }
@@ -315,13 +331,13 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_small_kernel<C, RES>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_small_kernel<C, RES, F32IN>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
 }
 
 // Returns TQ1_ERR_UNSUPPORTED (launching nothing) when the shape does not
 // fit this kernel's staging; the caller then uses the general kernel.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status, const float* res) {
+                     unsigned* status, const float* res, const float* x) {
   if (t < 1 || t > 4) return TQ1_ERR_UNSUPPORTED;
   const DeviceInfo& di = device_info();
   SmallArgs a = {};
@@ -329,6 +345,7 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.q8 = q8;
   a.y = y;
   a.res = res;
+  a.x = x;
   a.status = status;
   a.n = n;
   a.t = static_cast<int>(t);
@@ -349,12 +366,15 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.nkc_magic = a.nkc > 1 ? static_cast<uint32_t>(((uint64_t{1} << 32) + a.nkc - 1) / a.nkc) : 0u;
   if (static_cast<int64_t>(a.rows_round / kRowsPerTask) * a.nkc >= (int64_t{1} << 20)) return TQ1_ERR_UNSUPPORTED;
   switch (rung) {
-    case 1: return res ? launch_small_rung<1, true>(a, static_cast<int>(grid), s)
-                       : launch_small_rung<1, false>(a, static_cast<int>(grid), s);
-    case 2: return res ? launch_small_rung<2, true>(a, static_cast<int>(grid), s)
-                       : launch_small_rung<2, false>(a, static_cast<int>(grid), s);
-    default: return res ? launch_small_rung<4, true>(a, static_cast<int>(grid), s)
-                        : launch_small_rung<4, false>(a, static_cast<int>(grid), s);
+    case 1: return x ? launch_small_rung<1, false, true>(a, static_cast<int>(grid), s)
+                     : (res ? launch_small_rung<1, true, false>(a, static_cast<int>(grid), s)
+                            : launch_small_rung<1, false, false>(a, static_cast<int>(grid), s));
+    case 2: return x ? launch_small_rung<2, false, true>(a, static_cast<int>(grid), s)
+                     : (res ? launch_small_rung<2, true, false>(a, static_cast<int>(grid), s)
+                            : launch_small_rung<2, false, false>(a, static_cast<int>(grid), s));
+    default: return x ? launch_small_rung<4, false, true>(a, static_cast<int>(grid), s)
+                      : (res ? launch_small_rung<4, true, false>(a, static_cast<int>(grid), s)
+                             : launch_small_rung<4, false, false>(a, static_cast<int>(grid), s));
   }
 }
 

@@ -154,6 +154,58 @@ __device__ __forceinline__ float packed_dot(const Packed& P, const uint32_t* rec
   return s * P.dw;
 }
 
+// Quantise 32 fp32 activations (16-byte aligned, global) to one Q8_1 chunk
+// and write it as chunk j of a record, with the same operations and rounding
+// as q8_1_quantize_acts (d = amax / 127 with IEEE division, q =
+// round-half-away(x / d) clamped to +-127, stored scale fp16(d)), so the
+// record equals the one built from the quantised block.  Two lanes per chunk
+// (lane pair 2p, 2p+1 of the warp; every lane of the warp calls this, `live`
+// false for pairs without a chunk): lane half h takes values 16h .. 16h+15.
+__device__ __forceinline__ void quantize_precord_half(const float* xs, uint32_t* rec, int j, int h, bool live) {
+  float v[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 f = live ? __ldg(reinterpret_cast<const float4*>(xs + 16 * h) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[4 * q] = f.x;
+    v[4 * q + 1] = f.y;
+    v[4 * q + 2] = f.z;
+    v[4 * q + 3] = f.w;
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  const float d = __fdiv_rn(m, 127.0f);
+  int sum = 0;
+  uint32_t words[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      int q = 0;
+      if (d != 0.0f) {
+        float r = roundf(__fdiv_rn(v[4 * w + i], d));
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        q = static_cast<int>(r);
+      }
+      sum += q;
+      word |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * i);
+    }
+    words[w] = word;
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  if (!live) return;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) rec[8 * (4 * h + w) + j] = words[w];
+  if (h == 0) {
+    const int slot = j & 3;
+    const float dh = __half2float(__float2half_rn(d));
+    rec[64 + j] = __float_as_uint(dh * __int_as_float((127 - 2 * slot) << 23));  // d / 4^slot, exact
+    rec[72 + j] = static_cast<uint32_t>(-(sum << (2 * slot)));
+  }
+}
+
 // Build one chunk (j) of one column's record from its Q8_1 block (global).
 __device__ __forceinline__ void fill_precord_chunk(const uint8_t* blk, uint32_t* rec, int j) {
   const uint32_t* s = reinterpret_cast<const uint32_t*>(blk);

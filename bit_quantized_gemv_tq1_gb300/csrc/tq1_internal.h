@@ -32,8 +32,10 @@ int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int
 
 // Decode-path kernel for 1 <= t <= 4 columns.  Returns TQ1_ERR_UNSUPPORTED
 // without launching when the shape does not fit its staging.
+// With `x` (fp32 activations [t][k]) the kernel quantises them to Q8_1 in its
+// prologue and `q8` is unused.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status, const float* res = nullptr);
+                     unsigned* status, const float* res = nullptr, const float* x = nullptr);
 
 // Expert-routed mat-vec over a compacted routing table in `ws` (general
 // dp4a kernel).

@@ -115,6 +115,18 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
 int tq1_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream);
 
 /*
+ * Decode mat-vec straight from fp32 activations: the Q8_1 quantisation of x
+ * (the same operations and rounding as q8_1_quantize_acts) runs in the
+ * mat-vec kernel's prologue, so a decode step needs one launch per mat-vec
+ * instead of two.  y equals, bit for bit, q8_1_quantize_acts followed by
+ * tq1_mmv.  x: fp32 [t][k], device, 16-byte aligned.  1 <= t <= 4 (larger t:
+ * TQ1_ERR_UNSUPPORTED; quantise once and call tq1_mmv).  Errors as tq1_mmv.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Current behavior" (activations
+ * are quantised to Q8_1 before the MMVQ kernel: here inside it).
+ */
+int tq1_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t, void* stream);
+
+/*
  * Mat-vec with a residual added in the kernel's epilogue:
  *   y[c][r] = res[c][r] + sum_k w[r][k] * x[c][k]
  * (one fp32 add per output after the dot product; the same kernels, rungs and

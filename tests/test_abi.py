@@ -84,6 +84,14 @@ def test_other_host_checks(lib):
     assert lib.tq1_mmv_id(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 0, 2, FAKE, ws, None) == 0
 
 
+def test_mmv_f32_host_checks(lib):
+    assert lib.tq1_mmv_f32(FAKE, FAKE, FAKE, 10, 256, 5, None) == -4   # t > 4: not fused
+    assert lib.tq1_mmv_f32(FAKE, None, FAKE, 10, 256, 1, None) == -1
+    assert lib.tq1_mmv_f32(FAKE, FAKE + 4, FAKE, 10, 256, 1, None) == -3
+    assert lib.tq1_mmv_f32(FAKE, FAKE, FAKE, 10, 300, 1, None) == -2
+    assert lib.tq1_mmv_f32(None, None, None, 0, 256, 1, None) == 0
+
+
 def test_mmv_add_host_checks(lib):
     assert lib.tq1_mmv_add(FAKE, FAKE, None, FAKE, 10, 256, 1, None) == -1   # null residual
     assert lib.tq1_mmv_add(FAKE, FAKE, FAKE + 4, FAKE, 10, 256, 1, None) == -3

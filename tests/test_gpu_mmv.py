@@ -175,3 +175,24 @@ def test_mmv_add_residual(n, k, t):
     L.tq1_mmv_add(blocks, q8, r, r, n, k, t)  # in place
     np.testing.assert_array_equal(G.host(r), G.host(y))
     assert L.tq1_sync_status() == 0
+
+
+@pytest.mark.parametrize("n,k,t", [(5120, 6144, 1), (300, 2048, 2), (77, 1024, 3), (129, 4096, 4), (1, 256, 1)])
+def test_mmv_f32_fused_quantisation_matches_two_step(n, k, t):
+    # Quantisation inside the decode kernel gives the records, hence the
+    # outputs, of q8_1_quantize_acts followed by tq1_mmv, bit for bit; the
+    # activations include an all-zero chunk and ties.
+    p = synth.matvec(n, k, t, p_zero=0.4, seed=3 * n + t)
+    x = p.x.copy()
+    x[0, :32] = 0.0
+    x[-1, -32:] = np.arange(32, dtype=np.float32) - 15.5
+    blocks = G.quantize_rows(p.w)
+    L, torch = G.lib(), G.torch()
+    y1 = torch.full((t, n), float("nan"), dtype=torch.float32, device="cuda")
+    y2 = torch.full((t, n), float("nan"), dtype=torch.float32, device="cuda")
+    xd = G.dev(x)
+    L.tq1_mmv_f32(blocks, xd, y1, n, k, t)
+    L.tq1_mmv(blocks, G.quantize_acts(x), y2, n, k, t)
+    assert L.tq1_sync_status() == 0
+    np.testing.assert_array_equal(G.host(y1), G.host(y2))
+    G.assert_close(G.host(y1), orc.mmv_f64(orc.tq1_encode_rows(p.w), orc.q8_1_quantize(x), n, k, t))
