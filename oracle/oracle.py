@@ -25,6 +25,7 @@ _lib = None
 
 QK = 256
 BLOCK_BYTES = 54
+TQ2_BYTES = 66
 QK8 = 32
 Q8_BYTES = 36
 
@@ -68,6 +69,15 @@ def _load():
         lib.orc_mmv_f64_rows.argtypes = [P, P, P, I64, I64, I64, P, I64]
         lib.orc_mmv_id_f64.argtypes = [P, I64, P, P, P, I64, I64, I64, I64]
         lib.orc_mmv_id_f64_rows.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, I64]
+        lib.orc_tq2_elem_pos.restype = None
+        lib.orc_tq2_elem_pos.argtypes = [ctypes.c_int, P, P]
+        lib.orc_tq2_code.restype = ctypes.c_int
+        lib.orc_tq2_code.argtypes = [P, ctypes.c_int]
+        lib.orc_tq2_encode_rows.argtypes = [P, P, I64, I64]
+        lib.orc_tq2_decode_rows.argtypes = [P, P, P, I64, I64]
+        lib.orc_tq2_mmv_partials.argtypes = [P, P, P, I64, I64, I64]
+        lib.orc_tq2_mmv_f64.argtypes = [P, P, P, I64, I64, I64]
+        lib.orc_tq2_mmv_f64_rows.argtypes = [P, P, P, I64, I64, I64, P, I64]
         lib.orc_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -193,4 +203,59 @@ def mmv_id_f64_rows(expert_blocks: np.ndarray, n_experts: int, q8: np.ndarray, i
     _load().orc_mmv_id_f64_rows(_ptr(np.ascontiguousarray(expert_blocks)), n_experts,
                                 _ptr(np.ascontiguousarray(q8)), _ptr(ids), _ptr(out), n, k, t, top_k,
                                 _ptr(rows), rows.size)
+    return out
+
+
+# ------------------------------------------------------------------ TQ2_0 --
+# The 2-bit sibling format (reading R6 of tq1_oracle.c): qs[64] with four
+# 2-bit codes per byte, fp16 d at byte 64, 66 bytes per 256-block.
+def tq2_elem_pos(e: int) -> tuple[int, int]:
+    bi, f = ctypes.c_int(), ctypes.c_int()
+    _load().orc_tq2_elem_pos(e, ctypes.byref(bi), ctypes.byref(f))
+    return bi.value, f.value
+
+
+def tq2_code(block: np.ndarray, e: int) -> int:
+    block = np.ascontiguousarray(block, dtype=np.uint8)
+    assert block.size == TQ2_BYTES
+    return int(_load().orc_tq2_code(_ptr(block), e))
+
+
+def tq2_encode_rows(w: np.ndarray) -> np.ndarray:
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    assert k % QK == 0
+    out = np.zeros((n, k // QK, TQ2_BYTES), dtype=np.uint8)
+    _load().orc_tq2_encode_rows(_ptr(w), _ptr(out), n, k)
+    return out
+
+
+def tq2_decode_rows(blocks: np.ndarray, n: int, k: int) -> tuple[np.ndarray, np.ndarray]:
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    assert blocks.size == n * (k // QK) * TQ2_BYTES
+    trits = np.zeros((n, k), dtype=np.int8)
+    scales = np.zeros((n, k // QK), dtype=np.float32)
+    _load().orc_tq2_decode_rows(_ptr(blocks), _ptr(trits), _ptr(scales), n, k)
+    return trits, scales
+
+
+def tq2_mmv_partials(blocks: np.ndarray, q8: np.ndarray, n: int, k: int, t: int) -> np.ndarray:
+    out = np.zeros((t, n, k // QK8), dtype=np.int32)
+    _load().orc_tq2_mmv_partials(_ptr(np.ascontiguousarray(blocks)), _ptr(np.ascontiguousarray(q8)),
+                                 _ptr(out), n, k, t)
+    return out
+
+
+def tq2_mmv_f64(blocks: np.ndarray, q8: np.ndarray, n: int, k: int, t: int) -> np.ndarray:
+    out = np.zeros((t, n), dtype=np.float64)
+    _load().orc_tq2_mmv_f64(_ptr(np.ascontiguousarray(blocks)), _ptr(np.ascontiguousarray(q8)), _ptr(out), n, k, t)
+    return out
+
+
+def tq2_mmv_f64_rows(blocks: np.ndarray, q8: np.ndarray, n: int, k: int, t: int, rows) -> np.ndarray:
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    assert rows.size == 0 or (rows.min() >= 0 and rows.max() < n)
+    out = np.zeros((t, rows.size), dtype=np.float64)
+    _load().orc_tq2_mmv_f64_rows(_ptr(np.ascontiguousarray(blocks)), _ptr(np.ascontiguousarray(q8)), _ptr(out),
+                                 n, k, t, _ptr(rows), rows.size)
     return out

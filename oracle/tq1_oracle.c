@@ -1,5 +1,6 @@
 /*
- * tq1_oracle.c -- plain, slow, CPU oracle for the TQ1_0 ternary mat-vec.
+ * tq1_oracle.c -- plain, slow, CPU oracle for the TQ1_0 ternary mat-vec (and
+ * its 2-bit sibling TQ2_0).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
  * load this file; only the tests, the smoke check and the benchmark's CPU
@@ -31,6 +32,15 @@
  *      never used by the dot product below.
  *   R5 mat-vec-id: token t's activations are used for every one of its
  *      top_k slots; ids outside [0, n_experts) leave their output untouched.
+ *   R6 TQ2_0, the 2-bit sibling format P1 "Upstream state" names without a
+ *      layout: qs[64] holding four 2-bit codes per byte, then the fp16 d at
+ *      byte 64; 66 bytes per 256-element block.  Code = trit + 1 (0/1/2 means
+ *      -1/0/+1; the unused code 3 decodes to +2).  Element order continues
+ *      P1's chunk pattern with four codes per byte: chunk c (elements 32c ..
+ *      32c+31) reads code c % 4 (bits 2(c%4)..2(c%4)+1) of bytes qs[32(c/4)
+ *      .. 32(c/4)+31].  Quantisation from fp32 as R3.  Parity of this layout
+ *      is unpinned by the pages; the tests pin the arithmetic on it against
+ *      the TQ1_0 oracle (same trits, same outputs).
  *
  * Every floating-point result of the dot product is computed in fp64: each
  * product d_w*d_a*I is exact in fp64 (11+11+13 significant bits), so the
@@ -46,6 +56,7 @@
 
 #define ORC_QK 256            /* weights per TQ1_0 block          */
 #define ORC_BLOCK_BYTES 54    /* qs[48] + qh[4] + fp16 d          */
+#define ORC_TQ2_BYTES 66      /* R6: qs[64] + fp16 d              */
 #define ORC_QK8 32            /* activations per Q8_1 block       */
 #define ORC_Q8_BYTES 36       /* fp16 d + fp16 s + int8 q[32]     */
 
@@ -181,6 +192,66 @@ void orc_tq1_decode_rows(const uint8_t* blocks, int8_t* trits, float* scales, in
 }
 
 /* ------------------------------------------------------------------ */
+/* TQ2_0 (R6).                                                         */
+/* ------------------------------------------------------------------ */
+
+/* Element e (0..255) of a TQ2_0 block lives in byte *byte_idx, 2-bit field
+ * *field (bits 2*field .. 2*field+1). */
+void orc_tq2_elem_pos(int e, int* byte_idx, int* field) {
+  const int chunk = e / 32;
+  *byte_idx = 32 * (chunk / 4) + e % 32;
+  *field = chunk % 4;
+}
+
+/* Code (0..3) of element e; its value is code - 1. */
+int orc_tq2_code(const uint8_t* blk, int e) {
+  int bi, f;
+  orc_tq2_elem_pos(e, &bi, &f);
+  return (blk[bi] >> (2 * f)) & 3;
+}
+
+/* R6 + R3: quantise one 256-weight block to TQ2_0. */
+static void orc_tq2_encode_block(const float* x, uint8_t* blk) {
+  float amax = 0.0f;
+  for (int i = 0; i < ORC_QK; ++i) {
+    const float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  const uint16_t d16 = orc_f16_from_f32(amax);
+  memset(blk, 0, ORC_TQ2_BYTES);
+  for (int e = 0; e < ORC_QK; ++e) {
+    float r = amax != 0.0f ? roundf(x[e] / amax) : 0.0f; /* roundf: halves away from zero */
+    if (r > 1.0f) r = 1.0f;
+    if (r < -1.0f) r = -1.0f;
+    int bi, f;
+    orc_tq2_elem_pos(e, &bi, &f);
+    blk[bi] = (uint8_t)(blk[bi] | (((int)r + 1) << (2 * f)));
+  }
+  blk[64] = (uint8_t)(d16 & 0xFF);
+  blk[65] = (uint8_t)(d16 >> 8);
+}
+
+/* w: fp32 [n][k], k % 256 == 0.  blocks: [n][k/256] x 66 bytes. */
+void orc_tq2_encode_rows(const float* w, uint8_t* blocks, int64_t n, int64_t k) {
+  const int64_t nb = k / ORC_QK;
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t b = 0; b < nb; ++b)
+      orc_tq2_encode_block(w + r * k + b * ORC_QK, blocks + (r * nb + b) * ORC_TQ2_BYTES);
+}
+
+/* Decode to values (code - 1) [n][k] and scales d [n][k/256]. */
+void orc_tq2_decode_rows(const uint8_t* blocks, int8_t* trits, float* scales, int64_t n, int64_t k) {
+  const int64_t nb = k / ORC_QK;
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* blk = blocks + (r * nb + b) * ORC_TQ2_BYTES;
+      for (int e = 0; e < ORC_QK; ++e) trits[r * k + b * ORC_QK + e] = (int8_t)(orc_tq2_code(blk, e) - 1);
+      scales[r * nb + b] = orc_f32_from_f16((uint16_t)(blk[64] | (blk[65] << 8)));
+    }
+  }
+}
+
+/* ------------------------------------------------------------------ */
 /* Q8_1 activations (R4).                                              */
 /* ------------------------------------------------------------------ */
 
@@ -223,43 +294,56 @@ static float orc_q8_scale(const uint8_t* blk) { return orc_f32_from_f16((uint16_
 /* Dot products.                                                       */
 /* ------------------------------------------------------------------ */
 
+/* Weight formats of the dot products below: 1 = TQ1_0, 2 = TQ2_0 (R6). */
+static int64_t orc_fmt_bytes(int fmt) { return fmt == 2 ? ORC_TQ2_BYTES : ORC_BLOCK_BYTES; }
+
+/* Value (-1, 0, +1; +2 for TQ2_0's unused code) of element e of a block. */
+static int orc_elem_value(int fmt, const uint8_t* wblk, int e) {
+  if (fmt == 2) return orc_tq2_code(wblk, e) - 1;
+  int bi, dg;
+  orc_tq1_elem_pos(e, &bi, &dg);
+  return orc_tq1_digit(wblk[bi], dg) - 1;
+}
+
+static double orc_block_scale(int fmt, const uint8_t* wblk) {
+  const int at = fmt == 2 ? 64 : 52;
+  return (double)orc_f32_from_f16((uint16_t)(wblk[at] | (wblk[at + 1] << 8)));
+}
+
 /* Integer partial of one row against one column over one 32-element chunk:
  * I = sum over the chunk of (digit - 1) * q.  Elements are visited in
  * natural order and each one's byte/digit is looked up (P1: the CPU walk). */
-static int32_t orc_chunk_partial(const uint8_t* wblk, const uint8_t* qblk, int chunk) {
+static int32_t orc_chunk_partial(int fmt, const uint8_t* wblk, const uint8_t* qblk, int chunk) {
   int32_t acc = 0;
-  for (int i = 0; i < ORC_QK8; ++i) {
-    const int e = chunk * ORC_QK8 + i;
-    int bi, dg;
-    orc_tq1_elem_pos(e, &bi, &dg);
-    const int trit = orc_tq1_digit(wblk[bi], dg) - 1;
-    acc += trit * (int)(int8_t)qblk[4 + i];
-  }
+  for (int i = 0; i < ORC_QK8; ++i)
+    acc += orc_elem_value(fmt, wblk, chunk * ORC_QK8 + i) * (int)(int8_t)qblk[4 + i];
   return acc;
 }
 
 /* part[c][r][k/32] = integer per-32 partials (exact). */
-void orc_mmv_partials(const uint8_t* blocks, const uint8_t* q8, int32_t* part, int64_t n, int64_t k, int64_t t) {
-  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8;
+static void orc_partials_fmt(int fmt, const uint8_t* blocks, const uint8_t* q8, int32_t* part, int64_t n, int64_t k,
+                             int64_t t) {
+  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8, bb = orc_fmt_bytes(fmt);
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < n; ++r)
     for (int64_t c = 0; c < t; ++c)
       for (int64_t b = 0; b < nb; ++b)
         for (int j = 0; j < 8; ++j)
-          part[(c * n + r) * nq + b * 8 + j] = orc_chunk_partial(
-              blocks + (r * nb + b) * ORC_BLOCK_BYTES, q8 + (c * nq + b * 8 + j) * ORC_Q8_BYTES, j);
+          part[(c * n + r) * nq + b * 8 + j] =
+              orc_chunk_partial(fmt, blocks + (r * nb + b) * bb, q8 + (c * nq + b * 8 + j) * ORC_Q8_BYTES, j);
 }
 
 /* y = sum_b d_w[b] * sum_j d_a[8b+j] * I_j   (fp64; natural order). */
-static double orc_row_dot(const uint8_t* wrow, const uint8_t* qcol, int64_t nb) {
+static double orc_row_dot(int fmt, const uint8_t* wrow, const uint8_t* qcol, int64_t nb) {
+  const int64_t bb = orc_fmt_bytes(fmt);
   double y = 0.0;
   for (int64_t b = 0; b < nb; ++b) {
-    const uint8_t* wblk = wrow + b * ORC_BLOCK_BYTES;
-    const double dw = (double)orc_f32_from_f16((uint16_t)(wblk[52] | (wblk[53] << 8)));
+    const uint8_t* wblk = wrow + b * bb;
+    const double dw = orc_block_scale(fmt, wblk);
     double acc = 0.0;
     for (int j = 0; j < 8; ++j) {
       const uint8_t* qblk = qcol + (b * 8 + j) * ORC_Q8_BYTES;
-      acc += (double)orc_q8_scale(qblk) * (double)orc_chunk_partial(wblk, qblk, j);
+      acc += (double)orc_q8_scale(qblk) * (double)orc_chunk_partial(fmt, wblk, qblk, j);
     }
     y += dw * acc;
   }
@@ -267,23 +351,51 @@ static double orc_row_dot(const uint8_t* wrow, const uint8_t* qcol, int64_t nb) 
 }
 
 /* y[c][r] for all rows r < n and columns c < t. */
-void orc_mmv_f64(const uint8_t* blocks, const uint8_t* q8, double* y, int64_t n, int64_t k, int64_t t) {
-  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8;
+static void orc_f64_fmt(int fmt, const uint8_t* blocks, const uint8_t* q8, double* y, int64_t n, int64_t k,
+                        int64_t t) {
+  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8, bb = orc_fmt_bytes(fmt);
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < n; ++r)
     for (int64_t c = 0; c < t; ++c)
-      y[c * n + r] = orc_row_dot(blocks + r * nb * ORC_BLOCK_BYTES, q8 + c * nq * ORC_Q8_BYTES, nb);
+      y[c * n + r] = orc_row_dot(fmt, blocks + r * nb * bb, q8 + c * nq * ORC_Q8_BYTES, nb);
 }
 
 /* Sampled rows: y[c][i] = row rows[i] against column c. */
-void orc_mmv_f64_rows(const uint8_t* blocks, const uint8_t* q8, double* y, int64_t n, int64_t k, int64_t t,
-                      const int64_t* rows, int64_t nrows) {
-  (void)n;
-  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8;
+static void orc_f64_rows_fmt(int fmt, const uint8_t* blocks, const uint8_t* q8, double* y, int64_t k, int64_t t,
+                             const int64_t* rows, int64_t nrows) {
+  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8, bb = orc_fmt_bytes(fmt);
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < nrows; ++i)
     for (int64_t c = 0; c < t; ++c)
-      y[c * nrows + i] = orc_row_dot(blocks + rows[i] * nb * ORC_BLOCK_BYTES, q8 + c * nq * ORC_Q8_BYTES, nb);
+      y[c * nrows + i] = orc_row_dot(fmt, blocks + rows[i] * nb * bb, q8 + c * nq * ORC_Q8_BYTES, nb);
+}
+
+void orc_mmv_partials(const uint8_t* blocks, const uint8_t* q8, int32_t* part, int64_t n, int64_t k, int64_t t) {
+  orc_partials_fmt(1, blocks, q8, part, n, k, t);
+}
+
+void orc_mmv_f64(const uint8_t* blocks, const uint8_t* q8, double* y, int64_t n, int64_t k, int64_t t) {
+  orc_f64_fmt(1, blocks, q8, y, n, k, t);
+}
+
+void orc_mmv_f64_rows(const uint8_t* blocks, const uint8_t* q8, double* y, int64_t n, int64_t k, int64_t t,
+                      const int64_t* rows, int64_t nrows) {
+  (void)n;
+  orc_f64_rows_fmt(1, blocks, q8, y, k, t, rows, nrows);
+}
+
+void orc_tq2_mmv_partials(const uint8_t* blocks, const uint8_t* q8, int32_t* part, int64_t n, int64_t k, int64_t t) {
+  orc_partials_fmt(2, blocks, q8, part, n, k, t);
+}
+
+void orc_tq2_mmv_f64(const uint8_t* blocks, const uint8_t* q8, double* y, int64_t n, int64_t k, int64_t t) {
+  orc_f64_fmt(2, blocks, q8, y, n, k, t);
+}
+
+void orc_tq2_mmv_f64_rows(const uint8_t* blocks, const uint8_t* q8, double* y, int64_t n, int64_t k, int64_t t,
+                          const int64_t* rows, int64_t nrows) {
+  (void)n;
+  orc_f64_rows_fmt(2, blocks, q8, y, k, t, rows, nrows);
 }
 
 /* R5: y[c][s][r] = expert ids[c][s] (matrix at expert_blocks + e*n*nb*54)
@@ -299,7 +411,7 @@ void orc_mmv_id_f64(const uint8_t* expert_blocks, int64_t n_experts, const uint8
       if (e < 0 || e >= n_experts) continue;
       for (int64_t r = 0; r < n; ++r)
         y[(c * top_k + s) * n + r] =
-            orc_row_dot(expert_blocks + e * ebytes + r * nb * ORC_BLOCK_BYTES, q8 + c * nq * ORC_Q8_BYTES, nb);
+            orc_row_dot(1, expert_blocks + e * ebytes + r * nb * ORC_BLOCK_BYTES, q8 + c * nq * ORC_Q8_BYTES, nb);
     }
   }
 }
@@ -317,7 +429,8 @@ void orc_mmv_id_f64_rows(const uint8_t* expert_blocks, int64_t n_experts, const 
       if (e < 0 || e >= n_experts) continue;
       for (int64_t i = 0; i < nrows; ++i)
         y[(c * top_k + s) * nrows + i] =
-            orc_row_dot(expert_blocks + e * ebytes + rows[i] * nb * ORC_BLOCK_BYTES, q8 + c * nq * ORC_Q8_BYTES, nb);
+            orc_row_dot(1, expert_blocks + e * ebytes + rows[i] * nb * ORC_BLOCK_BYTES, q8 + c * nq * ORC_Q8_BYTES,
+                        nb);
     }
   }
 }
