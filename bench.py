@@ -42,6 +42,7 @@ if ROOT not in sys.path:
 
 METRIC = "TQ1_0 mat-vec effective HBM GB/s (% of GB300 peak) at T=1; µs/call vs T=1..32"
 QK, BLOCK_BYTES, QK8, Q8_BYTES = 256, 54, 32, 36
+TQ2_BYTES = 66
 N2, K2 = 5120, 6144
 
 
@@ -353,6 +354,7 @@ def run_ours(args, ws, rank, local):
         extra["moe_c4"] = moe_bench(lib, L, synth, dev, stream, capture, args)
         extra["dequant_c2"] = dequant_bench(lib, L, synth, dev, stream, capture, args)
         extra["decode_chain_c2"] = fused_chain_bench(lib, L, synth, dev, stream, capture, args)
+        extra["tq2_c2"] = tq2_bench(lib, L, synth, dev, stream, capture, args)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -525,6 +527,50 @@ def dequant_bench(lib, L, synth, dev, stream, capture, args) -> dict:
     return out
 
 
+def tq2_bench(lib, L, synth, dev, stream, capture, args) -> dict:
+    """TQ2_0 (2-bit codes, 66-byte blocks) mat-vec on config 2's shape
+    (N=5120, K=6144) and distribution at T = 1, 2, 4, 8, 16, 32, cycling
+    weight copies whose total exceeds 4x L2.  Algorithmic bytes: packed
+    weights + Q8_1 activations + fp32 outputs."""
+    import torch
+
+    c2 = synth.CONFIGS["c2"]
+    n, k = c2["n"], c2["k"]
+    wbytes = n * (k // QK) * TQ2_BYTES
+    copies = max(8, int(math.ceil(4 * 129 * 2 ** 20 / wbytes)))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2200)
+    blocks = torch.empty(copies * wbytes, dtype=torch.uint8, device=dev)
+    for l in range(copies):
+        w = synth.device_weights(n, k, c2["p_zero"], c2["d_lo"], c2["d_hi"], gen, dev)
+        L.tq2_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+        del w
+    tmax = 32
+    x = synth.device_activations((copies * tmax, k), gen, dev)
+    qbytes = (k // QK8) * Q8_BYTES
+    q8 = torch.empty(copies * tmax * qbytes, dtype=torch.uint8, device=dev)
+    L.q8_1_quantize_acts(x, q8, copies * tmax, k)
+    y = torch.empty((copies * tmax, n), dtype=torch.float32, device=dev)
+    peak = float(measured_peaks()["hbm_gbs"])
+    out = {"workload": f"TQ2_0 N=5120 K=6144, c2 distribution, {copies} weight copies", "copies": copies}
+    for t in (1, 2, 4, 8, 16, 32):
+        def calls(s, t=t):
+            for l in range(copies):
+                assert lib.tq2_mmv(blocks.data_ptr() + l * wbytes, q8.data_ptr() + l * tmax * qbytes,
+                                   y.data_ptr() + l * tmax * n * 4, n, k, t, s) == 0
+
+        g = capture(calls)
+        ms = _time_graph(g, stream, 10) / copies
+        assert lib.tq1_sync_status(stream.cuda_stream) == 0
+        byts = wbytes + t * qbytes + 4 * t * n
+        gbs = byts / (ms * 1e-3) / 1e9
+        out[f"t{t}"] = {"us_per_call": round(ms * 1e3, 3), "gbs": round(gbs, 1),
+                        "frac_of_measured_hbm": round(gbs / peak, 4)}
+        del g
+    del blocks
+    return out
+
+
 def moe_bench(lib, L, synth, dev, stream, capture, args) -> dict:
     """Config 4: 128 experts of N=768, K=2048, Zipf top-8 routing, T=1 and 32.
     Effective bytes count the packed weights of the experts actually routed
@@ -641,6 +687,25 @@ def run_profile_case(args, local):
         for i in range(args.profile_calls):
             l = i % copies
             assert lib.tq1_mmv(blocks.data_ptr() + l * wbytes, q8.data_ptr(), y.data_ptr(), n, k, t, s) == 0
+    elif case.startswith("tq2c2"):
+        # TQ2_0 on config 2's shape: tq2c2 (T=1) or tq2c2t<T>.
+        c = synth.CONFIGS["c2"]
+        n, k = c["n"], c["k"]
+        t = int(case[6:]) if len(case) > 6 else 1
+        wbytes = n * (k // QK) * TQ2_BYTES
+        copies = max(1, min(args.layers or 40, (2 * 2 ** 30) // wbytes))
+        blocks = torch.empty(copies * wbytes, dtype=torch.uint8, device=dev)
+        for l in range(copies):
+            w = synth.device_weights(n, k, c["p_zero"], c["d_lo"], c["d_hi"], gen, dev)
+            L.tq2_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+            del w
+        x = synth.device_activations((t, k), gen, dev)
+        q8 = torch.empty(t * (k // QK8) * Q8_BYTES, dtype=torch.uint8, device=dev)
+        y = torch.empty((t, n), dtype=torch.float32, device=dev)
+        L.q8_1_quantize_acts(x, q8, t, k)
+        for i in range(args.profile_calls):
+            l = i % copies
+            assert lib.tq2_mmv(blocks.data_ptr() + l * wbytes, q8.data_ptr(), y.data_ptr(), n, k, t, s) == 0
     elif case.startswith("c4"):
         t = int(case[3:]) if len(case) > 3 else 1
         m = synth.config_moe(t)
@@ -681,7 +746,8 @@ def main(argv=None):
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per mat-vec launch from an ncu capture of the current kernel")
     ap.add_argument("--profile", default=None,
-                    help="run a fixed eager workload for ncu instead of timing (c2, c3t<T>, c4t<T>, c5)")
+                    help="run a fixed eager workload for ncu instead of timing "
+                         "(c2, c3t<T>, c4t<T>, c5, tq2c2, tq2c2t<T>)")
     ap.add_argument("--profile-calls", type=int, default=12)
     args = ap.parse_args(argv)
     if args.profile:

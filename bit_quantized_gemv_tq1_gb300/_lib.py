@@ -57,6 +57,11 @@ def library() -> ctypes.CDLL:
         lib.tq1_last_cuda_error.argtypes = []
         lib.tq1_blocks_bytes.restype = SZ
         lib.tq1_blocks_bytes.argtypes = [I64, I64]
+        lib.tq2_blocks_bytes.restype = SZ
+        lib.tq2_blocks_bytes.argtypes = [I64, I64]
+        lib.tq2_quantize_rows.argtypes = [P, P, I64, I64, P]
+        lib.tq2_mmv.argtypes = [P, P, P, I64, I64, I64, P]
+        lib.tq2_mmv_partials.argtypes = [P, P, P, I64, I64, I64, P]
         lib.tq1_q8_1_bytes.restype = SZ
         lib.tq1_q8_1_bytes.argtypes = [I64, I64]
         lib.tq1_quantize_rows.argtypes = [P, P, I64, I64, P]
@@ -75,7 +80,8 @@ def library() -> ctypes.CDLL:
         lib.tq1_sync_status.argtypes = [P]
         for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_add", "tq1_mmv_f32",
                      "tq1_mmv_partials", "tq1_mmv_id", "tq1_mmv_id_slots", "tq1_mmv_id_noalloc",
-                     "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status"):
+                     "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status", "tq2_quantize_rows",
+                     "tq2_mmv", "tq2_mmv_partials"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -185,6 +191,23 @@ def tq1_get_rows(blocks, row_ids, n_ids: int, out, n: int, k: int, out_f16: bool
     """out[i] = dequantised row row_ids[i] of the n x k TQ1_0 matrix."""
     _check(library().tq1_get_rows(_addr(blocks), _addr(row_ids), n_ids, _addr(out), n, k, int(bool(out_f16)),
                                   _stream(stream)), "tq1_get_rows")
+
+
+def tq2_blocks_bytes(n: int, k: int) -> int:
+    return int(library().tq2_blocks_bytes(n, k))
+
+
+def tq2_quantize_rows(w, blocks, n: int, k: int, stream=None) -> None:
+    _check(library().tq2_quantize_rows(_addr(w), _addr(blocks), n, k, _stream(stream)), "tq2_quantize_rows")
+
+
+def tq2_mmv(blocks, q8, y, n: int, k: int, t: int, stream=None) -> None:
+    _check(library().tq2_mmv(_addr(blocks), _addr(q8), _addr(y), n, k, t, _stream(stream)), "tq2_mmv")
+
+
+def tq2_mmv_partials(blocks, q8, part, n: int, k: int, t: int, stream=None) -> None:
+    _check(library().tq2_mmv_partials(_addr(blocks), _addr(q8), _addr(part), n, k, t, _stream(stream)),
+           "tq2_mmv_partials")
 
 
 def tq1_sync_status(stream=None) -> int:

@@ -115,18 +115,33 @@ size_t tq1_blocks_bytes(int64_t n, int64_t k) {
   return static_cast<size_t>(n) * static_cast<size_t>(k / kQK) * kBlockBytes;
 }
 
+size_t tq2_blocks_bytes(int64_t n, int64_t k) {
+  if (n < 0 || k < 0) return 0;
+  return static_cast<size_t>(n) * static_cast<size_t>(k / kQK) * kTq2BlockBytes;
+}
+
 size_t tq1_q8_1_bytes(int64_t t, int64_t k) {
   if (t < 0 || k < 0) return 0;
   return static_cast<size_t>(t) * static_cast<size_t>(k / kQK8) * kQ8Bytes;
 }
 
-int tq1_quantize_rows(const float* w, void* blocks, int64_t n, int64_t k, void* stream) {
+static int quantize_rows_common(const float* w, void* blocks, int64_t n, int64_t k, void* stream, int fmt) {
   if (n < 0 || k <= 0 || (k % kQK) != 0) return TQ1_ERR_SHAPE;
   if (n == 0) return TQ1_OK;
   if (!w || !blocks) return TQ1_ERR_NULL;
   if (misaligned(w) || misaligned(blocks)) return TQ1_ERR_ALIGN;
   if (!status_ptr()) return TQ1_ERR_CUDA;
-  return launch_quantize_rows(w, static_cast<uint8_t*>(blocks), n, k, static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return fmt == kFmtTq2 ? launch_quantize_rows_tq2(w, static_cast<uint8_t*>(blocks), n, k, s)
+                        : launch_quantize_rows(w, static_cast<uint8_t*>(blocks), n, k, s);
+}
+
+int tq1_quantize_rows(const float* w, void* blocks, int64_t n, int64_t k, void* stream) {
+  return quantize_rows_common(w, blocks, n, k, stream, kFmtTq1);
+}
+
+int tq2_quantize_rows(const float* w, void* blocks, int64_t n, int64_t k, void* stream) {
+  return quantize_rows_common(w, blocks, n, k, stream, kFmtTq2);
 }
 
 int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* stream) {
@@ -139,7 +154,7 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
 }
 
 static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* part, int64_t n, int64_t k,
-                      int64_t t, void* stream, const float* res = nullptr) {
+                      int64_t t, void* stream, const float* res = nullptr, int fmt = kFmtTq1) {
   int rc = check_mmv_shape(n, k, t);
   if (rc != TQ1_OK) return rc;
   if (n == 0 || t == 0) return TQ1_OK;
@@ -154,18 +169,18 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
   const uint8_t* w = static_cast<const uint8_t*>(blocks);
   const uint8_t* a = static_cast<const uint8_t*>(q8);
   const int64_t q8_row = (k / kQK8) * kQ8Bytes;
-  if (y && t >= kTileMinT) {
+  if (y && t >= kTileMinT && fmt == kFmtTq1) {
     rc = launch_tile(w, a, y, n, k, t, s, st, res);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the dp4a kernels below
   }
   if (y && t <= 4) {
-    rc = launch_mmv_small(w, a, y, n, k, t, s, st, res);
+    rc = launch_mmv_small(w, a, y, n, k, t, s, st, res, nullptr, fmt);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
   }
   for (int64_t c0 = 0; c0 < t; c0 += 32) {
     const int64_t tc = t - c0 < 32 ? t - c0 : 32;
     rc = launch_mmv(w, a + c0 * q8_row, y ? y + c0 * n : nullptr, part ? part + c0 * n * (k / kQK8) : nullptr, n,
-                    k, tc, s, st, res ? res + c0 * n : nullptr);
+                    k, tc, s, st, res ? res + c0 * n : nullptr, fmt);
     if (rc != TQ1_OK) return rc;
   }
   return TQ1_OK;
@@ -173,6 +188,16 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
 
 int tq1_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream) {
   return mmv_common(blocks, q8, y, nullptr, n, k, t, stream);
+}
+
+int tq2_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream) {
+  return mmv_common(blocks, q8, y, nullptr, n, k, t, stream, nullptr, kFmtTq2);
+}
+
+int tq2_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,
+                     void* stream) {
+  if (!part && n > 0 && t > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;
+  return mmv_common(blocks, q8, nullptr, part, n, k, t, stream, nullptr, kFmtTq2);
 }
 
 int tq1_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t, void* stream) {

@@ -1,5 +1,7 @@
 // mmv.cu -- TQ1_0 x Q8_1 mat-vec for T <= 32 columns, its debug variant that
-// exports the exact per-32 integer partials, and the expert-routed variant.
+// exports the exact per-32 integer partials, and the expert-routed variant;
+// the same kernel serves TQ2_0 weights (2-bit codes: the unit's digit words
+// are its 16 qs words shifted and masked).
 //
 // Structure (PrismML-Eng/llama.cpp issue #139, "Proposed approach" option 1:
 // a dedicated kernel that consumes whole 256-element blocks and iterates over
@@ -32,8 +34,10 @@ namespace tq1 {
 
 constexpr int kThreads = 256;
 constexpr int kPassUnits = kThreads;
-constexpr uint32_t kPassBytes = kPassUnits * kBlockBytes;  // 13824, a multiple of 16
-constexpr uint32_t kStageBytes = kPassBytes + 32;          // + 16 alignment slack + 4 over-read
+// Pass bytes (units x block bytes: 13824 for TQ1_0, 16896 for TQ2_0, both
+// multiples of 16) and ring stage bytes (+ 16 alignment slack + over-read).
+__host__ __device__ constexpr uint32_t pass_bytes(int bb) { return kPassUnits * static_cast<uint32_t>(bb); }
+__host__ __device__ constexpr uint32_t stage_bytes(int bb) { return pass_bytes(bb) + 32; }
 constexpr int kStages = 3;
 constexpr size_t kActBudget = 96 * 1024;   // activation records per CTA
 constexpr size_t kAccBudget = 16 * 1024;   // per-tile row accumulators
@@ -49,6 +53,7 @@ struct MmvArgs {
   unsigned* status;
   int64_t n, k, t;
   int nb;             // k / 256
+  int bb;             // bytes per weight block (format)
   int cc;             // columns per activation staging chunk
   int rt;             // rows per tile
   int top_k;
@@ -81,7 +86,7 @@ __device__ __forceinline__ int64_t split_point(int64_t total, int64_t parts, int
 template <int CMAX, int MODE>
 __device__ Tile get_tile(const MmvArgs& a, const Plan& P, int idx) {
   Tile T;
-  const int64_t rowbytes = static_cast<int64_t>(a.nb) * kBlockBytes;
+  const int64_t rowbytes = static_cast<int64_t>(a.nb) * a.bb;
   if (MODE != kModeMoe) {
     const int64_t r = P.v0 + static_cast<int64_t>(idx) * a.rt;
     T.row0 = r;
@@ -169,18 +174,20 @@ __device__ __forceinline__ void cursor_next(const MmvArgs& a, const Plan& P, Cur
 __device__ __forceinline__ void issue_pass(const MmvArgs& a, const Tile& T, int p, uint8_t* stage, uint64_t* bar,
                                            uint64_t policy) {
   const int units = min(kPassUnits, T.rows * a.nb - p * kPassUnits);
-  const uint8_t* src = T.src + static_cast<int64_t>(p) * kPassBytes;
+  const uint8_t* src = T.src + static_cast<int64_t>(p) * pass_bytes(a.bb);
   const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
   const uint8_t* a0 = src - delta;
-  const uint32_t total = delta + static_cast<uint32_t>(units) * kBlockBytes;
+  const uint32_t total = delta + static_cast<uint32_t>(units) * static_cast<uint32_t>(a.bb);
   const uint32_t main = total & ~15u;
   for (uint32_t i = main; i < total; ++i) stage[i] = __ldg(a0 + i);
   mbar_arrive_expect_tx(bar, main);
   if (main) bulk_g2s(stage, a0, main, bar, policy);
 }
 
-template <int CMAX, int MODE>
+template <int CMAX, int MODE, int FMT>
 __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const MmvArgs a) {
+  constexpr int kBB = fmt_block_bytes<FMT>();
+  constexpr uint32_t kStageBytes = stage_bytes(kBB);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   uint32_t* act = reinterpret_cast<uint32_t*>(ring + kStages * kStageBytes);
@@ -294,11 +301,12 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const MmvArgs a) {
     const int units = T.rows * nb;
     const int u = ubase + tid;
     const bool valid = u < units;
-    const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(T.src + static_cast<int64_t>(p) * kPassBytes) & 15u);
-    BlockDigits D;
+    const uint32_t delta =
+        static_cast<uint32_t>(reinterpret_cast<uintptr_t>(T.src + static_cast<int64_t>(p) * pass_bytes(kBB)) & 15u);
+    typename FmtDigits<FMT>::type D;
     int b = 0, rloc = 0;
     if (valid) {
-      decode_block(stage, delta + static_cast<uint32_t>(tid) * kBlockBytes, D);
+      decode_block(stage, delta + static_cast<uint32_t>(tid) * kBB, D);
       rloc = u / nb;
       b = u - rloc * nb;
     }
@@ -380,9 +388,9 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const MmvArgs a) {
 }
 
 // ----------------------------------------------------------------- host ---
-template <int CMAX, int MODE>
+template <int CMAX, int MODE, int FMT>
 static size_t smem_bytes(int cc, int nb, int rt) {
-  size_t b = static_cast<size_t>(kStages) * kStageBytes;
+  size_t b = static_cast<size_t>(kStages) * stage_bytes(fmt_block_bytes<FMT>());
   b += static_cast<size_t>(cc) * nb * kRecWords * 4;
   b += static_cast<size_t>(kPassUnits) * cc * 4;
   b += static_cast<size_t>(rt) * CMAX * 4 + 4;
@@ -391,10 +399,11 @@ static size_t smem_bytes(int cc, int nb, int rt) {
   return b;
 }
 
-template <int CMAX, int MODE>
+template <int CMAX, int MODE, int FMT>
 static int launch_rung(const MmvArgs& args0, int grid, cudaStream_t s) {
   MmvArgs a = args0;
-  const size_t bytes = smem_bytes<CMAX, MODE>(a.cc, a.nb, a.rt);
+  a.bb = fmt_block_bytes<FMT>();
+  const size_t bytes = smem_bytes<CMAX, MODE, FMT>(a.cc, a.nb, a.rt);
   const DeviceInfo& di = device_info();
   if (bytes > di.max_smem_optin) return TQ1_ERR_UNSUPPORTED;
   // Allow the device's full opt-in shared memory (less the kernel's static
@@ -403,9 +412,9 @@ static int launch_rung(const MmvArgs& args0, int grid, cudaStream_t s) {
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
   if (max_dyn[di.device] == 0) {
     cudaFuncAttributes fa{};
-    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_kernel<CMAX, MODE>))) return TQ1_ERR_CUDA;
+    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_kernel<CMAX, MODE, FMT>))) return TQ1_ERR_CUDA;
     const size_t lim = di.max_smem_optin - fa.sharedSizeBytes;
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_kernel<CMAX, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_kernel<CMAX, MODE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(lim))))
       return TQ1_ERR_CUDA;
     max_dyn[di.device] = lim;
@@ -421,18 +430,18 @@ static int launch_rung(const MmvArgs& args0, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_kernel<CMAX, MODE>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_kernel<CMAX, MODE, FMT>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 static int dispatch_rung(int rung, const MmvArgs& a, int grid, cudaStream_t s) {
   switch (rung) {
-    case 1: return launch_rung<1, MODE>(a, grid, s);
-    case 2: return launch_rung<2, MODE>(a, grid, s);
-    case 4: return launch_rung<4, MODE>(a, grid, s);
-    case 8: return launch_rung<8, MODE>(a, grid, s);
-    case 16: return launch_rung<16, MODE>(a, grid, s);
-    default: return launch_rung<32, MODE>(a, grid, s);
+    case 1: return launch_rung<1, MODE, FMT>(a, grid, s);
+    case 2: return launch_rung<2, MODE, FMT>(a, grid, s);
+    case 4: return launch_rung<4, MODE, FMT>(a, grid, s);
+    case 8: return launch_rung<8, MODE, FMT>(a, grid, s);
+    case 16: return launch_rung<16, MODE, FMT>(a, grid, s);
+    default: return launch_rung<32, MODE, FMT>(a, grid, s);
   }
 }
 
@@ -443,7 +452,7 @@ static int rung_for(int64_t t) {
 }
 
 int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int64_t n, int64_t k, int64_t t,
-               cudaStream_t s, unsigned* status, const float* res) {
+               cudaStream_t s, unsigned* status, const float* res, int fmt) {
   const DeviceInfo& di = device_info();
   MmvArgs a = {};
   a.w = w;
@@ -468,8 +477,11 @@ int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int
   const int64_t rows_per_cta = (n + grid - 1) / grid;
   const int64_t rt_cap = std::max<int64_t>(1, static_cast<int64_t>(kAccBudget / (4 * rung)));
   a.rt = static_cast<int>(std::min<int64_t>(rows_per_cta, rt_cap));
-  if (part) return dispatch_rung<kModePartials>(rung, a, static_cast<int>(grid), s);
-  return dispatch_rung<kModeY>(rung, a, static_cast<int>(grid), s);
+  if (fmt == kFmtTq2)
+    return part ? dispatch_rung<kModePartials, kFmtTq2>(rung, a, static_cast<int>(grid), s)
+                : dispatch_rung<kModeY, kFmtTq2>(rung, a, static_cast<int>(grid), s);
+  if (part) return dispatch_rung<kModePartials, kFmtTq1>(rung, a, static_cast<int>(grid), s);
+  return dispatch_rung<kModeY, kFmtTq1>(rung, a, static_cast<int>(grid), s);
 }
 
 int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float* y, int64_t n, int64_t k,
@@ -493,7 +505,7 @@ int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float*
   if (cc < 1) return TQ1_ERR_UNSUPPORTED;
   a.cc = static_cast<int>(cc);
   a.rt = static_cast<int>(kAccBudget / (4 * 32));
-  return launch_rung<32, kModeMoe>(a, di.num_sms, s);
+  return launch_rung<32, kModeMoe, kFmtTq1>(a, di.num_sms, s);
 }
 
 }  // namespace tq1

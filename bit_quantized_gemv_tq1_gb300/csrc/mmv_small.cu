@@ -1,5 +1,6 @@
 // mmv_small.cu -- TQ1_0 x Q8_1 mat-vec for 1, 2 and 4 token columns: the
-// decode path.
+// decode path.  The same kernel runs TQ2_0 weights, whose 2-bit codes are
+// already in the packed-digit layout below (no expansion step).
 //
 // PrismML-Eng/llama.cpp issue #139, "Proposed approach" option 1: a kernel
 // that consumes whole 256-element blocks and iterates over packed bytes, so
@@ -91,15 +92,16 @@ struct SmallArgs {
 
 }  // namespace
 
-template <int C, bool RES, bool F32IN>
+template <int C, bool RES, bool F32IN, int FMT>
 __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(const SmallArgs a) {
+  constexpr int kBB = fmt_block_bytes<FMT>();
   constexpr int kThreads = SmallCfg<C>::kThreads;
   constexpr int kWarps = kThreads / 32;
   constexpr int kHeld = SmallCfg<C>::kHeld;
   extern __shared__ __align__(128) uint8_t smem[];
   const int nb = a.nb;
   const int nkc = a.nkc;  // 8-block chunks per row
-  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBlockBytes;
+  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBB;
   const uint32_t gstride = group_stride(rowbytes);
   // Layout: slab | activation records | per-(row, chunk) partials | barriers
   uint8_t* slab = smem;
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
     T.live = T.row < rows && b < nb;
     const uint32_t gbase = static_cast<uint32_t>(rs + T.g * kRowsPerTask) * rowbytes;
     T.off = static_cast<uint32_t>(T.g) * gstride + ((wlow + gbase) & 15u) + static_cast<uint32_t>(r) * rowbytes +
-            static_cast<uint32_t>(b) * kBlockBytes;
+            static_cast<uint32_t>(b) * kBB;
     return T;
   };
 
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
     if (task < ntasks0) {
       const TaskPos T = task_pos(0, task);
       if (!mbar_wait(&bars[T.g], 0)) ok = false;
-      if (ok && T.live) expand_pack(slab, T.off, held[h]);
+      if (ok && T.live) unit_pack<FMT>(slab, T.off, held[h]);
     }
   }
 
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
         break;
       }
       Packed P;
-      if (T.live) expand_pack(slab, T.off, P);
+      if (T.live) unit_pack<FMT>(slab, T.off, P);
       dot_task(T, P);
     }
     abort = __syncthreads_or(!ok) != 0;  // slab free, all tasks of the round done
@@ -301,7 +303,7 @@ static size_t small_smem(int nb, int rows_cta, uint32_t slab_bytes) {
   return b;
 }
 
-template <int C, bool RES, bool F32IN>
+template <int C, bool RES, bool F32IN, int FMT>
 static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   const DeviceInfo& di = device_info();
   const size_t bytes = small_smem<C>(a.nb, a.rows_cta, a.slab_bytes);
@@ -309,14 +311,14 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
   if (max_dyn[di.device] == 0) {
     cudaFuncAttributes fa{};
-    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C, RES, F32IN>))) return TQ1_ERR_CUDA;
+    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C, RES, F32IN, FMT>))) return TQ1_ERR_CUDA;
     const size_t lim = di.max_smem_optin - fa.sharedSizeBytes;
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(lim))))
       return TQ1_ERR_CUDA;
     // Two CTAs of consecutive calls share an SM: ask for the largest
     // shared-memory carveout so the L1 split never limits residency.
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN, FMT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
       return TQ1_ERR_CUDA;
     max_dyn[di.device] = lim;
   }
@@ -331,13 +333,13 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_small_kernel<C, RES, F32IN>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_small_kernel<C, RES, F32IN, FMT>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
 }
 
 // Returns TQ1_ERR_UNSUPPORTED (launching nothing) when the shape does not
 // fit this kernel's staging; the caller then uses the general kernel.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status, const float* res, const float* x) {
+                     unsigned* status, const float* res, const float* x, int fmt) {
   if (t < 1 || t > 4) return TQ1_ERR_UNSUPPORTED;
   const DeviceInfo& di = device_info();
   SmallArgs a = {};
@@ -352,7 +354,7 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.nb = static_cast<int>(k / kQK);
   const int rung = t == 1 ? 1 : (t == 2 ? 2 : 4);
   const uint32_t slab = rung == 1 ? SmallCfg<1>::kSlab : (rung == 2 ? SmallCfg<2>::kSlab : SmallCfg<4>::kSlab);
-  const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * kBlockBytes;
+  const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes);
   // Shared memory is sized to the CTA's rows (capped at the rung's slab
   // budget): two CTAs of consecutive calls must fit on one SM together.
   const int64_t grid = std::min<int64_t>(di.num_sms, n);
@@ -365,16 +367,25 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.nkc = (a.nb + kLanesPerRow - 1) / kLanesPerRow;
   a.nkc_magic = a.nkc > 1 ? static_cast<uint32_t>(((uint64_t{1} << 32) + a.nkc - 1) / a.nkc) : 0u;
   if (static_cast<int64_t>(a.rows_round / kRowsPerTask) * a.nkc >= (int64_t{1} << 20)) return TQ1_ERR_UNSUPPORTED;
+  const int g = static_cast<int>(grid);
+  if (fmt == kFmtTq2) {  // plain mat-vec only
+    if (x || res) return TQ1_ERR_UNSUPPORTED;
+    switch (rung) {
+      case 1: return launch_small_rung<1, false, false, kFmtTq2>(a, g, s);
+      case 2: return launch_small_rung<2, false, false, kFmtTq2>(a, g, s);
+      default: return launch_small_rung<4, false, false, kFmtTq2>(a, g, s);
+    }
+  }
   switch (rung) {
-    case 1: return x ? launch_small_rung<1, false, true>(a, static_cast<int>(grid), s)
-                     : (res ? launch_small_rung<1, true, false>(a, static_cast<int>(grid), s)
-                            : launch_small_rung<1, false, false>(a, static_cast<int>(grid), s));
-    case 2: return x ? launch_small_rung<2, false, true>(a, static_cast<int>(grid), s)
-                     : (res ? launch_small_rung<2, true, false>(a, static_cast<int>(grid), s)
-                            : launch_small_rung<2, false, false>(a, static_cast<int>(grid), s));
-    default: return x ? launch_small_rung<4, false, true>(a, static_cast<int>(grid), s)
-                      : (res ? launch_small_rung<4, true, false>(a, static_cast<int>(grid), s)
-                             : launch_small_rung<4, false, false>(a, static_cast<int>(grid), s));
+    case 1: return x ? launch_small_rung<1, false, true, kFmtTq1>(a, g, s)
+                     : (res ? launch_small_rung<1, true, false, kFmtTq1>(a, g, s)
+                            : launch_small_rung<1, false, false, kFmtTq1>(a, g, s));
+    case 2: return x ? launch_small_rung<2, false, true, kFmtTq1>(a, g, s)
+                     : (res ? launch_small_rung<2, true, false, kFmtTq1>(a, g, s)
+                            : launch_small_rung<2, false, false, kFmtTq1>(a, g, s));
+    default: return x ? launch_small_rung<4, false, true, kFmtTq1>(a, g, s)
+                      : (res ? launch_small_rung<4, true, false, kFmtTq1>(a, g, s)
+                             : launch_small_rung<4, false, false, kFmtTq1>(a, g, s));
   }
 }
 

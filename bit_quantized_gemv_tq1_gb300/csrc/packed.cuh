@@ -117,6 +117,34 @@ __device__ __forceinline__ void expand_pack(const uint8_t* slab, uint32_t off, P
   Q.dw = __half2float(__ushort_as_half(static_cast<unsigned short>((w[13] >> sh) & 0xFFFFu)));
 }
 
+// TQ2_0 block at byte offset `off` (even) of `slab`: its qs words already
+// are packed-digit registers.  qs word i < 8 holds, in field f of byte lane
+// m, element 32f + 4i + m (chunk f, activation word i): exactly register a[i];
+// qs word 8 + i holds chunk 4 + f, word i: register b[i].  Reads 68 bytes
+// from (off & ~3).
+__device__ __forceinline__ void load_pack_tq2(const uint8_t* slab, uint32_t off, Packed& Q) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(slab + (off & ~3u));
+  const uint32_t sh = (off & 2u) * 8u;
+  uint32_t w[17];
+#pragma unroll
+  for (int m = 0; m < 17; ++m) w[m] = p[m];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    Q.a[i] = __funnelshift_r(w[i], w[i + 1], sh);
+    Q.b[i] = __funnelshift_r(w[8 + i], w[9 + i], sh);
+  }
+  Q.dw = __half2float(__ushort_as_half(static_cast<unsigned short>((w[16] >> sh) & 0xFFFFu)));
+}
+
+// Packed registers of one block of either weight format.
+template <int FMT>
+__device__ __forceinline__ void unit_pack(const uint8_t* slab, uint32_t off, Packed& Q) {
+  if (FMT == kFmtTq2)
+    load_pack_tq2(slab, off, Q);
+  else
+    expand_pack(slab, off, Q);
+}
+
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   int d;
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));

@@ -1,5 +1,5 @@
-// quantize.cu -- fp32 -> TQ1_0 weight blocks and fp32 -> Q8_1 activation
-// blocks, bit-exact with the rounding readings of the library:
+// quantize.cu -- fp32 -> TQ1_0 (and TQ2_0) weight blocks and fp32 -> Q8_1
+// activation blocks, bit-exact with the rounding readings of the library:
 //   weights: d = fp16(amax); t = amax ? clamp(round_half_away(w / amax), -1, 1) : 0
 //   activations: d = amax / 127; q = d ? clamp(round_half_away(x / d), -127, 127) : 0;
 //                stored fp16(d), fp16(d * sum(q)), q[32]
@@ -82,6 +82,53 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) quantize_rows_kernel(const 
   __threadfence();
 }
 
+// TQ2_0 (four 2-bit codes per byte, code = trit + 1; chunk c reads field
+// c % 4 of bytes 32(c/4) .. 32(c/4)+31): one warp per 256-weight block, lane
+// i packs qs[i] from elements i + 32f and qs[32 + i] from 128 + i + 32f
+// (f < 4).  Same scale and rounding as the TQ1_0 encoder.
+__global__ void __launch_bounds__(kWarpsPerCta * 32) quantize_rows_tq2_kernel(const float* __restrict__ w,
+                                                                              uint8_t* __restrict__ out,
+                                                                              int64_t nblocks) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t blk = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (blk < nblocks) {
+    const float* x = w + blk * kQK;
+    float v[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int f = 0; f < 4; ++f) v[h][f] = x[128 * h + 32 * f + lane];
+    float m = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int f = 0; f < 4; ++f) m = fmaxf(m, fabsf(v[h][f]));
+    const float amax = warp_max(m);
+    uint8_t* o = out + blk * kTq2BlockBytes;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t byte = 0;
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        int code = 1;
+        if (amax != 0.0f) {
+          float r = roundf(__fdiv_rn(v[h][f], amax));  // roundf: halves away from zero
+          r = fminf(fmaxf(r, -1.0f), 1.0f);
+          code = static_cast<int>(r) + 1;
+        }
+        byte |= static_cast<uint32_t>(code) << (2 * f);
+      }
+      o[32 * h + lane] = static_cast<uint8_t>(byte);
+    }
+    if (lane == 0) {  // fp16 scale: one 16-bit store (66 * blk + 64 is even)
+      const __half_raw d16 = __float2half_rn(amax);
+      *reinterpret_cast<unsigned short*>(o + 64) = d16.x;
+    }
+  }
+  __threadfence();
+}
+
 // One warp per Q8_1 block of 32 activations.  This kernel does not signal
 // its dependents early: its grid spans several waves, and a dependent grid
 // admitted while those waves are still being placed ends up unevenly spread
@@ -135,6 +182,10 @@ static int launch_simple(void (*kern)(const float*, uint8_t*, int64_t), const fl
 
 int launch_quantize_rows(const float* w, uint8_t* blocks, int64_t n, int64_t k, cudaStream_t s) {
   return launch_simple(quantize_rows_kernel, w, blocks, n * (k / kQK), s);
+}
+
+int launch_quantize_rows_tq2(const float* w, uint8_t* blocks, int64_t n, int64_t k, cudaStream_t s) {
+  return launch_simple(quantize_rows_tq2_kernel, w, blocks, n * (k / kQK), s);
 }
 
 int launch_quantize_acts(const float* x, uint8_t* q8, int64_t t, int64_t k, cudaStream_t s) {

@@ -9,6 +9,13 @@
 //   e <  240: byte qs[32 + (e-160) % 16], digit (e-160) / 16  (same pattern)
 //   e >= 240: byte qh[(e-240) % 4],       digit (e-240) / 4   (same pattern)
 // Q8_1 activation block: fp16 d, fp16 s, int8 q[32] (36 bytes).
+//
+// TQ2_0, the 2-bit sibling format the same page names ("Upstream state")
+// without giving its layout; this library reads it as: 256 ternary weights
+// in 66 bytes, qs[64] holding four 2-bit codes per byte (code = trit + 1),
+// then an fp16 scale d.  Chunk c (elements 32c .. 32c+31) reads field c % 4
+// (bits 2(c%4) .. 2(c%4)+1) of bytes qs[32(c/4) .. 32(c/4)+31], the page's
+// chunk pattern with four codes per byte.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -19,6 +26,14 @@ namespace tq1 {
 
 constexpr int kQK = 256;          // weights per TQ1_0 block
 constexpr int kBlockBytes = 54;   // qs[48] + qh[4] + fp16 d
+constexpr int kTq2BlockBytes = 66;  // TQ2_0: qs[64] + fp16 d
+
+// Weight formats of the mat-vec kernels.
+enum : int { kFmtTq1 = 0, kFmtTq2 = 1 };
+template <int FMT>
+__host__ __device__ constexpr int fmt_block_bytes() {
+  return FMT == kFmtTq2 ? kTq2BlockBytes : kBlockBytes;
+}
 constexpr int kQK8 = 32;          // activations per Q8_1 block
 constexpr int kQ8Bytes = 36;      // fp16 d + fp16 s + int8 q[32]
 
@@ -188,6 +203,30 @@ __device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, 
   D.dw = __half2float(__ushort_as_half(static_cast<unsigned short>((w[13] >> sh) & 0xFFFFu)));
 }
 
+// TQ2_0 block as 64 dp4a-ready words: d[c][w] holds the codes of chunk c,
+// activation word w (byte lanes 0..3, values 0..3), plus the scale.
+struct BlockDigits2 {
+  uint32_t d[8][8];
+  float dw;
+};
+
+// Decode the TQ2_0 block at byte offset `off` (even) of shared memory region
+// `base`.  Reads 68 bytes from (off & ~3).
+__device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, BlockDigits2& D) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(base + (off & ~3u));
+  const uint32_t sh = (off & 2u) * 8u;  // 0 or 16
+  uint32_t w[17];
+#pragma unroll
+  for (int m = 0; m < 17; ++m) w[m] = p[m];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t q = __funnelshift_r(w[i], w[i + 1], sh);
+#pragma unroll
+    for (int f = 0; f < 4; ++f) D.d[4 * (i >> 3) + f][i & 7] = (q >> (2 * f)) & 0x03030303u;
+  }
+  D.dw = __half2float(__ushort_as_half(static_cast<unsigned short>((w[16] >> sh) & 0xFFFFu)));
+}
+
 // Activation record of one column over one 256-block, in shared memory:
 //   words  0..63: the 8 Q8_1 chunks' int8 values (chunk j at words 8j..8j+7)
 //   words 64..71: the 8 chunk scales as fp32
@@ -248,8 +287,41 @@ __device__ __forceinline__ void block_partials(const BlockDigits& D, const uint3
   }
 }
 
+__device__ __forceinline__ void block_partials(const BlockDigits2& D, const uint32_t* rec, int (&I)[8]) {
+  const int4 s0 = *reinterpret_cast<const int4*>(rec + 72);
+  const int4 s1 = *reinterpret_cast<const int4*>(rec + 76);
+  I[0] = s0.x; I[1] = s0.y; I[2] = s0.z; I[3] = s0.w;
+  I[4] = s1.x; I[5] = s1.y; I[6] = s1.z; I[7] = s1.w;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 q0 = *reinterpret_cast<const uint4*>(rec + 8 * c);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(rec + 8 * c + 4);
+    int acc = I[c];
+    acc = __dp4a(static_cast<int>(D.d[c][0]), static_cast<int>(q0.x), acc);
+    acc = __dp4a(static_cast<int>(D.d[c][1]), static_cast<int>(q0.y), acc);
+    acc = __dp4a(static_cast<int>(D.d[c][2]), static_cast<int>(q0.z), acc);
+    acc = __dp4a(static_cast<int>(D.d[c][3]), static_cast<int>(q0.w), acc);
+    acc = __dp4a(static_cast<int>(D.d[c][4]), static_cast<int>(q1.x), acc);
+    acc = __dp4a(static_cast<int>(D.d[c][5]), static_cast<int>(q1.y), acc);
+    acc = __dp4a(static_cast<int>(D.d[c][6]), static_cast<int>(q1.z), acc);
+    acc = __dp4a(static_cast<int>(D.d[c][7]), static_cast<int>(q1.w), acc);
+    I[c] = acc;
+  }
+}
+
+// Digit words of one block per weight format.
+template <int FMT>
+struct FmtDigits {
+  using type = BlockDigits;
+};
+template <>
+struct FmtDigits<kFmtTq2> {
+  using type = BlockDigits2;
+};
+
 // d_w * sum_j d_a[j] * I_j for one block, fp32, fixed order.
-__device__ __forceinline__ float block_dot(const BlockDigits& D, const uint32_t* rec) {
+template <class Digits>
+__device__ __forceinline__ float block_dot(const Digits& D, const uint32_t* rec) {
   int I[8];
   block_partials(D, rec, I);
   const float4 a0 = *reinterpret_cast<const float4*>(rec + 64);

@@ -23,19 +23,21 @@ bool cuda_ok(cudaError_t err);
 
 // Kernel launchers.  All return a TQ1_* status code and never synchronise.
 int launch_quantize_rows(const float* w, uint8_t* blocks, int64_t n, int64_t k, cudaStream_t s);
+int launch_quantize_rows_tq2(const float* w, uint8_t* blocks, int64_t n, int64_t k, cudaStream_t s);
 int launch_quantize_acts(const float* x, uint8_t* q8, int64_t t, int64_t k, cudaStream_t s);
 
 // y[c][r] (y != nullptr) or int32 partials part[c][r][k/32] (part != nullptr)
 // for columns c < t <= 32.  `res` (optional, y's layout) is added to y.
+// `fmt`: kFmtTq1 (TQ1_0 blocks) or kFmtTq2 (TQ2_0 blocks).
 int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int64_t n, int64_t k, int64_t t,
-               cudaStream_t s, unsigned* status, const float* res = nullptr);
+               cudaStream_t s, unsigned* status, const float* res = nullptr, int fmt = 0);
 
 // Decode-path kernel for 1 <= t <= 4 columns.  Returns TQ1_ERR_UNSUPPORTED
 // without launching when the shape does not fit its staging.
 // With `x` (fp32 activations [t][k]) the kernel quantises them to Q8_1 in its
 // prologue and `q8` is unused.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status, const float* res = nullptr, const float* x = nullptr);
+                     unsigned* status, const float* res = nullptr, const float* x = nullptr, int fmt = 0);
 
 // Expert-routed mat-vec over a compacted routing table in `ws` (general
 // dp4a kernel).

@@ -22,6 +22,15 @@
  *   Q8_1 block, 36 bytes, 32 activations: fp16 d @0, fp16 s @2, int8 q[32] @4.
  *   A [t][k] activation matrix is [t][k/32] blocks.
  *
+ *   TQ2_0 block, 66 bytes, 256 weights (the 2-bit sibling format the same
+ *   page names in "Upstream state" without a layout; this library's reading):
+ *     bytes  0..63  qs[64]  four 2-bit codes per byte, code = trit + 1
+ *     bytes 64..65  d       fp16 scale, little-endian
+ *   Element e of a block is field (e/32) % 4 (bits 2f..2f+1) of byte
+ *   qs[32 * (e/128) + e % 32]: chunk c reads one field of 32 consecutive
+ *   bytes, the chunk pattern above with four codes per byte.  Code 3 is never
+ *   written and decodes to +2*d.
+ *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller and must be
  *     16-byte aligned (TQ1_ERR_ALIGN otherwise).  The library never
@@ -73,8 +82,10 @@ const char* tq1_version(void);
  * library (empty if none); explains a TQ1_ERR_CUDA. */
 const char* tq1_last_cuda_error(void);
 
-/* Bytes of a TQ1_0 matrix [n][k/256] and of a Q8_1 matrix [t][k/32]. */
+/* Bytes of a TQ1_0 matrix [n][k/256], a TQ2_0 matrix [n][k/256] and a Q8_1
+ * matrix [t][k/32]. */
 size_t tq1_blocks_bytes(int64_t n, int64_t k);
+size_t tq2_blocks_bytes(int64_t n, int64_t k);
 size_t tq1_q8_1_bytes(int64_t t, int64_t k);
 
 /*
@@ -232,6 +243,33 @@ int tq1_mmv_id_noalloc(const void* expert_blocks, int64_t n_experts, const void*
  * itself reported an error).
  */
 int tq1_sync_status(void* stream);
+
+/*
+ * TQ2_0 weights (2-bit codes; format at the top of this file).
+ *
+ * tq2_quantize_rows: fp32 w[n][k] -> TQ2_0 blocks, with the same scale and
+ * trit rounding as tq1_quantize_rows (so both formats hold the same trits and
+ * scales for the same weights).  Bit-exact, deterministic.
+ *
+ * tq2_mmv: y[c][r] = sum_k w[r][k] * x[c][k] for TQ2_0 blocks [n][k/256] and
+ * Q8_1 q8 [t][k/32], accumulated exactly as tq1_mmv (exact int32 per-32
+ * partials, fp32 scale-and-sum per block).  t <= 4 runs the decode kernel
+ * (the codes already are its packed-digit registers: masked dp4a, no
+ * expansion); larger t runs the general dp4a kernel in chunks of up to 32
+ * columns.  No scratch.  Deterministic.
+ *
+ * tq2_mmv_partials: the exact int32 partials part[c][r][k/32] of tq2_mmv
+ * (debug, as tq1_mmv_partials).
+ *
+ * Arguments, alignment, shapes and errors as the TQ1_0 counterparts.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Upstream state" (TQ2_0 as the
+ * stalled sibling of the TQ1_0 port) and "Proposed approach" (whole-block
+ * kernels that load each packed byte once).
+ */
+int tq2_quantize_rows(const float* w, void* blocks, int64_t n, int64_t k, void* stream);
+int tq2_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream);
+int tq2_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,
+                     void* stream);
 
 #ifdef __cplusplus
 }

@@ -30,7 +30,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_id", "tq1_mmv_partials",
                  "tq1_mmv_id_workspace_size", "tq1_sync_status", "tq1_status_string", "tq1_dequantize_rows",
-                 "tq1_get_rows"):
+                 "tq1_get_rows", "tq2_quantize_rows", "tq2_mmv", "tq2_mmv_partials", "tq2_blocks_bytes"):
         assert want in names
 
 
@@ -109,3 +109,16 @@ def test_dequant_host_checks(lib):
     assert lib.tq1_get_rows(FAKE, FAKE, -1, FAKE, 4, 256, 0, None) == -2
     assert lib.tq1_get_rows(FAKE, FAKE + 4, 3, FAKE, 4, 256, 0, None) == -3
     assert lib.tq1_get_rows(None, None, 0, None, 4, 256, 0, None) == 0
+
+
+def test_tq2_host_checks(lib):
+    assert L.tq2_blocks_bytes(5120, 6144) == 5120 * 24 * 66
+    assert lib.tq2_quantize_rows(FAKE, FAKE, 4, 100, None) == -2
+    assert lib.tq2_quantize_rows(None, FAKE, 4, 256, None) == -1
+    assert lib.tq2_quantize_rows(FAKE, FAKE + 2, 4, 256, None) == -3
+    assert lib.tq2_mmv(FAKE, FAKE, FAKE, 10, 300, 1, None) == -2
+    assert lib.tq2_mmv(FAKE, None, FAKE, 10, 256, 1, None) == -1
+    assert lib.tq2_mmv(FAKE + 4, FAKE, FAKE, 10, 256, 1, None) == -3
+    assert lib.tq2_mmv(FAKE, FAKE, FAKE, 10, 256 * 246, 1, None) == -4
+    assert lib.tq2_mmv(None, None, None, 0, 256, 3, None) == 0
+    assert lib.tq2_mmv_partials(FAKE, FAKE, None, 4, 256, 1, None) == -1
