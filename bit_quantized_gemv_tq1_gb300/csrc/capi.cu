@@ -169,8 +169,8 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
   const uint8_t* w = static_cast<const uint8_t*>(blocks);
   const uint8_t* a = static_cast<const uint8_t*>(q8);
   const int64_t q8_row = (k / kQK8) * kQ8Bytes;
-  if (y && t >= kTileMinT && fmt == kFmtTq1) {
-    rc = launch_tile(w, a, y, n, k, t, s, st, res);
+  if (y && t >= kTileMinT) {
+    rc = launch_tile(w, a, y, n, k, t, s, st, res, fmt);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the dp4a kernels below
   }
   if (y && t <= 4) {

@@ -58,6 +58,11 @@
 // Requires the weight row stride (k/256 * 54 bytes) to be a multiple of 16
 // (k a multiple of 2048): the launcher returns TQ1_ERR_UNSUPPORTED otherwise
 // and the caller uses the dp4a kernels.
+//
+// TQ2_0 weights (66-byte blocks of 2-bit codes) run the same kernel: the
+// 80-byte window still covers a block at any even offset (14 + 66 bytes), the
+// row-stride rule is the same (k a multiple of 2048), and the expansion is a
+// shift and mask per chunk word before the same byte permute to fp16.
 #include <cuda.h>
 
 #include <algorithm>
@@ -365,6 +370,30 @@ __device__ __forceinline__ void expand_quarter(const uint32_t (&wv)[13], uint32_
   }
 }
 
+// TQ2_0: quarter Q (chunks 2Q, 2Q + 1) from the block's 16 qs words; chunk j
+// reads field j % 4 of qs words 8 * (j / 4) .. + 7.  Code 3 (never written by
+// the encoder) selects bytes 6-7 of the table, which hold fp16(2 d_w).
+template <int Q>
+__device__ __forceinline__ void expand_quarter_tq2(const uint32_t (&wv)[16], uint32_t tlo, uint32_t thi,
+                                                   uint32_t (&out)[32]) {
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    const int j = 2 * Q + jj;
+#pragma unroll
+    for (int wd = 0; wd < 8; ++wd) {
+      const uint32_t D = (wv[8 * (j >> 2) + wd] >> (2 * (j & 3))) & 0x03030303u;
+      digits_to_f16(D, tlo, thi, out[16 * jj + 2 * wd], out[16 * jj + 2 * wd + 1]);
+    }
+  }
+}
+
+template <int J0>
+__device__ __forceinline__ void realign_tq2(const uint32_t (&W)[20], uint32_t sh, uint32_t (&wv)[16], uint32_t& h) {
+#pragma unroll
+  for (int m = 0; m < 16; ++m) wv[m] = __funnelshift_r(W[J0 + m], W[J0 + m + 1], sh);
+  h = (W[J0 + 16] >> sh) & 0xFFFFu;
+}
+
 // The 13 logical words of a block and its fp16 scale from the row's raw
 // window W (20 words), where the block starts 4*J0 + sh/8 bytes in.
 template <int J0>
@@ -454,10 +483,11 @@ __global__ void __launch_bounds__(kPrepThreads) tile_prep_kernel(const uint8_t* 
   }
 }
 
-template <int TOK>
+template <int TOK, int FMT>
 __global__ void __launch_bounds__(kTThreads, 1)
     tile_kernel(const TileArgs a, const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmb) {
   using C = TileCfg<TOK>;
+  constexpr int kBB = fmt_block_bytes<FMT>();
   extern __shared__ __align__(1024) uint8_t tsmem_raw[];
   __shared__ __align__(8) uint64_t afull_bar[kGroups], aempty_bar[kGroups];
   __shared__ __align__(8) uint64_t bfull_bar[C::kRB], bempty_bar[C::kRB];
@@ -503,7 +533,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const int bi = static_cast<int>(j % nblk);
     const int row0 = (unit_tile(static_cast<int>(j / nblk)) / a.tiles_n) * kTileRows;
     mbar_arrive_expect_tx(&wfull_bar[ws], kWRawBytes);
-    tma_load_2d(wraw + ws * kWRawBytes, &tmw, ((kb0 + bi) * kBlockBytes) & ~15, row0, &wfull_bar[ws]);
+    tma_load_2d(wraw + ws * kWRawBytes, &tmw, ((kb0 + bi) * kBB) & ~15, row0, &wfull_bar[ws]);
   };
   const uint32_t nfirst = nall < static_cast<uint32_t>(kRW) ? nall : static_cast<uint32_t>(kRW);
 
@@ -574,29 +604,53 @@ __global__ void __launch_bounds__(kTThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty_bar[ws]);
-      const uint32_t off = static_cast<uint32_t>((kb0 + bi) * kBlockBytes) & 15u;
+      const uint32_t off = static_cast<uint32_t>((kb0 + bi) * kBB) & 15u;
       const uint32_t sh = (off & 2u) * 8u;
-      uint32_t wv[13], h;
-      switch (off >> 2) {
-        case 0: realign<0>(W, sh, wv, h); break;
-        case 1: realign<1>(W, sh, wv, h); break;
-        case 2: realign<2>(W, sh, wv, h); break;
-        default: realign<3>(W, sh, wv, h); break;
-      }
-      const uint32_t tlo = h ^ 0x8000u;  // bytes 0-1: -d_w, bytes 2-3: 0
-      const uint32_t thi = h;            // bytes 4-5: +d_w
-      // The slot is free once the MMAs of this group's previous block are done.
-      if (!warp_wait(&aempty_bar[g], (c & 1u) ^ 1u, abort_flag)) break;
-      tc_fence_after();
       uint32_t out[32];
-      expand_quarter<0>(wv, tlo, thi, out);
-      tmem_st32(tslot + 0 * 32, out);
-      expand_quarter<1>(wv, tlo, thi, out);
-      tmem_st32(tslot + 1 * 32, out);
-      expand_quarter<2>(wv, tlo, thi, out);
-      tmem_st32(tslot + 2 * 32, out);
-      expand_quarter<3>(wv, tlo, thi, out);
-      tmem_st32(tslot + 3 * 32, out);
+      if (FMT == kFmtTq2) {
+        uint32_t wv[16], h;
+        switch (off >> 2) {
+          case 0: realign_tq2<0>(W, sh, wv, h); break;
+          case 1: realign_tq2<1>(W, sh, wv, h); break;
+          case 2: realign_tq2<2>(W, sh, wv, h); break;
+          default: realign_tq2<3>(W, sh, wv, h); break;
+        }
+        const uint32_t tlo = h ^ 0x8000u;  // bytes 0-1: -d_w, bytes 2-3: 0
+        const uint32_t h2 = __half_as_ushort(__float2half_rn(2.0f * __half2float(__ushort_as_half(
+                                static_cast<unsigned short>(h)))));
+        const uint32_t thi = h | (h2 << 16);  // bytes 4-5: +d_w, bytes 6-7: +2 d_w
+        if (!warp_wait(&aempty_bar[g], (c & 1u) ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        expand_quarter_tq2<0>(wv, tlo, thi, out);
+        tmem_st32(tslot + 0 * 32, out);
+        expand_quarter_tq2<1>(wv, tlo, thi, out);
+        tmem_st32(tslot + 1 * 32, out);
+        expand_quarter_tq2<2>(wv, tlo, thi, out);
+        tmem_st32(tslot + 2 * 32, out);
+        expand_quarter_tq2<3>(wv, tlo, thi, out);
+        tmem_st32(tslot + 3 * 32, out);
+      } else {
+        uint32_t wv[13], h;
+        switch (off >> 2) {
+          case 0: realign<0>(W, sh, wv, h); break;
+          case 1: realign<1>(W, sh, wv, h); break;
+          case 2: realign<2>(W, sh, wv, h); break;
+          default: realign<3>(W, sh, wv, h); break;
+        }
+        const uint32_t tlo = h ^ 0x8000u;  // bytes 0-1: -d_w, bytes 2-3: 0
+        const uint32_t thi = h;            // bytes 4-5: +d_w
+        // The slot is free once the MMAs of this group's previous block are done.
+        if (!warp_wait(&aempty_bar[g], (c & 1u) ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        expand_quarter<0>(wv, tlo, thi, out);
+        tmem_st32(tslot + 0 * 32, out);
+        expand_quarter<1>(wv, tlo, thi, out);
+        tmem_st32(tslot + 1 * 32, out);
+        expand_quarter<2>(wv, tlo, thi, out);
+        tmem_st32(tslot + 2 * 32, out);
+        expand_quarter<3>(wv, tlo, thi, out);
+        tmem_st32(tslot + 3 * 32, out);
+      }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
@@ -869,7 +923,7 @@ cudaMemPool_t scratch_pool(int dev) {
   return pools[dev];
 }
 
-template <int TOK>
+template <int TOK, int FMT>
 int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms, cudaStream_t s) {
   using C = TileCfg<TOK>;
   const DeviceInfo& di = device_info();
@@ -877,7 +931,7 @@ int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
   if (C::kSmem + 2048 > di.max_smem_optin) return TQ1_ERR_UNSUPPORTED;
   if (!configured[di.device]) {
-    if (!cuda_ok(cudaFuncSetAttribute(tile_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!cuda_ok(cudaFuncSetAttribute(tile_kernel<TOK, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(C::kSmem))))
       return TQ1_ERR_CUDA;
     configured[di.device] = true;
@@ -886,7 +940,7 @@ int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms
   a.tiles_n = (a.t + TOK - 1) / TOK;
   a.t_pad = a.tiles_n * TOK;
   const int nb = a.k / kQK;
-  const uint64_t rowbytes = static_cast<uint64_t>(nb) * kBlockBytes;
+  const uint64_t rowbytes = static_cast<uint64_t>(nb) * fmt_block_bytes<FMT>();
   const size_t hilo_bytes = 2 * static_cast<size_t>(a.t_pad) * a.k * sizeof(uint16_t);
   const size_t ws_bytes = hilo_bytes + static_cast<size_t>(a.t_pad) * sizeof(float);
 
@@ -942,20 +996,19 @@ int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    if (!cuda_ok(cudaLaunchKernelEx(&cfg, tile_kernel<TOK>, a, tmw, tmb))) rc = TQ1_ERR_CUDA;
+    if (!cuda_ok(cudaLaunchKernelEx(&cfg, tile_kernel<TOK, FMT>, a, tmw, tmb))) rc = TQ1_ERR_CUDA;
   }
   // The scratch goes back to the pool once the kernels above have finished.
   if (!cuda_ok(cudaFreeAsync(ws, s)) && rc == TQ1_OK) rc = TQ1_ERR_CUDA;
   return rc;
 }
 
-}  // namespace
-
-int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                unsigned* status, const float* res) {
+template <int FMT>
+int launch_tile_fmt(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t,
+                           cudaStream_t s, unsigned* status, const float* res) {
   if (n > (int64_t{1} << 30) || t > (int64_t{1} << 24) || k > (int64_t{1} << 30)) return TQ1_ERR_UNSUPPORTED;
   // The weight map's row stride must be a multiple of 16 bytes.
-  if (((k / kQK) * kBlockBytes) % 16 != 0) return TQ1_ERR_UNSUPPORTED;
+  if (((k / kQK) * fmt_block_bytes<FMT>()) % 16 != 0) return TQ1_ERR_UNSUPPORTED;
   const DeviceInfo& di = device_info();
   TileArgs a = {};
   a.y = y;
@@ -964,10 +1017,18 @@ int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_
   a.n = static_cast<int>(n);
   a.k = static_cast<int>(k);
   a.t = static_cast<int>(t);
-  if (t <= 8) return launch_tile_tok<8>(w, q8, a, di.num_sms, s);
-  if (t <= 16) return launch_tile_tok<16>(w, q8, a, di.num_sms, s);
-  if (t <= 32) return launch_tile_tok<32>(w, q8, a, di.num_sms, s);
-  return launch_tile_tok<64>(w, q8, a, di.num_sms, s);
+  if (t <= 8) return launch_tile_tok<8, FMT>(w, q8, a, di.num_sms, s);
+  if (t <= 16) return launch_tile_tok<16, FMT>(w, q8, a, di.num_sms, s);
+  if (t <= 32) return launch_tile_tok<32, FMT>(w, q8, a, di.num_sms, s);
+  return launch_tile_tok<64, FMT>(w, q8, a, di.num_sms, s);
+}
+
+}  // namespace
+
+int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
+                unsigned* status, const float* res, int fmt) {
+  return fmt == kFmtTq2 ? launch_tile_fmt<kFmtTq2>(w, q8, y, n, k, t, s, status, res)
+                        : launch_tile_fmt<kFmtTq1>(w, q8, y, n, k, t, s, status, res);
 }
 
 }  // namespace tq1

@@ -48,8 +48,9 @@ int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float*
 
 // y[c][r] for any t on the tensor cores (tcgen05): 128-row tiles, split-K
 // over a thread-block cluster when the tiles alone cannot fill the GPU.
+// `fmt`: kFmtTq1 or kFmtTq2 weight blocks.
 int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                unsigned* status, const float* res = nullptr);
+                unsigned* status, const float* res = nullptr, int fmt = 0);
 
 // Rows of TQ1_0 blocks to fp32 (f16 = false) or fp16 values: out row i is
 // source row row_ids[i] (row_ids == nullptr: row i).

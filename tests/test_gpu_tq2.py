@@ -1,7 +1,9 @@
 """TQ2_0 (2-bit ternary codes) on the GPU vs the oracle: encoder bytes
 bit-exact, integer partials bit-exact, fp32 outputs within max(1e-3 |ref|,
-1e-4), over the decode rungs (t <= 4), the general kernel (t > 4, chunks of
-32 columns) and the full-size decode workload (sampled rows)."""
+1e-4), over the decode rungs (t <= 4), the general kernel (t > 4 where k is
+not a multiple of 2048, chunks of 32 columns), the tensor-core tile path
+(t >= 7, k a multiple of 2048) and the full-size decode and prefill shapes
+(sampled rows)."""
 import numpy as np
 import pytest
 
@@ -125,3 +127,39 @@ def test_determinism():
     y0 = _mmv(blocks, q8, 700, 4096, 3)
     for _ in range(3):
         np.testing.assert_array_equal(_mmv(blocks, q8, 700, 4096, 3), y0)
+
+
+# t >= 7 with k a multiple of 2048 runs the tensor-core tile path.
+TILE = [(300, 2048, 7), (129, 4096, 12), (640, 6144, 16), (257, 2048, 33), (1000, 4096, 64), (200, 2048, 100)]
+
+
+@pytest.mark.parametrize("n,k,t", TILE)
+def test_tile_path(n, k, t):
+    p = synth.matvec(n, k, t, p_zero=0.4, seed=3 * n + k + t)
+    blocks, q8 = _quantize_tq2(p.w), G.quantize_acts(p.x)
+    ref = orc.tq2_mmv_f64(orc.tq2_encode_rows(p.w), orc.q8_1_quantize(p.x), n, k, t)
+    G.assert_close(_mmv(blocks, q8, n, k, t), ref)
+
+
+def test_tile_path_code_three():
+    # Raw blocks with every code, including the unused 3 (+2 d), through the
+    # fp16 table of the tensor-core expansion.
+    n, k, t = 130, 2048, 9
+    rng = np.random.default_rng(19)
+    raw = rng.integers(0, 256, size=(n, k // 256, TQ2_BYTES), dtype=np.uint8)
+    d = rng.uniform(0.01, 0.1, size=(n, k // 256)).astype(np.float16)
+    raw[:, :, 64:66] = d.view(np.uint8).reshape(n, k // 256, 2)
+    x = synth.matvec(1, k, t, seed=2).x
+    y = _mmv(G.dev(raw.reshape(-1)), G.quantize_acts(x), n, k, t)
+    G.assert_close(y, orc.tq2_mmv_f64(raw, orc.q8_1_quantize(x), n, k, t))
+
+
+def test_prefill_shape_sampled_rows():
+    # N=14336, K=4096, T=512 (the prefill workload's shape) in TQ2_0.
+    p = synth.config_matvec("c5")
+    blocks = _quantize_tq2(p.w)
+    rng = np.random.default_rng(55)
+    rows = np.unique(np.concatenate([[0, 127, 128, p.n - 1], rng.integers(0, p.n, 60)]))
+    y = _mmv(blocks, G.quantize_acts(p.x), p.n, p.k, p.t)
+    ref = orc.tq2_mmv_f64(orc.tq2_encode_rows(p.w[rows]), orc.q8_1_quantize(p.x), rows.size, p.k, p.t)
+    G.assert_close(y[:, rows], ref)
