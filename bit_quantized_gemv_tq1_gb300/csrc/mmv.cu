@@ -336,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const MmvArgs a) {
             int I[8];
             block_partials(D, act + (static_cast<size_t>(c) * nb + b) * kRecWords, I);
             int4* dst = reinterpret_cast<int4*>(a.part + ((T.col0 + c0 + c) * a.n + T.row0 + rloc) * nq + b * 8);
-            dst[0] = make_int4(I[0], I[1], I[2], I[3]);
-            dst[1] = make_int4(I[4], I[5], I[6], I[7]);
+            dst[0] = make_int4(I[0] - kFloatBias, I[1] - kFloatBias, I[2] - kFloatBias, I[3] - kFloatBias);
+            dst[1] = make_int4(I[4] - kFloatBias, I[5] - kFloatBias, I[6] - kFloatBias, I[7] - kFloatBias);
           }
         }
       } else {

@@ -33,7 +33,12 @@ __host__ __device__ __forceinline__ uint32_t group_stride(uint32_t rowbytes) {
 // four activation words meeting one packed register are contiguous):
 //   words 8w + j  (w, j < 8): int8x4 word w of Q8_1 chunk j
 //   words 64 + j:  chunk j's fp32 scale divided by 4^(j mod 4)
-//   words 72 + j:  -4^(j mod 4) * sum of chunk j's int8 values
+//   words 72 + j:  kFloatBias - 4^(j mod 4) * sum of chunk j's int8 values
+// The dp4a sums of a chunk start from word 72 + j, so they end as
+// kFloatBias + 4^s * I with |4^s * I| <= 64 * 32 * 127 * 2 < 2^22: the bit
+// pattern of the fp32 number 1.5 * 2^23 + 4^s * I, exactly.  One fp32
+// subtraction then gives 4^s * I as a float (no integer-to-float conversion,
+// which issues on a slow pipe).
 constexpr int kPRec = 100;  // stride: 16-byte aligned, 4 banks apart
 
 struct Packed {
@@ -171,14 +176,14 @@ __device__ __forceinline__ float packed_dot(const Packed& P, const uint32_t* rec
   }
   const float4 a0 = *reinterpret_cast<const float4*>(rec + 64);
   const float4 a1 = *reinterpret_cast<const float4*>(rec + 68);
-  float s = a0.x * static_cast<float>(I0);
-  s = fmaf(a0.y, static_cast<float>(I1), s);
-  s = fmaf(a0.z, static_cast<float>(I2), s);
-  s = fmaf(a0.w, static_cast<float>(I3), s);
-  s = fmaf(a1.x, static_cast<float>(I4), s);
-  s = fmaf(a1.y, static_cast<float>(I5), s);
-  s = fmaf(a1.z, static_cast<float>(I6), s);
-  s = fmaf(a1.w, static_cast<float>(I7), s);
+  float s = a0.x * unbias(I0);
+  s = fmaf(a0.y, unbias(I1), s);
+  s = fmaf(a0.z, unbias(I2), s);
+  s = fmaf(a0.w, unbias(I3), s);
+  s = fmaf(a1.x, unbias(I4), s);
+  s = fmaf(a1.y, unbias(I5), s);
+  s = fmaf(a1.z, unbias(I6), s);
+  s = fmaf(a1.w, unbias(I7), s);
   return s * P.dw;
 }
 
@@ -230,7 +235,7 @@ __device__ __forceinline__ void quantize_precord_half(const float* xs, uint32_t*
     const int slot = j & 3;
     const float dh = __half2float(__float2half_rn(d));
     rec[64 + j] = __float_as_uint(dh * __int_as_float((127 - 2 * slot) << 23));  // d / 4^slot, exact
-    rec[72 + j] = static_cast<uint32_t>(-(sum << (2 * slot)));
+    rec[72 + j] = static_cast<uint32_t>(kFloatBias - (sum << (2 * slot)));
   }
 }
 
@@ -248,7 +253,7 @@ __device__ __forceinline__ void fill_precord_chunk(const uint8_t* blk, uint32_t*
   const int slot = j & 3;
   const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(ds & 0xFFFFu)));
   rec[64 + j] = __float_as_uint(d * __int_as_float((127 - 2 * slot) << 23));  // d / 4^slot, exact
-  rec[72 + j] = static_cast<uint32_t>(-(sum << (2 * slot)));
+  rec[72 + j] = static_cast<uint32_t>(kFloatBias - (sum << (2 * slot)));
 }
 
 }  // namespace packed

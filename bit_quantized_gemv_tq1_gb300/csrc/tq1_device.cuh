@@ -227,15 +227,24 @@ __device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, 
   D.dw = __half2float(__ushort_as_half(static_cast<unsigned short>((w[16] >> sh) & 0xFFFFu)));
 }
 
+// Integer dot products seeded with kFloatBias end as the bit pattern of the
+// fp32 number 1.5 * 2^23 + I whenever |I| < 2^22 (every per-chunk partial
+// here: at most 64 * 32 * 127 * 2); one fp32 subtraction of the bias then
+// gives I exactly, without an integer-to-float conversion (a slow pipe).
+constexpr int kFloatBias = 0x4B400000;  // bits of 12582912.0f = 1.5 * 2^23
+constexpr float kFloatBiasValue = 12582912.0f;
+__device__ __forceinline__ float unbias(int v) { return __fsub_rn(__int_as_float(v), kFloatBiasValue); }
+
 // Activation record of one column over one 256-block, in shared memory:
 //   words  0..63: the 8 Q8_1 chunks' int8 values (chunk j at words 8j..8j+7)
 //   words 64..71: the 8 chunk scales as fp32
-//   words 72..79: minus the sum of each chunk's int8 values
+//   words 72..79: kFloatBias minus the sum of each chunk's int8 values
 // Stride 100 words: 16-byte aligned and 4 banks apart for consecutive blocks.
 constexpr int kRecWords = 100;
 
-// Exact per-chunk integer partials I_j = sum (digit - 1) * q over the block.
-// The -1 offset enters as the precomputed -sum(q) accumulator seed.
+// Exact per-chunk integer partials I_j = sum (digit - 1) * q over the block,
+// plus kFloatBias.  The -1 offset enters as the precomputed -sum(q)
+// accumulator seed.
 __device__ __forceinline__ void block_partials(const BlockDigits& D, const uint32_t* rec, int (&I)[8]) {
   const int4 s0 = *reinterpret_cast<const int4*>(rec + 72);
   const int4 s1 = *reinterpret_cast<const int4*>(rec + 76);
@@ -326,14 +335,14 @@ __device__ __forceinline__ float block_dot(const Digits& D, const uint32_t* rec)
   block_partials(D, rec, I);
   const float4 a0 = *reinterpret_cast<const float4*>(rec + 64);
   const float4 a1 = *reinterpret_cast<const float4*>(rec + 68);
-  float s = a0.x * static_cast<float>(I[0]);
-  s = fmaf(a0.y, static_cast<float>(I[1]), s);
-  s = fmaf(a0.z, static_cast<float>(I[2]), s);
-  s = fmaf(a0.w, static_cast<float>(I[3]), s);
-  s = fmaf(a1.x, static_cast<float>(I[4]), s);
-  s = fmaf(a1.y, static_cast<float>(I[5]), s);
-  s = fmaf(a1.z, static_cast<float>(I[6]), s);
-  s = fmaf(a1.w, static_cast<float>(I[7]), s);
+  float s = a0.x * unbias(I[0]);
+  s = fmaf(a0.y, unbias(I[1]), s);
+  s = fmaf(a0.z, unbias(I[2]), s);
+  s = fmaf(a0.w, unbias(I[3]), s);
+  s = fmaf(a1.x, unbias(I[4]), s);
+  s = fmaf(a1.y, unbias(I[5]), s);
+  s = fmaf(a1.z, unbias(I[6]), s);
+  s = fmaf(a1.w, unbias(I[7]), s);
   return s * D.dw;
 }
 
@@ -351,7 +360,7 @@ __device__ __forceinline__ void fill_record_chunk(const uint8_t* src, uint32_t* 
     sum = __dp4a(static_cast<int>(q), 0x01010101, sum);
   }
   rec[64 + lane8] = __float_as_uint(__half2float(__ushort_as_half(static_cast<unsigned short>(ds & 0xFFFFu))));
-  rec[72 + lane8] = static_cast<uint32_t>(-sum);
+  rec[72 + lane8] = static_cast<uint32_t>(kFloatBias - sum);
 }
 
 }  // namespace tq1
