@@ -62,6 +62,10 @@ def library() -> ctypes.CDLL:
         lib.tq2_quantize_rows.argtypes = [P, P, I64, I64, P]
         lib.tq2_mmv.argtypes = [P, P, P, I64, I64, I64, P]
         lib.tq2_mmv_partials.argtypes = [P, P, P, I64, I64, I64, P]
+        lib.tq2_dequantize_rows.argtypes = [P, P, I64, I64, ctypes.c_int, P]
+        lib.tq2_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
+        lib.tq2_mmv_id_slots.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
+        lib.tq2_get_rows.argtypes = [P, P, I64, P, I64, I64, ctypes.c_int, P]
         lib.tq1_q8_1_bytes.restype = SZ
         lib.tq1_q8_1_bytes.argtypes = [I64, I64]
         lib.tq1_quantize_rows.argtypes = [P, P, I64, I64, P]
@@ -81,7 +85,8 @@ def library() -> ctypes.CDLL:
         for name in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_add", "tq1_mmv_f32",
                      "tq1_mmv_partials", "tq1_mmv_id", "tq1_mmv_id_slots", "tq1_mmv_id_noalloc",
                      "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status", "tq2_quantize_rows",
-                     "tq2_mmv", "tq2_mmv_partials"):
+                     "tq2_mmv", "tq2_mmv_partials", "tq2_dequantize_rows", "tq2_get_rows", "tq2_mmv_id",
+                     "tq2_mmv_id_slots"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -208,6 +213,30 @@ def tq2_mmv(blocks, q8, y, n: int, k: int, t: int, stream=None) -> None:
 def tq2_mmv_partials(blocks, q8, part, n: int, k: int, t: int, stream=None) -> None:
     _check(library().tq2_mmv_partials(_addr(blocks), _addr(q8), _addr(part), n, k, t, _stream(stream)),
            "tq2_mmv_partials")
+
+
+def tq2_mmv_id(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, t: int, top_k: int, ws,
+               ws_bytes: int | None = None, stream=None) -> None:
+    wsb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(library().tq2_mmv_id(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(y), n, k, t, top_k,
+                                _addr(ws), wsb, _stream(stream)), "tq2_mmv_id")
+
+
+def tq2_mmv_id_slots(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, t: int, top_k: int, ws,
+                     ws_bytes: int | None = None, stream=None) -> None:
+    wsb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(library().tq2_mmv_id_slots(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(y), n, k, t,
+                                      top_k, _addr(ws), wsb, _stream(stream)), "tq2_mmv_id_slots")
+
+
+def tq2_dequantize_rows(blocks, out, n: int, k: int, out_f16: bool = False, stream=None) -> None:
+    _check(library().tq2_dequantize_rows(_addr(blocks), _addr(out), n, k, int(out_f16), _stream(stream)),
+           "tq2_dequantize_rows")
+
+
+def tq2_get_rows(blocks, row_ids, n_ids: int, out, n: int, k: int, out_f16: bool = False, stream=None) -> None:
+    _check(library().tq2_get_rows(_addr(blocks), _addr(row_ids), n_ids, _addr(out), n, k, int(out_f16),
+                                  _stream(stream)), "tq2_get_rows")
 
 
 def tq1_sync_status(stream=None) -> int:

@@ -225,29 +225,39 @@ int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t 
   return mmv_common(blocks, q8, nullptr, part, n, k, t, stream);
 }
 
-int tq1_dequantize_rows(const void* blocks, void* out, int64_t n, int64_t k, int out_f16, void* stream) {
-  if (n < 0 || k <= 0 || (k % kQK) != 0) return TQ1_ERR_SHAPE;
-  if (n == 0) return TQ1_OK;
-  if (!blocks || !out) return TQ1_ERR_NULL;
-  if (misaligned(blocks) || misaligned(out)) return TQ1_ERR_ALIGN;
-  if (n > (int64_t{1} << 40) / k) return TQ1_ERR_UNSUPPORTED;
-  unsigned* st = status_ptr();
-  if (!st) return TQ1_ERR_CUDA;
-  return launch_dequant(static_cast<const uint8_t*>(blocks), nullptr, n, out, n, k, out_f16 != 0,
-                        static_cast<cudaStream_t>(stream), st);
-}
-
-int tq1_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n, int64_t k,
-                 int out_f16, void* stream) {
+static int dequant_common(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n,
+                          int64_t k, int out_f16, void* stream, int fmt) {
   if (n < 0 || n_ids < 0 || k <= 0 || (k % kQK) != 0) return TQ1_ERR_SHAPE;
   if (n_ids == 0) return TQ1_OK;
-  if (!blocks || !row_ids || !out) return TQ1_ERR_NULL;
-  if (misaligned(blocks) || misaligned(row_ids) || misaligned(out)) return TQ1_ERR_ALIGN;
+  if (!blocks || !out || (row_ids == nullptr && n_ids != n)) return TQ1_ERR_NULL;
+  if (misaligned(blocks) || misaligned(out) || (row_ids && misaligned(row_ids))) return TQ1_ERR_ALIGN;
   if (n_ids > (int64_t{1} << 40) / k) return TQ1_ERR_UNSUPPORTED;
   unsigned* st = status_ptr();
   if (!st) return TQ1_ERR_CUDA;
   return launch_dequant(static_cast<const uint8_t*>(blocks), row_ids, n_ids, out, n, k, out_f16 != 0,
-                        static_cast<cudaStream_t>(stream), st);
+                        static_cast<cudaStream_t>(stream), st, fmt);
+}
+
+int tq1_dequantize_rows(const void* blocks, void* out, int64_t n, int64_t k, int out_f16, void* stream) {
+  if (n < 0) return TQ1_ERR_SHAPE;
+  return dequant_common(blocks, nullptr, n, out, n, k, out_f16, stream, kFmtTq1);
+}
+
+int tq1_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n, int64_t k,
+                 int out_f16, void* stream) {
+  if (!row_ids && n_ids > 0 && n >= 0 && k > 0 && (k % kQK) == 0) return TQ1_ERR_NULL;
+  return dequant_common(blocks, row_ids, n_ids, out, n, k, out_f16, stream, kFmtTq1);
+}
+
+int tq2_dequantize_rows(const void* blocks, void* out, int64_t n, int64_t k, int out_f16, void* stream) {
+  if (n < 0) return TQ1_ERR_SHAPE;
+  return dequant_common(blocks, nullptr, n, out, n, k, out_f16, stream, kFmtTq2);
+}
+
+int tq2_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n, int64_t k,
+                 int out_f16, void* stream) {
+  if (!row_ids && n_ids > 0 && n >= 0 && k > 0 && (k % kQK) == 0) return TQ1_ERR_NULL;
+  return dequant_common(blocks, row_ids, n_ids, out, n, k, out_f16, stream, kFmtTq2);
 }
 
 size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k) {
@@ -260,7 +270,7 @@ size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k) {
 
 static int mmv_id_common(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
                          int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream,
-                         bool per_slot) {
+                         bool per_slot, int fmt = kFmtTq1) {
   int rc = check_mmv_shape(n, k, t);
   if (rc != TQ1_OK) return rc;
   if (n_experts <= 0 || top_k < 0) return TQ1_ERR_SHAPE;
@@ -279,17 +289,17 @@ static int mmv_id_common(const void* expert_blocks, int64_t n_experts, const voi
   const int act_div = per_slot ? 1 : static_cast<int>(top_k);
   MoePlan plan{};
   // A few pairs (decode): no routing table, each CTA reads its pair's id.
-  if (t * top_k <= kMoeDirectMaxPairs && moe_direct_plan(n, k, t * top_k, &plan))
-    return launch_moe_direct(w, a, ids, y, n, k, top_k, n_experts, t * top_k, plan, s, st, act_div);
-  const bool small = moe_small_plan(n, k, t * top_k, n_experts, &plan);
+  if (t * top_k <= kMoeDirectMaxPairs && moe_direct_plan(n, k, t * top_k, &plan, fmt))
+    return launch_moe_direct(w, a, ids, y, n, k, top_k, n_experts, t * top_k, plan, s, st, act_div, fmt);
+  const bool small = moe_small_plan(n, k, t * top_k, n_experts, &plan, fmt);
   rc = launch_moe_compact(ids, t, top_k, n_experts, small ? plan.chunk : 1, small ? plan.row_blocks : 1, table, s,
                           st);
   if (rc != TQ1_OK) return rc;
   if (small) {
-    rc = launch_moe_small(w, a, y, n, k, top_k, n_experts, t * top_k, plan, table, s, st, act_div);
+    rc = launch_moe_small(w, a, y, n, k, top_k, n_experts, t * top_k, plan, table, s, st, act_div, fmt);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
   }
-  return launch_mmv_id(w, n_experts, a, y, n, k, t, top_k, table, s, st, act_div);
+  return launch_mmv_id(w, n_experts, a, y, n, k, t, top_k, table, s, st, act_div, fmt);
 }
 
 extern "C" {
@@ -302,6 +312,16 @@ int tq1_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, con
 int tq1_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
                      int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream) {
   return mmv_id_common(expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, ws, ws_bytes, stream, true);
+}
+
+int tq2_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+               int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream) {
+  return mmv_id_common(expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, ws, ws_bytes, stream, false, kFmtTq2);
+}
+
+int tq2_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+                     int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream) {
+  return mmv_id_common(expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, ws, ws_bytes, stream, true, kFmtTq2);
 }
 
 int tq1_sync_status(void* stream) {

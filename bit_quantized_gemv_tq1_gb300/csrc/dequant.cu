@@ -13,6 +13,11 @@
 // ((uint8)(b*3^k)*3) >> 8.  Stores are 16-byte vectors, a warp writing one
 // contiguous 1 KiB (fp32) or 512 B (fp16) span: the kernel is bound by the
 // output bytes written to HBM.
+//
+// TQ2_0 blocks (2-bit codes, 66 bytes) take the same path: lane l's eight
+// elements lie in chunk c = l / 4, so they are field c % 4 of the eight
+// consecutive bytes qs[32 * (c / 4) + 8 * (l % 4) ..]; code 3 (never written
+// by the encoder) gives +2d, the fourth entry of the value table.
 #include <algorithm>
 
 #include "../../include/tq1.h"
@@ -32,7 +37,7 @@ __device__ __forceinline__ uint32_t digit_of(uint32_t b, uint32_t k) {
   return (((b * p) & 0xFFu) * 3u) >> 8;
 }
 
-template <bool F16>
+template <bool F16, int FMT>
 __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __restrict__ blocks,
                                                              const int32_t* __restrict__ row_ids, int64_t n_out,
                                                              void* __restrict__ out, int64_t n, int nb,
@@ -41,9 +46,14 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
   const int lane = threadIdx.x & 31;
   const int64_t units = n_out * nb;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * kDqWarps;
-  // Byte offset of this lane's first byte within the block, and its digit(s).
+  constexpr int kBB = fmt_block_bytes<FMT>();
+  // Byte offset of this lane's first byte within the block, and its digit(s)
+  // (TQ2_0: its 2-bit field).
   int boff, dig;
-  if (lane < 20) {
+  if (FMT == kFmtTq2) {
+    boff = 32 * (lane >> 4) + 8 * (lane & 3);
+    dig = (lane >> 2) & 3;
+  } else if (lane < 20) {
     boff = 8 * (lane & 3);
     dig = lane >> 2;
   } else if (lane < 30) {
@@ -75,17 +85,17 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
         }
       }
       if (live[x]) {
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(blocks + (srow * nb + bb[x]) * kBlockBytes);
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(blocks + (srow * nb + bb[x]) * kBB);
 #pragma unroll
         for (int i = 0; i < 4; ++i) hw[x][i] = __ldg(h + (boff >> 1) + i);
-        hw[x][4] = __ldg(h + 26);
+        hw[x][4] = __ldg(h + (kBB - 2) / 2);
       }
     }
 #pragma unroll
     for (int x = 0; x < kDqUnits; ++x) {
       if (!live[x]) continue;
       uint32_t by[8];
-      if (lane < 30) {
+      if (FMT == kFmtTq2 || lane < 30) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           by[2 * i] = hw[x][i] & 0xFFu;
@@ -101,14 +111,17 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
       uint32_t dg[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        dg[i] = digit_of(by[i], lane < 30 ? static_cast<uint32_t>(dig) : static_cast<uint32_t>(dig + (i >> 2)));
+        dg[i] = FMT == kFmtTq2 ? (by[i] >> (2 * dig)) & 3u
+                               : digit_of(by[i], lane < 30 ? static_cast<uint32_t>(dig) : static_cast<uint32_t>(dig + (i >> 2)));
       const int64_t e0 = orow[x] * static_cast<int64_t>(nb) * kQK + static_cast<int64_t>(bb[x]) * kQK + 8 * lane;
       const uint32_t h16 = hw[x][4];
       if (F16) {
-        // fp16 values by byte permute from the table {-d, 0, +d}: a digit
-        // pair (a, b) selects bytes 2a, 2a+1, 2b, 2b+1 (selector
-        // 34 * (a + 256 b) + 0x1010).
-        const uint32_t tlo = h16 ^ 0x8000u, thi = h16;
+        // fp16 values by byte permute from the table {-d, 0, +d, +2d}: a
+        // digit pair (a, b) selects bytes 2a, 2a+1, 2b, 2b+1 (selector
+        // 34 * (a + 256 b) + 0x1010).  TQ1_0 digits never reach the fourth.
+        const uint32_t d2 = __half_as_ushort(__float2half_rn(2.0f * __half2float(__ushort_as_half(
+                                static_cast<unsigned short>(h16)))));
+        const uint32_t tlo = h16 ^ 0x8000u, thi = h16 | (d2 << 16);
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = __byte_perm(tlo, thi, (dg[2 * i] | (dg[2 * i + 1] << 8)) * 34u + 0x1010u);
@@ -117,7 +130,8 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
         const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(h16)));
         float v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = dg[i] == 1u ? 0.0f : (dg[i] == 2u ? dw : -dw);  // exact
+        for (int i = 0; i < 8; ++i)
+          v[i] = dg[i] == 1u ? 0.0f : (dg[i] == 2u ? dw : (dg[i] == 3u ? 2.0f * dw : -dw));  // exact
         float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + e0);
         __stcs(o, make_float4(v[0], v[1], v[2], v[3]));
         __stcs(o + 1, make_float4(v[4], v[5], v[6], v[7]));
@@ -129,7 +143,7 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
 }  // namespace
 
 int launch_dequant(const uint8_t* blocks, const int32_t* row_ids, int64_t n_out, void* out, int64_t n, int64_t k,
-                   bool f16, cudaStream_t s, unsigned* status) {
+                   bool f16, cudaStream_t s, unsigned* status, int fmt) {
   const DeviceInfo& di = device_info();
   const int nb = static_cast<int>(k / kQK);
   const int64_t warps = n_out * nb;
@@ -144,8 +158,13 @@ int launch_dequant(const uint8_t* blocks, const int32_t* row_ids, int64_t n_out,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = f16 ? cudaLaunchKernelEx(&cfg, dequant_kernel<true>, blocks, row_ids, n_out, out, n, nb, status)
-                            : cudaLaunchKernelEx(&cfg, dequant_kernel<false>, blocks, row_ids, n_out, out, n, nb, status);
+  cudaError_t e;
+  if (fmt == kFmtTq2)
+    e = f16 ? cudaLaunchKernelEx(&cfg, dequant_kernel<true, kFmtTq2>, blocks, row_ids, n_out, out, n, nb, status)
+            : cudaLaunchKernelEx(&cfg, dequant_kernel<false, kFmtTq2>, blocks, row_ids, n_out, out, n, nb, status);
+  else
+    e = f16 ? cudaLaunchKernelEx(&cfg, dequant_kernel<true, kFmtTq1>, blocks, row_ids, n_out, out, n, nb, status)
+            : cudaLaunchKernelEx(&cfg, dequant_kernel<false, kFmtTq1>, blocks, row_ids, n_out, out, n, nb, status);
   return cuda_ok(e) ? TQ1_OK : TQ1_ERR_CUDA;
 }
 

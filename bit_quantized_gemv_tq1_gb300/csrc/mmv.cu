@@ -485,7 +485,8 @@ int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int
 }
 
 int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float* y, int64_t n, int64_t k,
-                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status, int act_div) {
+                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status, int act_div,
+                  int fmt) {
   const DeviceInfo& di = device_info();
   MmvArgs a = {};
   a.act_div = act_div;
@@ -505,7 +506,8 @@ int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float*
   if (cc < 1) return TQ1_ERR_UNSUPPORTED;
   a.cc = static_cast<int>(cc);
   a.rt = static_cast<int>(kAccBudget / (4 * 32));
-  return launch_rung<32, kModeMoe, kFmtTq1>(a, di.num_sms, s);
+  return fmt == kFmtTq2 ? launch_rung<32, kModeMoe, kFmtTq2>(a, di.num_sms, s)
+                        : launch_rung<32, kModeMoe, kFmtTq1>(a, di.num_sms, s);
 }
 
 }  // namespace tq1

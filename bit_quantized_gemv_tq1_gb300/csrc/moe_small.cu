@@ -52,10 +52,12 @@ struct MoeArgs {
 
 }  // namespace
 
+template <int FMT>
 __global__ void __launch_bounds__(kMThreads, 2) moe_small_kernel(const MoeArgs a) {
+  constexpr int kBB = fmt_block_bytes<FMT>();
   extern __shared__ __align__(128) uint8_t smem[];
   const int nb = a.nb, nkc = a.nkc;
-  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBlockBytes;
+  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBB;
   const uint32_t gstride = group_stride(rowbytes);
   uint8_t* slab = smem;
   uint32_t* recs = reinterpret_cast<uint32_t*>(smem + a.slab_bytes);
@@ -156,8 +158,8 @@ __global__ void __launch_bounds__(kMThreads, 2) moe_small_kernel(const MoeArgs a
       if (row < rows && b < nb) {
         Packed P;
         const uint32_t off = static_cast<uint32_t>(g) * gstride + ((wlow + static_cast<uint32_t>(g) * kRowsPerTask * rowbytes) & 15u) +
-                             static_cast<uint32_t>(r) * rowbytes + static_cast<uint32_t>(b) * kBlockBytes;
-        expand_pack(slab, off, P);
+                             static_cast<uint32_t>(r) * rowbytes + static_cast<uint32_t>(b) * kBB;
+        unit_pack<FMT>(slab, off, P);
 #pragma unroll
         for (int c = 0; c < kChunk; ++c)
           if (c < pc) acc[c] = packed_dot(P, recs + c * rstride + b * kPRec);
@@ -225,10 +227,12 @@ struct DirectArgs {
   uint32_t slab_bytes;
 };
 
+template <int FMT>
 __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectArgs a) {
+  constexpr int kBB = fmt_block_bytes<FMT>();
   extern __shared__ __align__(128) uint8_t smem[];
   const int nb = a.nb, nkc = a.nkc;
-  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBlockBytes;
+  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBB;
   const uint32_t gstride = group_stride(rowbytes);
   uint8_t* slab = smem;
   uint32_t* recs = reinterpret_cast<uint32_t*>(smem + a.slab_bytes);
@@ -291,8 +295,8 @@ __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectAr
       Packed P;
       const uint32_t off = static_cast<uint32_t>(g) * gstride +
                            ((wlow + static_cast<uint32_t>(g) * kRowsPerTask * rowbytes) & 15u) +
-                           static_cast<uint32_t>(r) * rowbytes + static_cast<uint32_t>(b) * kBlockBytes;
-      expand_pack(slab, off, P);
+                           static_cast<uint32_t>(r) * rowbytes + static_cast<uint32_t>(b) * kBB;
+      unit_pack<FMT>(slab, off, P);
       v = packed_dot(P, recs + b * kPRec);
     }
     v += __shfl_xor_sync(0xffffffffu, v, 1);
@@ -322,11 +326,11 @@ __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectAr
 
 // Rows per CTA so that pairs x row blocks is about one CTA per SM, within the
 // shared-memory budget; false if even four rows do not fit.
-bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan) {
+bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan, int fmt) {
   const DeviceInfo& di = device_info();
   const int nb = static_cast<int>(k / kQK);
   const int nkc = (nb + kLanesPerRow - 1) / kLanesPerRow;
-  const uint32_t gs = group_stride(static_cast<uint32_t>(nb) * kBlockBytes);
+  const uint32_t gs = group_stride(static_cast<uint32_t>(nb) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes));
   int64_t rows = (n * pairs + di.num_sms - 1) / std::max(1, di.num_sms);
   rows = ((std::max<int64_t>(rows, kRowsPerTask) + kRowsPerTask - 1) / kRowsPerTask) * kRowsPerTask;
   rows = std::min<int64_t>(rows, kDMaxRows);
@@ -344,7 +348,7 @@ bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan) {
 
 int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
                       int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
-                      unsigned* status, int act_div) {
+                      unsigned* status, int act_div, int fmt) {
   const DeviceInfo& di = device_info();
   DirectArgs a = {};
   a.act_div = act_div;
@@ -360,16 +364,17 @@ int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, f
   a.nkc = (a.nb + kLanesPerRow - 1) / kLanesPerRow;
   a.rows = plan.rows;
   a.row_blocks = plan.row_blocks;
-  const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * kBlockBytes;
+  const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes);
   a.slab_bytes = static_cast<uint32_t>(plan.rows / kRowsPerTask) * group_stride(rowbytes);
   const size_t smem = a.slab_bytes + static_cast<size_t>(a.nb) * kPRec * 4 + static_cast<size_t>(plan.rows) * a.nkc * 4;
-  static bool configured[64] = {};
+  auto kern = fmt == kFmtTq2 ? moe_direct_kernel<kFmtTq2> : moe_direct_kernel<kFmtTq1>;
+  static bool configured[2][64] = {};
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
-  if (!configured[di.device]) {
-    if (!cuda_ok(cudaFuncSetAttribute(moe_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!configured[fmt == kFmtTq2][di.device]) {
+    if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kDSmemBudget))))
       return TQ1_ERR_CUDA;
-    configured[di.device] = true;
+    configured[fmt == kFmtTq2][di.device] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pairs * plan.row_blocks));
@@ -381,17 +386,17 @@ int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, f
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&cfg, moe_direct_kernel, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, kern, a)) ? TQ1_OK : TQ1_ERR_CUDA;
 }
 
 // Rows per task and row blocks per expert: enough tasks for about two per
 // CTA slot when every routed pair lands on its own expert, within the shared
 // memory budget (two CTAs per SM).
-bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoePlan* plan) {
+bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoePlan* plan, int fmt) {
   const DeviceInfo& di = device_info();
   const int nb = static_cast<int>(k / kQK);
   const int nkc = (nb + kLanesPerRow - 1) / kLanesPerRow;
-  const uint32_t rowbytes = static_cast<uint32_t>(nb) * kBlockBytes;
+  const uint32_t rowbytes = static_cast<uint32_t>(nb) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes);
   const int64_t chunks = std::min<int64_t>(pairs, n_experts + pairs / kChunk);
   const int64_t want_tasks = 2 * static_cast<int64_t>(std::max(1, di.num_sms));
   int64_t rows = (n * std::max<int64_t>(chunks, 1) + want_tasks - 1) / want_tasks;
@@ -411,7 +416,7 @@ bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoeP
 
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
-                     unsigned* status, int act_div) {
+                     unsigned* status, int act_div, int fmt) {
   const DeviceInfo& di = device_info();
   MoeArgs a = {};
   a.act_div = act_div;
@@ -428,17 +433,18 @@ int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.rows = plan.rows;
   a.row_blocks = plan.row_blocks;
   a.pairs = pairs;
-  const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * kBlockBytes;
+  const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes);
   a.slab_bytes = static_cast<uint32_t>(plan.rows / kRowsPerTask) * group_stride(rowbytes);
   const size_t smem = a.slab_bytes + static_cast<size_t>(kChunk) * a.nb * kPRec * 4 +
                       static_cast<size_t>(plan.rows) * a.nkc * kChunk * 4;
-  static bool configured[64] = {};
+  auto kern = fmt == kFmtTq2 ? moe_small_kernel<kFmtTq2> : moe_small_kernel<kFmtTq1>;
+  static bool configured[2][64] = {};
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
-  if (!configured[di.device]) {
-    if (!cuda_ok(cudaFuncSetAttribute(moe_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!configured[fmt == kFmtTq2][di.device]) {
+    if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kMoeSmemBudget))))
       return TQ1_ERR_CUDA;
-    configured[di.device] = true;
+    configured[fmt == kFmtTq2][di.device] = true;
   }
   // Upper bound on the tasks: every pair on its own expert.
   const int64_t max_tasks = std::min<int64_t>(pairs, n_experts) * plan.row_blocks +
@@ -454,7 +460,7 @@ int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&cfg, moe_small_kernel, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, kern, a)) ? TQ1_OK : TQ1_ERR_CUDA;
 }
 
 }  // namespace tq1

@@ -44,7 +44,8 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
 // `act_div`: the activation row of routed pair p is p / act_div (top_k: one
 // row per token shared by its slots; 1: one row per (token, slot)).
 int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float* y, int64_t n, int64_t k,
-                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status, int act_div);
+                  int64_t t, int64_t top_k, const int32_t* ws, cudaStream_t s, unsigned* status, int act_div,
+                  int fmt = 0);
 
 // y[c][r] for any t on the tensor cores (tcgen05): 128-row tiles, split-K
 // over a thread-block cluster when the tiles alone cannot fill the GPU.
@@ -52,10 +53,10 @@ int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float*
 int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
                 unsigned* status, const float* res = nullptr, int fmt = 0);
 
-// Rows of TQ1_0 blocks to fp32 (f16 = false) or fp16 values: out row i is
-// source row row_ids[i] (row_ids == nullptr: row i).
+// Rows of TQ1_0 (fmt kFmtTq1) or TQ2_0 blocks to fp32 (f16 = false) or fp16
+// values: out row i is source row row_ids[i] (row_ids == nullptr: row i).
 int launch_dequant(const uint8_t* blocks, const int32_t* row_ids, int64_t n_out, void* out, int64_t n, int64_t k,
-                   bool f16, cudaStream_t s, unsigned* status);
+                   bool f16, cudaStream_t s, unsigned* status, int fmt = 0);
 
 // Workspace layout of the routing table (int32 words):
 //   [0]                   n_active
@@ -82,17 +83,17 @@ int launch_moe_compact(const int32_t* ids, int64_t t, int64_t top_k, int64_t n_e
 struct MoePlan {
   int chunk, rows, row_blocks;
 };
-bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoePlan* plan);
+bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoePlan* plan, int fmt = 0);
 
 // Expert-routed mat-vec without a routing table, for few pairs: one CTA per
 // (pair, row range) reads its expert id itself.  `plan` gives the rows per
 // CTA and the row ranges per pair.
-bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan);
+bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan, int fmt = 0);
 int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
                       int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
-                      unsigned* status, int act_div);
+                      unsigned* status, int act_div, int fmt = 0);
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
-                     unsigned* status, int act_div);
+                     unsigned* status, int act_div, int fmt = 0);
 
 }  // namespace tq1

@@ -271,6 +271,30 @@ int tq2_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, 
 int tq2_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,
                      void* stream);
 
+/*
+ * TQ2_0 rows to fp32 (out_f16 == 0) or fp16 values, d * (code - 1) exactly:
+ * the whole matrix (tq2_dequantize_rows) or the rows listed in row_ids
+ * (tq2_get_rows).  Arguments, layouts, errors and the handling of
+ * out-of-range ids as tq1_dequantize_rows / tq1_get_rows.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Upstream state" (the TQ2_0
+ * sibling format) and "Current behavior" (the dequantise walk of a block).
+ */
+/*
+ * Expert-routed mat-vec over TQ2_0 experts (each expert [n][k/256] x 66
+ * bytes, back to back): the same routing, workspace
+ * (tq1_mmv_id_workspace_size), kernels, layouts and errors as tq1_mmv_id
+ * (one activation row per token) and tq1_mmv_id_slots (one per token and
+ * slot).
+ */
+int tq2_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+               int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
+int tq2_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
+                     int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
+
+int tq2_dequantize_rows(const void* blocks, void* out, int64_t n, int64_t k, int out_f16, void* stream);
+int tq2_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n, int64_t k,
+                 int out_f16, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -78,6 +78,7 @@ def _load():
         lib.orc_tq2_mmv_partials.argtypes = [P, P, P, I64, I64, I64]
         lib.orc_tq2_mmv_f64.argtypes = [P, P, P, I64, I64, I64]
         lib.orc_tq2_mmv_f64_rows.argtypes = [P, P, P, I64, I64, I64, P, I64]
+        lib.orc_tq2_mmv_id_f64.argtypes = [P, I64, P, P, P, I64, I64, I64, I64]
         lib.orc_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -258,4 +259,20 @@ def tq2_mmv_f64_rows(blocks: np.ndarray, q8: np.ndarray, n: int, k: int, t: int,
     out = np.zeros((t, rows.size), dtype=np.float64)
     _load().orc_tq2_mmv_f64_rows(_ptr(np.ascontiguousarray(blocks)), _ptr(np.ascontiguousarray(q8)), _ptr(out),
                                  n, k, t, _ptr(rows), rows.size)
+    return out
+
+
+def tq2_dequantize_rows(blocks: np.ndarray, n: int, k: int) -> np.ndarray:
+    """Values TQ2_0 blocks encode, fp32 [n][k]: (code - 1) * d per element
+    (the oracle decode scaled by its block's fp16 scale; exact in fp32)."""
+    trits, scales = tq2_decode_rows(blocks, n, k)
+    return (trits.astype(np.float32).reshape(n, k // QK, QK) * scales[:, :, None]).reshape(n, k)
+
+
+def tq2_mmv_id_f64(expert_blocks: np.ndarray, n_experts: int, q8: np.ndarray, ids: np.ndarray,
+                   n: int, k: int, t: int, top_k: int, fill: float = np.nan) -> np.ndarray:
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    out = np.full((t, top_k, n), fill, dtype=np.float64)
+    _load().orc_tq2_mmv_id_f64(_ptr(np.ascontiguousarray(expert_blocks)), n_experts, _ptr(np.ascontiguousarray(q8)),
+                               _ptr(ids), _ptr(out), n, k, t, top_k)
     return out

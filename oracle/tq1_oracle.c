@@ -398,41 +398,44 @@ void orc_tq2_mmv_f64_rows(const uint8_t* blocks, const uint8_t* q8, double* y, i
   orc_f64_rows_fmt(2, blocks, q8, y, k, t, rows, nrows);
 }
 
-/* R5: y[c][s][r] = expert ids[c][s] (matrix at expert_blocks + e*n*nb*54)
- * against token c's activations. */
-void orc_mmv_id_f64(const uint8_t* expert_blocks, int64_t n_experts, const uint8_t* q8, const int32_t* ids,
-                    double* y, int64_t n, int64_t k, int64_t t, int64_t top_k) {
-  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8;
-  const int64_t ebytes = n * nb * ORC_BLOCK_BYTES;
+/* R5: y[c][s][r] = expert ids[c][s] (matrix at expert_blocks + e*n*nb*bytes)
+ * against token c's activations; only the listed rows (all rows when rows is
+ * NULL: y[c][s][r], else y[c][s][i] for row rows[i]). */
+static void orc_mmv_id_fmt(int fmt, const uint8_t* expert_blocks, int64_t n_experts, const uint8_t* q8,
+                           const int32_t* ids, double* y, int64_t n, int64_t k, int64_t t, int64_t top_k,
+                           const int64_t* rows, int64_t nrows) {
+  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8, bb = orc_fmt_bytes(fmt);
+  const int64_t ebytes = n * nb * bb;
+  const int64_t m = rows ? nrows : n;
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t c = 0; c < t; ++c) {
     for (int64_t s = 0; s < top_k; ++s) {
       const int32_t e = ids[c * top_k + s];
       if (e < 0 || e >= n_experts) continue;
-      for (int64_t r = 0; r < n; ++r)
-        y[(c * top_k + s) * n + r] =
-            orc_row_dot(1, expert_blocks + e * ebytes + r * nb * ORC_BLOCK_BYTES, q8 + c * nq * ORC_Q8_BYTES, nb);
+      for (int64_t i = 0; i < m; ++i) {
+        const int64_t r = rows ? rows[i] : i;
+        y[(c * top_k + s) * m + i] =
+            orc_row_dot(fmt, expert_blocks + e * ebytes + r * nb * bb, q8 + c * nq * ORC_Q8_BYTES, nb);
+      }
     }
   }
+}
+
+void orc_mmv_id_f64(const uint8_t* expert_blocks, int64_t n_experts, const uint8_t* q8, const int32_t* ids,
+                    double* y, int64_t n, int64_t k, int64_t t, int64_t top_k) {
+  orc_mmv_id_fmt(1, expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, NULL, 0);
 }
 
 /* Sampled variant of mat-vec-id: only the listed rows of every slot. */
 void orc_mmv_id_f64_rows(const uint8_t* expert_blocks, int64_t n_experts, const uint8_t* q8, const int32_t* ids,
                          double* y, int64_t n, int64_t k, int64_t t, int64_t top_k, const int64_t* rows,
                          int64_t nrows) {
-  const int64_t nb = k / ORC_QK, nq = k / ORC_QK8;
-  const int64_t ebytes = n * nb * ORC_BLOCK_BYTES;
-#pragma omp parallel for collapse(2) schedule(static)
-  for (int64_t c = 0; c < t; ++c) {
-    for (int64_t s = 0; s < top_k; ++s) {
-      const int32_t e = ids[c * top_k + s];
-      if (e < 0 || e >= n_experts) continue;
-      for (int64_t i = 0; i < nrows; ++i)
-        y[(c * top_k + s) * nrows + i] =
-            orc_row_dot(1, expert_blocks + e * ebytes + rows[i] * nb * ORC_BLOCK_BYTES, q8 + c * nq * ORC_Q8_BYTES,
-                        nb);
-    }
-  }
+  orc_mmv_id_fmt(1, expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, rows, nrows);
+}
+
+void orc_tq2_mmv_id_f64(const uint8_t* expert_blocks, int64_t n_experts, const uint8_t* q8, const int32_t* ids,
+                        double* y, int64_t n, int64_t k, int64_t t, int64_t top_k) {
+  orc_mmv_id_fmt(2, expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, NULL, 0);
 }
 
 int orc_num_threads(void) {

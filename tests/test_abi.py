@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_id", "tq1_mmv_partials",
                  "tq1_mmv_id_workspace_size", "tq1_sync_status", "tq1_status_string", "tq1_dequantize_rows",
-                 "tq1_get_rows", "tq2_quantize_rows", "tq2_mmv", "tq2_mmv_partials", "tq2_blocks_bytes"):
+                 "tq1_get_rows", "tq2_quantize_rows", "tq2_mmv", "tq2_mmv_partials", "tq2_blocks_bytes", "tq2_dequantize_rows", "tq2_get_rows", "tq2_mmv_id",
+                 "tq2_mmv_id_slots"):
         assert want in names
 
 
@@ -122,3 +123,23 @@ def test_tq2_host_checks(lib):
     assert lib.tq2_mmv(FAKE, FAKE, FAKE, 10, 256 * 246, 1, None) == -4
     assert lib.tq2_mmv(None, None, None, 0, 256, 3, None) == 0
     assert lib.tq2_mmv_partials(FAKE, FAKE, None, 4, 256, 1, None) == -1
+
+
+def test_tq2_dequant_host_checks(lib):
+    assert lib.tq2_dequantize_rows(FAKE, FAKE, 4, 100, 0, None) == -2
+    assert lib.tq2_dequantize_rows(None, FAKE, 4, 256, 0, None) == -1
+    assert lib.tq2_dequantize_rows(FAKE, FAKE + 8, 4, 256, 1, None) == -3
+    assert lib.tq2_dequantize_rows(None, None, 0, 256, 0, None) == 0
+    assert lib.tq2_get_rows(FAKE, None, 3, FAKE, 4, 256, 0, None) == -1
+    assert lib.tq2_get_rows(FAKE, FAKE, -1, FAKE, 4, 256, 0, None) == -2
+    assert lib.tq2_get_rows(FAKE, FAKE + 4, 3, FAKE, 4, 256, 0, None) == -3
+    assert lib.tq2_get_rows(None, None, 0, None, 4, 256, 0, None) == 0
+
+
+def test_tq2_mmv_id_host_checks(lib):
+    ws = L.tq1_mmv_id_workspace_size(8, 2, 2)
+    assert lib.tq2_mmv_id(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 2, 2, FAKE, ws - 1, None) == -5
+    assert lib.tq2_mmv_id(FAKE, 0, FAKE, FAKE, FAKE, 16, 256, 2, 2, FAKE, ws, None) == -2
+    assert lib.tq2_mmv_id(FAKE, 8, FAKE, None, FAKE, 16, 256, 2, 2, FAKE, ws, None) == -1
+    assert lib.tq2_mmv_id_slots(FAKE, 8, FAKE, FAKE, FAKE, 16, 300, 2, 2, FAKE, ws, None) == -2
+    assert lib.tq2_mmv_id_slots(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 0, 2, FAKE, ws, None) == 0

@@ -147,3 +147,72 @@ def test_per_slot_activations(t, top_k, n_experts):
             e = int(m.ids[c, s])
             ref[c, s] = orc.mmv_f64(ob[e], oq[c * top_k + s], m.n, m.k, 1)[0]
     G.assert_close(G.host(y), ref)
+
+
+# ------------------------------------------------------------------ TQ2_0 --
+def _experts_gpu_tq2(m):
+    t = G.torch()
+    eb = m.n * (m.k // 256) * 66
+    blocks = t.empty(m.n_experts * eb, dtype=t.uint8, device="cuda")
+    for e in range(m.n_experts):
+        w = G.dev(m.expert_weights(e).astype(np.float32))
+        G.lib().tq2_quantize_rows(w, blocks[e * eb:(e + 1) * eb], m.n, m.k)
+    return blocks
+
+
+def _oracle_blocks_tq2(m, experts):
+    eb = m.n * (m.k // 256) * 66
+    out = np.zeros((m.n_experts, eb), np.uint8)
+    for e in experts:
+        out[e] = orc.tq2_encode_rows(m.expert_weights(e)).reshape(-1)
+    return out
+
+
+def _tq2_id(blocks, m, ids, q8, slots=False, t=None):
+    L, torch = G.lib(), G.torch()
+    t = m.t if t is None else t
+    ws_bytes = L.tq1_mmv_id_workspace_size(m.n_experts, t, m.top_k)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    y = torch.full((t, m.top_k, m.n), float("nan"), dtype=torch.float32, device="cuda")
+    fn = L.tq2_mmv_id_slots if slots else L.tq2_mmv_id
+    fn(blocks, m.n_experts, q8, G.dev(ids.astype(np.int32)), y, m.n, m.k, t, m.top_k, ws)
+    assert L.tq1_sync_status() == 0
+    return G.host(y)
+
+
+@pytest.mark.parametrize("t", [1, 32])
+def test_tq2_config4_sampled_rows(t):
+    # Direct mode (t = 1: 8 pairs) and the compacted path (t = 32: 256 pairs).
+    m = synth.config_moe(t)
+    y = _tq2_id(_experts_gpu_tq2(m), m, m.ids, G.quantize_acts(m.x))
+    ob = _oracle_blocks_tq2(m, np.unique(m.ids))
+    ref = orc.tq2_mmv_id_f64(ob, m.n_experts, orc.q8_1_quantize(m.x), m.ids, m.n, m.k, m.t, m.top_k)
+    G.assert_close(y, ref)
+
+
+def test_tq2_routings_long_rows():
+    # Repeated, unused and all-expert routings with long rows (k = 256 * 63,
+    # 4158 bytes per TQ2_0 row).
+    for ids in (ROUTINGS["repeated_and_unused"], ROUTINGS["every_expert"]):
+        ids = ids.astype(np.int32)
+        t, top_k = ids.shape
+        m = synth.moe(7, 40, 256 * 63, t, top_k, seed=43)
+        m.ids = ids
+        y = _tq2_id(_experts_gpu_tq2(m), m, ids, G.quantize_acts(m.x))
+        ref = orc.tq2_mmv_id_f64(_oracle_blocks_tq2(m, range(7)), 7, orc.q8_1_quantize(m.x), ids, m.n, m.k, t, top_k)
+        G.assert_close(y, ref)
+
+
+@pytest.mark.parametrize("t,top_k,n_experts", [(1, 8, 16), (40, 2, 5)])
+def test_tq2_per_slot_activations(t, top_k, n_experts):
+    m = synth.moe(n_experts, 160, 1024, t, top_k, seed=19 + t)
+    x = np.random.default_rng(t + 5).standard_normal((t * top_k, m.k)).astype(np.float32)
+    y = _tq2_id(_experts_gpu_tq2(m), m, m.ids, G.quantize_acts(x), slots=True)
+    ob = _oracle_blocks_tq2(m, np.unique(m.ids))
+    oq = orc.q8_1_quantize(x).reshape(t * top_k, -1)
+    ref = np.zeros((t, top_k, m.n))
+    for c in range(t):
+        for s in range(top_k):
+            e = int(m.ids[c, s])
+            ref[c, s] = orc.tq2_mmv_f64(ob[e], oq[c * top_k + s], m.n, m.k, 1)[0]
+    G.assert_close(y, ref)

@@ -98,3 +98,29 @@ def test_unused_code_decodes_to_plus_two():
     q8 = orc.q8_1_quantize(x)  # q = 127 everywhere, d = 1/127
     part = orc.tq2_mmv_partials(blk, q8, 1, 256, 1)
     assert part[0, 0, 0] == 127 * (2 - 31) and np.all(part[0, 0, 1:] == -127 * 32)
+
+
+def test_dequantize_is_trits_times_scales():
+    p = synth.matvec(6, 768, 1, p_zero=0.4, seed=8)
+    got = orc.tq2_dequantize_rows(orc.tq2_encode_rows(p.w), 6, 768)
+    want = p.trits.astype(np.float32) * np.repeat(p.scales.astype(np.float32), 256, axis=1)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(got, p.w)  # the synthetic weights round-trip exactly
+
+
+def test_mmv_id_cross_format():
+    # Expert-routed mat-vec: the same experts encoded as TQ1_0 and TQ2_0 give
+    # bit-identical fp64 outputs (reading R5 of the oracle for the routing).
+    E, n, k, t, top_k = 5, 12, 512, 3, 2
+    p = synth.matvec(E * n, k, t, p_zero=0.4, seed=77)
+    ids = np.array([[0, 4], [2, 2], [1, 3]], dtype=np.int32)
+    q8 = orc.q8_1_quantize(p.x)
+    y1 = orc.mmv_id_f64(orc.tq1_encode_rows(p.w), E, q8, ids, n, k, t, top_k)
+    y2 = orc.tq2_mmv_id_f64(orc.tq2_encode_rows(p.w), E, q8, ids, n, k, t, top_k)
+    np.testing.assert_array_equal(y1, y2)
+    # and slot (c, s) is the dense mat-vec of expert ids[c, s] against token c
+    dense = orc.tq2_mmv_f64(orc.tq2_encode_rows(p.w), q8, E * n, k, t)
+    for c in range(t):
+        for s in range(top_k):
+            e = ids[c, s]
+            np.testing.assert_array_equal(y2[c, s], dense[c, e * n:(e + 1) * n])
