@@ -9,7 +9,7 @@ _EXPORTS = (
     "tq1_mmv_id", "tq1_mmv_id_slots", "tq1_mmv_id_noalloc", "tq1_mmv_id_workspace_size", "tq1_dequantize_rows",
     "tq1_get_rows", "tq1_sync_status", "tq1_blocks_bytes", "tq1_q8_1_bytes", "tq2_quantize_rows", "tq2_mmv",
     "tq2_mmv_partials", "tq2_blocks_bytes", "tq2_dequantize_rows", "tq2_get_rows", "tq2_mmv_id",
-    "tq2_mmv_id_slots", "Tq1Error", "library", "library_path", "STATUS",
+    "tq2_mmv_id_slots", "tq2_mmv_f32", "tq2_mmv_add", "Tq1Error", "library", "library_path", "STATUS",
 )
 __all__ = list(_EXPORTS)
 

@@ -63,6 +63,8 @@ def library() -> ctypes.CDLL:
         lib.tq2_mmv.argtypes = [P, P, P, I64, I64, I64, P]
         lib.tq2_mmv_partials.argtypes = [P, P, P, I64, I64, I64, P]
         lib.tq2_dequantize_rows.argtypes = [P, P, I64, I64, ctypes.c_int, P]
+        lib.tq2_mmv_f32.argtypes = [P, P, P, I64, I64, I64, P]
+        lib.tq2_mmv_add.argtypes = [P, P, P, P, I64, I64, I64, P]
         lib.tq2_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq2_mmv_id_slots.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq2_get_rows.argtypes = [P, P, I64, P, I64, I64, ctypes.c_int, P]
@@ -86,7 +88,7 @@ def library() -> ctypes.CDLL:
                      "tq1_mmv_partials", "tq1_mmv_id", "tq1_mmv_id_slots", "tq1_mmv_id_noalloc",
                      "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status", "tq2_quantize_rows",
                      "tq2_mmv", "tq2_mmv_partials", "tq2_dequantize_rows", "tq2_get_rows", "tq2_mmv_id",
-                     "tq2_mmv_id_slots"):
+                     "tq2_mmv_id_slots", "tq2_mmv_f32", "tq2_mmv_add"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -208,6 +210,15 @@ def tq2_quantize_rows(w, blocks, n: int, k: int, stream=None) -> None:
 
 def tq2_mmv(blocks, q8, y, n: int, k: int, t: int, stream=None) -> None:
     _check(library().tq2_mmv(_addr(blocks), _addr(q8), _addr(y), n, k, t, _stream(stream)), "tq2_mmv")
+
+
+def tq2_mmv_f32(blocks, x, y, n: int, k: int, t: int, stream=None) -> None:
+    _check(library().tq2_mmv_f32(_addr(blocks), _addr(x), _addr(y), n, k, t, _stream(stream)), "tq2_mmv_f32")
+
+
+def tq2_mmv_add(blocks, q8, res, y, n: int, k: int, t: int, stream=None) -> None:
+    _check(library().tq2_mmv_add(_addr(blocks), _addr(q8), _addr(res), _addr(y), n, k, t, _stream(stream)),
+           "tq2_mmv_add")
 
 
 def tq2_mmv_partials(blocks, q8, part, n: int, k: int, t: int, stream=None) -> None:

@@ -200,7 +200,8 @@ int tq2_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t 
   return mmv_common(blocks, q8, nullptr, part, n, k, t, stream, nullptr, kFmtTq2);
 }
 
-int tq1_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t, void* stream) {
+static int mmv_f32_common(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t,
+                          void* stream, int fmt) {
   int rc = check_mmv_shape(n, k, t);
   if (rc != TQ1_OK) return rc;
   if (n == 0 || t == 0) return TQ1_OK;
@@ -210,13 +211,27 @@ int tq1_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t
   unsigned* st = status_ptr();
   if (!st) return TQ1_ERR_CUDA;
   return launch_mmv_small(static_cast<const uint8_t*>(blocks), nullptr, y, n, k, t, static_cast<cudaStream_t>(stream),
-                          st, nullptr, x);
+                          st, nullptr, x, fmt);
+}
+
+int tq1_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t, void* stream) {
+  return mmv_f32_common(blocks, x, y, n, k, t, stream, kFmtTq1);
+}
+
+int tq2_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t, void* stream) {
+  return mmv_f32_common(blocks, x, y, n, k, t, stream, kFmtTq2);
 }
 
 int tq1_mmv_add(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
                 void* stream) {
   if (!res && n > 0 && t > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;
   return mmv_common(blocks, q8, y, nullptr, n, k, t, stream, res);
+}
+
+int tq2_mmv_add(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
+                void* stream) {
+  if (!res && n > 0 && t > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;
+  return mmv_common(blocks, q8, y, nullptr, n, k, t, stream, res, kFmtTq2);
 }
 
 int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,

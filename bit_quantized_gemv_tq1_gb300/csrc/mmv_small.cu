@@ -368,12 +368,17 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.nkc_magic = a.nkc > 1 ? static_cast<uint32_t>(((uint64_t{1} << 32) + a.nkc - 1) / a.nkc) : 0u;
   if (static_cast<int64_t>(a.rows_round / kRowsPerTask) * a.nkc >= (int64_t{1} << 20)) return TQ1_ERR_UNSUPPORTED;
   const int g = static_cast<int>(grid);
-  if (fmt == kFmtTq2) {  // plain mat-vec only
-    if (x || res) return TQ1_ERR_UNSUPPORTED;
+  if (fmt == kFmtTq2) {
     switch (rung) {
-      case 1: return launch_small_rung<1, false, false, kFmtTq2>(a, g, s);
-      case 2: return launch_small_rung<2, false, false, kFmtTq2>(a, g, s);
-      default: return launch_small_rung<4, false, false, kFmtTq2>(a, g, s);
+      case 1: return x ? launch_small_rung<1, false, true, kFmtTq2>(a, g, s)
+                       : (res ? launch_small_rung<1, true, false, kFmtTq2>(a, g, s)
+                              : launch_small_rung<1, false, false, kFmtTq2>(a, g, s));
+      case 2: return x ? launch_small_rung<2, false, true, kFmtTq2>(a, g, s)
+                       : (res ? launch_small_rung<2, true, false, kFmtTq2>(a, g, s)
+                              : launch_small_rung<2, false, false, kFmtTq2>(a, g, s));
+      default: return x ? launch_small_rung<4, false, true, kFmtTq2>(a, g, s)
+                        : (res ? launch_small_rung<4, true, false, kFmtTq2>(a, g, s)
+                               : launch_small_rung<4, false, false, kFmtTq2>(a, g, s));
     }
   }
   switch (rung) {

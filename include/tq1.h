@@ -272,6 +272,16 @@ int tq2_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t 
                      void* stream);
 
 /*
+ * TQ2_0 counterparts of tq1_mmv_f32 (Q8_1 quantisation fused into the decode
+ * kernel's prologue, 1 <= t <= 4, bit-identical to q8_1_quantize_acts +
+ * tq2_mmv) and tq1_mmv_add (y = res + W x, res may be y).  Arguments and
+ * errors as those.
+ */
+int tq2_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t, void* stream);
+int tq2_mmv_add(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
+                void* stream);
+
+/*
  * TQ2_0 rows to fp32 (out_f16 == 0) or fp16 values, d * (code - 1) exactly:
  * the whole matrix (tq2_dequantize_rows) or the rows listed in row_ids
  * (tq2_get_rows).  Arguments, layouts, errors and the handling of

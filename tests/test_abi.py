@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     for want in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_id", "tq1_mmv_partials",
                  "tq1_mmv_id_workspace_size", "tq1_sync_status", "tq1_status_string", "tq1_dequantize_rows",
                  "tq1_get_rows", "tq2_quantize_rows", "tq2_mmv", "tq2_mmv_partials", "tq2_blocks_bytes", "tq2_dequantize_rows", "tq2_get_rows", "tq2_mmv_id",
-                 "tq2_mmv_id_slots"):
+                 "tq2_mmv_id_slots", "tq2_mmv_f32", "tq2_mmv_add"):
         assert want in names
 
 
@@ -143,3 +143,10 @@ def test_tq2_mmv_id_host_checks(lib):
     assert lib.tq2_mmv_id(FAKE, 8, FAKE, None, FAKE, 16, 256, 2, 2, FAKE, ws, None) == -1
     assert lib.tq2_mmv_id_slots(FAKE, 8, FAKE, FAKE, FAKE, 16, 300, 2, 2, FAKE, ws, None) == -2
     assert lib.tq2_mmv_id_slots(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 0, 2, FAKE, ws, None) == 0
+
+
+def test_tq2_fused_entry_host_checks(lib):
+    assert lib.tq2_mmv_f32(FAKE, FAKE, FAKE, 10, 256, 5, None) == -4
+    assert lib.tq2_mmv_f32(FAKE, None, FAKE, 10, 256, 1, None) == -1
+    assert lib.tq2_mmv_add(FAKE, FAKE, None, FAKE, 10, 256, 1, None) == -1
+    assert lib.tq2_mmv_add(FAKE, FAKE, FAKE + 4, FAKE, 10, 256, 1, None) == -3

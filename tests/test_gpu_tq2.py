@@ -163,3 +163,36 @@ def test_prefill_shape_sampled_rows():
     y = _mmv(blocks, G.quantize_acts(p.x), p.n, p.k, p.t)
     ref = orc.tq2_mmv_f64(orc.tq2_encode_rows(p.w[rows]), orc.q8_1_quantize(p.x), rows.size, p.k, p.t)
     G.assert_close(y[:, rows], ref)
+
+
+@pytest.mark.parametrize("n,k,t", [(5120, 6144, 1), (300, 2048, 2), (77, 1024, 3), (129, 4096, 4)])
+def test_fused_quantisation_matches_two_step(n, k, t):
+    # tq2_mmv_f32 quantises in the decode kernel's prologue with the same
+    # operations as q8_1_quantize_acts: bit-identical outputs.
+    p = synth.matvec(n, k, t, seed=n + 3 * t)
+    blocks = _quantize_tq2(p.w)
+    two = _mmv(blocks, G.quantize_acts(p.x), n, k, t)
+    tt = G.torch()
+    y = tt.full((t, n), float("nan"), dtype=tt.float32, device="cuda")
+    G.lib().tq2_mmv_f32(blocks, G.dev(p.x.astype(np.float32)), y, n, k, t)
+    assert G.lib().tq1_sync_status() == 0
+    np.testing.assert_array_equal(G.host(y), two)
+
+
+@pytest.mark.parametrize("n,k,t", [(640, 2048, 1), (300, 2304, 3), (257, 2048, 9), (100, 2304, 40)])
+def test_residual_add(n, k, t):
+    # y = res + W x: the decode rungs, the tile path (t = 9) and the general
+    # kernel (k not a multiple of 2048); also in place (res is y).
+    p = synth.matvec(n, k, t, seed=7 * n + t)
+    blocks, q8 = _quantize_tq2(p.w), G.quantize_acts(p.x)
+    plain = _mmv(blocks, q8, n, k, t)
+    res = np.random.default_rng(t).standard_normal((t, n)).astype(np.float32)
+    tt = G.torch()
+    y = tt.full((t, n), float("nan"), dtype=tt.float32, device="cuda")
+    G.lib().tq2_mmv_add(blocks, q8, G.dev(res), y, n, k, t)
+    assert G.lib().tq1_sync_status() == 0
+    np.testing.assert_array_equal(G.host(y), (plain + res).astype(np.float32))
+    yy = G.dev(res)
+    G.lib().tq2_mmv_add(blocks, q8, yy, yy, n, k, t)
+    assert G.lib().tq1_sync_status() == 0
+    np.testing.assert_array_equal(G.host(yy), (plain + res).astype(np.float32))
