@@ -62,14 +62,14 @@ struct SmallCfg<1> {
 };
 template <>
 struct SmallCfg<2> {
-  static constexpr int kThreads = 256;
-  static constexpr int kHeld = 4;
+  static constexpr int kThreads = 448;
+  static constexpr int kHeld = 2;
   static constexpr uint32_t kSlab = 80 * 1024;
 };
 template <>
 struct SmallCfg<4> {
-  static constexpr int kThreads = 256;
-  static constexpr int kHeld = 4;
+  static constexpr int kThreads = 448;
+  static constexpr int kHeld = 2;
   static constexpr uint32_t kSlab = 64 * 1024;
 };
 
