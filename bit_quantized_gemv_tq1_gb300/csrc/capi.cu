@@ -20,7 +20,7 @@ constexpr int64_t kMaxK = 62720;  // activation records of one column must fit t
 // dp4a kernels (measured crossover on GB300 at N=5120, K=6144: the dp4a
 // kernel's cost grows with every column, the tile path's barely does).
 #ifndef TQ1_TILE_MIN_T
-#define TQ1_TILE_MIN_T 7
+#define TQ1_TILE_MIN_T 9
 #endif
 constexpr int64_t kTileMinT = TQ1_TILE_MIN_T;
 // Routed pairs up to which tq1_mmv_id skips the routing table (each pair's
@@ -173,7 +173,7 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
     rc = launch_tile(w, a, y, n, k, t, s, st, res, fmt);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the dp4a kernels below
   }
-  if (y && t <= 4) {
+  if (y && t <= 8) {
     rc = launch_mmv_small(w, a, y, n, k, t, s, st, res, nullptr, fmt);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
   }

@@ -72,6 +72,12 @@ struct SmallCfg<4> {
   static constexpr int kHeld = 2;
   static constexpr uint32_t kSlab = 64 * 1024;
 };
+template <>
+struct SmallCfg<8> {
+  static constexpr int kThreads = 448;
+  static constexpr int kHeld = 2;
+  static constexpr uint32_t kSlab = 48 * 1024;
+};
 
 struct SmallArgs {
   const uint8_t* w;
@@ -340,7 +346,7 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
 // fit this kernel's staging; the caller then uses the general kernel.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
                      unsigned* status, const float* res, const float* x, int fmt) {
-  if (t < 1 || t > 4) return TQ1_ERR_UNSUPPORTED;
+  if (t < 1 || t > 8 || (x && t > 4)) return TQ1_ERR_UNSUPPORTED;
   const DeviceInfo& di = device_info();
   SmallArgs a = {};
   a.w = w;
@@ -352,8 +358,11 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.n = n;
   a.t = static_cast<int>(t);
   a.nb = static_cast<int>(k / kQK);
-  const int rung = t == 1 ? 1 : (t == 2 ? 2 : 4);
-  const uint32_t slab = rung == 1 ? SmallCfg<1>::kSlab : (rung == 2 ? SmallCfg<2>::kSlab : SmallCfg<4>::kSlab);
+  const int rung = t == 1 ? 1 : (t == 2 ? 2 : (t <= 4 ? 4 : 8));
+  const uint32_t slab = rung == 1   ? SmallCfg<1>::kSlab
+                        : rung == 2 ? SmallCfg<2>::kSlab
+                        : rung == 4 ? SmallCfg<4>::kSlab
+                                    : SmallCfg<8>::kSlab;
   const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes);
   // Shared memory is sized to the CTA's rows (capped at the rung's slab
   // budget): two CTAs of consecutive calls must fit on one SM together.
@@ -376,9 +385,11 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
       case 2: return x ? launch_small_rung<2, false, true, kFmtTq2>(a, g, s)
                        : (res ? launch_small_rung<2, true, false, kFmtTq2>(a, g, s)
                               : launch_small_rung<2, false, false, kFmtTq2>(a, g, s));
-      default: return x ? launch_small_rung<4, false, true, kFmtTq2>(a, g, s)
-                        : (res ? launch_small_rung<4, true, false, kFmtTq2>(a, g, s)
-                               : launch_small_rung<4, false, false, kFmtTq2>(a, g, s));
+      case 4: return x ? launch_small_rung<4, false, true, kFmtTq2>(a, g, s)
+                       : (res ? launch_small_rung<4, true, false, kFmtTq2>(a, g, s)
+                              : launch_small_rung<4, false, false, kFmtTq2>(a, g, s));
+      default: return res ? launch_small_rung<8, true, false, kFmtTq2>(a, g, s)
+                          : launch_small_rung<8, false, false, kFmtTq2>(a, g, s);
     }
   }
   switch (rung) {
@@ -388,9 +399,11 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
     case 2: return x ? launch_small_rung<2, false, true, kFmtTq1>(a, g, s)
                      : (res ? launch_small_rung<2, true, false, kFmtTq1>(a, g, s)
                             : launch_small_rung<2, false, false, kFmtTq1>(a, g, s));
-    default: return x ? launch_small_rung<4, false, true, kFmtTq1>(a, g, s)
-                      : (res ? launch_small_rung<4, true, false, kFmtTq1>(a, g, s)
-                             : launch_small_rung<4, false, false, kFmtTq1>(a, g, s));
+    case 4: return x ? launch_small_rung<4, false, true, kFmtTq1>(a, g, s)
+                     : (res ? launch_small_rung<4, true, false, kFmtTq1>(a, g, s)
+                            : launch_small_rung<4, false, false, kFmtTq1>(a, g, s));
+    default: return res ? launch_small_rung<8, true, false, kFmtTq1>(a, g, s)
+                        : launch_small_rung<8, false, false, kFmtTq1>(a, g, s);
   }
 }
 

@@ -39,7 +39,7 @@ __host__ __device__ __forceinline__ uint32_t group_stride(uint32_t rowbytes) {
 // pattern of the fp32 number 1.5 * 2^23 + 4^s * I, exactly.  One fp32
 // subtraction then gives 4^s * I as a float (no integer-to-float conversion,
 // which issues on a slow pipe).
-constexpr int kPRec = 100;  // stride: 16-byte aligned, 4 banks apart
+constexpr int kPRec = 84;  // stride: 16-byte aligned; 8 consecutive records start 20 banks apart (mod 32: 8 distinct 4-bank groups)
 
 struct Packed {
   uint32_t a[8];  // slots 0..3: chunks 0..3, activation word w

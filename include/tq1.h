@@ -36,7 +36,7 @@
  *     16-byte aligned (TQ1_ERR_ALIGN otherwise).  The library never
  *     synchronises; work is enqueued on `stream` (a cudaStream_t, NULL for
  *     the legacy default stream) on the current device.  The only memory it
- *     takes is tq1_mmv's scratch for t >= 7, stream-ordered from its own
+ *     takes is tq1_mmv's scratch for t >= 9, stream-ordered from its own
  *     memory pool (see tq1_mmv).
  *   - Arguments are checked on the host before anything is launched; a
  *     failed check returns its negative code and launches nothing.
@@ -110,9 +110,9 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
  * w = d_w * trit and x = d_a * q, accumulated as
  *   sum_blocks d_w * sum_{chunks j} d_a[j] * I_j,   I_j = sum (trit * q) (exact int32)
  * in fp32.  blocks [n][k/256] TQ1_0, q8 [t][k/32] Q8_1, y fp32 [t][n].
- * t <= 6 runs the byte-major dp4a kernels (rungs of 1/2/4 columns, then a
- * general kernel with 8-column rungs);
- * t >= 7 (prefill included) runs the tensor-core path: a prep kernel splits
+ * t <= 8 runs the byte-major dp4a decode kernel (rungs of 1/2/4/8 columns;
+ * shapes whose staging does not fit it take a general dp4a kernel);
+ * t >= 9 (prefill included) runs the tensor-core path: a prep kernel splits
  * the activations into exact fp16 hi/lo parts in scratch taken from a
  * library-owned stream-ordered memory pool (cudaMallocFromPoolAsync /
  * cudaFreeAsync on `stream`: no synchronisation, capturable), then a tcgen05
@@ -253,10 +253,11 @@ int tq1_sync_status(void* stream);
  *
  * tq2_mmv: y[c][r] = sum_k w[r][k] * x[c][k] for TQ2_0 blocks [n][k/256] and
  * Q8_1 q8 [t][k/32], accumulated exactly as tq1_mmv (exact int32 per-32
- * partials, fp32 scale-and-sum per block).  t <= 4 runs the decode kernel
+ * partials, fp32 scale-and-sum per block).  t <= 8 runs the decode kernel
  * (the codes already are its packed-digit registers: masked dp4a, no
- * expansion); larger t runs the general dp4a kernel in chunks of up to 32
- * columns.  No scratch.  Deterministic.
+ * expansion); larger t runs the tensor-core tile path when k is a multiple
+ * of 2048 (activation scratch as tq1_mmv), else the general dp4a kernel in
+ * chunks of up to 32 columns.  Deterministic.
  *
  * tq2_mmv_partials: the exact int32 partials part[c][r][k/32] of tq2_mmv
  * (debug, as tq1_mmv_partials).
