@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kMThreads, 2) moe_small_kernel(const MoeArgs a
 // token's activation records while they arrive, and writes y[pair][rows].
 // A pair whose id is outside [0, n_experts) leaves its outputs untouched and
 // raises kStatusBadId.
-constexpr int kDThreads = 256;
+constexpr int kDThreads = 448;
 constexpr int kDWarps = kDThreads / 32;
 constexpr int kDMaxRows = 128;
 constexpr int kDMaxGroups = kDMaxRows / kRowsPerTask;
