@@ -30,7 +30,7 @@ using namespace packed;
 constexpr int kMThreads = 256;
 constexpr int kMWarps = kMThreads / 32;
 constexpr int kChunk = 4;        // pairs per task
-constexpr int kMaxRows = 128;    // rows per task
+constexpr int kMaxRows = 96;     // rows per task: task granularity (128-row tasks left some CTAs a whole extra task)
 constexpr int kMaxGroupsM = kMaxRows / kRowsPerTask;
 constexpr uint32_t kSlabBudget = 96 * 1024;
 constexpr size_t kMoeSmemBudget = 112 * 1024;  // two CTAs per SM
