@@ -119,9 +119,12 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
         // fp16 values by byte permute from the table {-d, 0, +d, +2d}: a
         // digit pair (a, b) selects bytes 2a, 2a+1, 2b, 2b+1 (selector
         // 34 * (a + 256 b) + 0x1010).  TQ1_0 digits never reach the fourth.
-        const uint32_t d2 = __half_as_ushort(__float2half_rn(2.0f * __half2float(__ushort_as_half(
-                                static_cast<unsigned short>(h16)))));
-        const uint32_t tlo = h16 ^ 0x8000u, thi = h16 | (d2 << 16);
+        uint32_t thi = h16;
+        if (FMT == kFmtTq2)
+          thi |= static_cast<uint32_t>(__half_as_ushort(__float2half_rn(
+                     2.0f * __half2float(__ushort_as_half(static_cast<unsigned short>(h16))))))
+                 << 16;
+        const uint32_t tlo = h16 ^ 0x8000u;
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = __byte_perm(tlo, thi, (dg[2 * i] | (dg[2 * i + 1] << 8)) * 34u + 0x1010u);
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          v[i] = dg[i] == 1u ? 0.0f : (dg[i] == 2u ? dw : (dg[i] == 3u ? 2.0f * dw : -dw));  // exact
+          v[i] = dg[i] == 1u ? 0.0f : (dg[i] == 2u ? dw : ((FMT == kFmtTq2 && dg[i] == 3u) ? 2.0f * dw : -dw));  // exact
         float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + e0);
         __stcs(o, make_float4(v[0], v[1], v[2], v[3]));
         __stcs(o + 1, make_float4(v[4], v[5], v[6], v[7]));
