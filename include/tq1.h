@@ -36,8 +36,9 @@
  *     16-byte aligned (TQ1_ERR_ALIGN otherwise).  The library never
  *     synchronises; work is enqueued on `stream` (a cudaStream_t, NULL for
  *     the legacy default stream) on the current device.  The only memory it
- *     takes is tq1_mmv's scratch for t >= 9, stream-ordered from its own
- *     memory pool (see tq1_mmv).
+ *     takes is the tensor-core path's activation scratch (the mat-vec entry
+ *     points at t >= 9 with k a multiple of 2048), stream-ordered from its
+ *     own memory pool (see tq1_mmv).
  *   - Arguments are checked on the host before anything is launched; a
  *     failed check returns its negative code and launches nothing.
  *   - Shapes: k must be a positive multiple of 256; n, t >= 0 (0 means there

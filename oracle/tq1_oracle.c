@@ -18,7 +18,7 @@
  *        ((uint8)(b*3^k) * 3) >> 8; digit 0/1/2 means -1/0/+1.  Q8_1: 32 int8
  *        values with an fp16 scale and an fp16 sum.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   R1 element order after element 160 continues the P1 pattern over the
  *      remaining 16 qs bytes, then over the 4 qh bytes (see tq1_elem_pos).
  *   R2 field order qs @0, qh @48, d @52 (little-endian fp16).
