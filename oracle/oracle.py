@@ -80,6 +80,8 @@ def _load():
         lib.orc_tq2_mmv_f64_rows.argtypes = [P, P, P, I64, I64, I64, P, I64]
         lib.orc_tq2_mmv_id_f64.argtypes = [P, I64, P, P, P, I64, I64, I64, I64]
         lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_set_num_threads.restype = None
+        lib.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
         return lib
 
@@ -91,6 +93,10 @@ def _ptr(a: np.ndarray):
 
 def num_threads() -> int:
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().orc_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- fp16 ----

@@ -438,6 +438,15 @@ void orc_tq2_mmv_id_f64(const uint8_t* expert_blocks, int64_t n_experts, const u
   orc_mmv_id_fmt(2, expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, NULL, 0);
 }
 
+/* Threads the dot products may use from now on (n >= 1). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : 1);
+#else
+  (void)n;
+#endif
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
