@@ -205,6 +205,16 @@ def cpu_oracle_baseline(budget_s: float = 12.0, min_calls: int = 1, max_calls: i
             "one_core": {"value": calls1 * alg_bytes(p.n, p.k, 1) / dt1 / 1e9, "calls": calls1, "seconds": dt1}}
 
 
+def oracle_checksum(blocks0, q80, n: int, k: int) -> float:
+    """The oracle's position-weighted checksum sum_i (i + 1) * y_i of one
+    config-2 call (the same weight copy and activations as the GPU's)."""
+    import numpy as np
+    from oracle import oracle as orc
+
+    y = orc.mmv_f64(blocks0, q80, n, k, 1)[0]
+    return float(np.dot(np.arange(1, n + 1, dtype=np.float64), y))
+
+
 # ------------------------------------------------------------------ ours ---
 def run_ours(args, ws, rank, local):
     import torch
@@ -319,6 +329,15 @@ def run_ours(args, ws, rank, local):
            "path": "pinned host fp32 activations -> device, captured library calls, fp32 outputs -> pinned host"}
     assert lib.tq1_sync_status(stream.cuda_stream) == 0
 
+    # Position-weighted checksum of call 0's outputs (a misplaced row changes
+    # it), logged with every run; the CPU leg compares it with the oracle's on
+    # the same inputs (kept here: the sweep below reuses the weight buffer).
+    import numpy as np
+    y0 = y[0].double().cpu().numpy()
+    checksum = {"gpu": float(np.dot(np.arange(1, n + 1, dtype=np.float64), y0)), "call": 0}
+    ck_blocks = blocks[:wbytes].cpu().numpy() if (rank == 0 and ws == 1 and not args.no_cpu) else None
+    ck_q8 = q8[:qbytes].cpu().numpy() if ck_blocks is not None else None
+
     # ---- T sweep (config 3 distribution), interleaved over T per pass
     sweep = None
     if not args.no_sweep:
@@ -369,6 +388,9 @@ def run_ours(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
+        ck = oracle_checksum(ck_blocks, ck_q8, n, k)
+        checksum["oracle"] = ck
+        checksum["rel_diff"] = abs(checksum["gpu"] - ck) / max(abs(ck), 1e-30)
         c = cpu_oracle_baseline(args.cpu_seconds)
         cpu = {"value": round(c["value"], 4), "unit": "GB/s", "cores": c["cores"], "kind": "oracle",
                "sample": f"{c['calls']} calls of the config-2 mat-vec (N=5120, K=6144, T=1), each = oracle Q8_1 "
@@ -401,6 +423,7 @@ def run_ours(args, ws, rank, local):
     out.update(extra)
     if cpu:
         out["cpu_baseline"] = cpu
+    out["checksum"] = checksum
     return out
 
 

@@ -53,6 +53,8 @@ def library() -> ctypes.CDLL:
         lib.tq1_status_string.argtypes = [ctypes.c_int]
         lib.tq1_version.restype = ctypes.c_char_p
         lib.tq1_version.argtypes = []
+        lib.tq1_debug_inject_wait_timeout.restype = None
+        lib.tq1_debug_inject_wait_timeout.argtypes = []
         lib.tq1_last_cuda_error.restype = ctypes.c_char_p
         lib.tq1_last_cuda_error.argtypes = []
         lib.tq1_blocks_bytes.restype = SZ

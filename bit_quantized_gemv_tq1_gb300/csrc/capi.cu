@@ -1,5 +1,6 @@
 // capi.cu -- the extern "C" entry points of libtq1 (declared in include/tq1.h):
 // host-side argument checks, rung/route selection and launches.
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -27,6 +28,7 @@ constexpr int64_t kTileMinT = TQ1_TILE_MIN_T;
 // rows are then read once per pair, not once per distinct expert).
 constexpr int64_t kMoeDirectMaxPairs = 32;
 std::mutex g_mu;
+std::atomic<int> g_inject_timeout{0};  // one-shot test hook (tq1_debug_inject_wait_timeout)
 DeviceInfo g_info[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
 bool g_have[kMaxDevices];
@@ -108,6 +110,8 @@ const char* tq1_status_string(int status) {
 
 const char* tq1_version(void) { return "0.1.0"; }
 
+void tq1_debug_inject_wait_timeout(void) { g_inject_timeout.store(1); }
+
 const char* tq1_last_cuda_error(void) { return g_last_err; }
 
 size_t tq1_blocks_bytes(int64_t n, int64_t k) {
@@ -174,7 +178,7 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the dp4a kernels below
   }
   if (y && t <= 8) {
-    rc = launch_mmv_small(w, a, y, n, k, t, s, st, res, nullptr, fmt);
+    rc = launch_mmv_small(w, a, y, n, k, t, s, st, res, nullptr, fmt, g_inject_timeout.exchange(0));
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
   }
   for (int64_t c0 = 0; c0 < t; c0 += 32) {

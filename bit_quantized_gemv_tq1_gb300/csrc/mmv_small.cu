@@ -94,6 +94,7 @@ struct SmallArgs {
   int nkc;              // 8-block chunks per row
   uint32_t slab_bytes;  // shared memory for weight rows (rounds of rows_round rows)
   uint32_t nkc_magic;   // ceil(2^32 / nkc) for nkc > 1: task / nkc == umulhi(task, magic)
+  int inject_timeout;   // test hook: CTA 0 issues no copy for its first row group (its waits give up)
 };
 
 }  // namespace
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
       const uint32_t total = delta + static_cast<uint32_t>(grows) * rowbytes;
       const uint32_t main = total & ~15u;
       uint8_t* dst = slab + static_cast<uint32_t>(g) * gstride;
+      if (a.inject_timeout && blockIdx.x == 0 && rd == 0 && g == 0) continue;  // nothing completes this barrier
       for (uint32_t i = main; i < total; ++i) dst[i] = __ldg(src - delta + i);
       mbar_arrive_expect_tx(&bars[g], main);
       if (main) bulk_g2s(dst, src - delta, main, &bars[g], policy);
@@ -345,7 +347,7 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
 // Returns TQ1_ERR_UNSUPPORTED (launching nothing) when the shape does not
 // fit this kernel's staging; the caller then uses the general kernel.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status, const float* res, const float* x, int fmt) {
+                     unsigned* status, const float* res, const float* x, int fmt, int inject_timeout) {
   if (t < 1 || t > 8 || (x && t > 4)) return TQ1_ERR_UNSUPPORTED;
   const DeviceInfo& di = device_info();
   SmallArgs a = {};
@@ -355,6 +357,7 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.res = res;
   a.x = x;
   a.status = status;
+  a.inject_timeout = inject_timeout;
   a.n = n;
   a.t = static_cast<int>(t);
   a.nb = static_cast<int>(k / kQK);

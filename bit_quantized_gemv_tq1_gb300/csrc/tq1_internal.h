@@ -36,8 +36,11 @@ int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int
 // without launching when the shape does not fit its staging.
 // With `x` (fp32 activations [t][k]) the kernel quantises them to Q8_1 in its
 // prologue and `q8` is unused.
+// `inject_timeout` (test hook): CTA 0 issues no copy for its first row group,
+// so its waits give up and the call reports a timeout.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status, const float* res = nullptr, const float* x = nullptr, int fmt = 0);
+                     unsigned* status, const float* res = nullptr, const float* x = nullptr, int fmt = 0,
+                     int inject_timeout = 0);
 
 // Expert-routed mat-vec over a compacted routing table in `ws` (general
 // dp4a kernel).

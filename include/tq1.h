@@ -79,6 +79,18 @@ const char* tq1_status_string(int status);
 /* Library version, e.g. "0.1.0". */
 const char* tq1_version(void);
 
+/*
+ * Test hook for the error path of the bounded transfer waits.  The next
+ * tq1_mmv / tq1_mmv_add / tq2_mmv / tq2_mmv_add call that runs the decode
+ * kernel (1 <= t <= 8) has its first CTA issue no copy (and no byte count)
+ * for its first 4-row group, so every wait on that group gives up after about
+ * 2 s: the call then reports TQ1_ERR_TIMEOUT through tq1_sync_status, its
+ * outputs are unspecified, and the device and the library stay usable.  The
+ * hook is one-shot: the call that consumes it clears it.  Nothing faults,
+ * traps or hangs.
+ */
+void tq1_debug_inject_wait_timeout(void);
+
 /* Name and text of the last CUDA runtime error this thread saw inside the
  * library (empty if none); explains a TQ1_ERR_CUDA. */
 const char* tq1_last_cuda_error(void);

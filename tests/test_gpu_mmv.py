@@ -196,3 +196,21 @@ def test_mmv_f32_fused_quantisation_matches_two_step(n, k, t):
     assert L.tq1_sync_status() == 0
     np.testing.assert_array_equal(G.host(y1), G.host(y2))
     G.assert_close(G.host(y1), orc.mmv_f64(orc.tq1_encode_rows(p.w), orc.q8_1_quantize(x), n, k, t))
+
+
+def test_bounded_wait_timeout_reports_status_and_recovers():
+    # Failure detection without a GPU fault: the test hook makes one CTA skip
+    # a weight copy, its bounded waits give up (about 2 s each), the call
+    # reports TQ1_ERR_TIMEOUT through the status word, and the next call on
+    # the same context is correct.
+    n, k = 640, 2048
+    p = synth.matvec(n, k, 1, seed=31)
+    blocks, q8 = _run(p)
+    L = G.lib()
+    L.library().tq1_debug_inject_wait_timeout()
+    torch = G.torch()
+    y = torch.zeros((1, n), dtype=torch.float32, device="cuda")
+    L.tq1_mmv(blocks, q8, y, n, k, 1)
+    assert L.tq1_sync_status() == -7  # TQ1_ERR_TIMEOUT
+    ob, oq = _oracle(p)
+    G.assert_close(G.mmv(blocks, q8, n, k, 1), orc.mmv_f64(ob, oq, n, k, 1))
