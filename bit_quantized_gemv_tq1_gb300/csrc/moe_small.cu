@@ -33,7 +33,7 @@ constexpr int kChunk = 4;        // pairs per task
 constexpr int kMaxRows = 96;     // rows per task: task granularity (128-row tasks left some CTAs a whole extra task)
 constexpr int kMaxGroupsM = kMaxRows / kRowsPerTask;
 constexpr uint32_t kSlabBudget = 96 * 1024;
-constexpr size_t kMoeSmemBudget = 112 * 1024;  // two CTAs per SM
+constexpr size_t kMoeSmemBudget = 112 * 1024;  // per CTA (two, or three for smaller tasks, per SM)
 
 struct MoeArgs {
   const uint8_t* w;      // expert 0's first weight block
@@ -53,7 +53,7 @@ struct MoeArgs {
 }  // namespace
 
 template <int FMT>
-__global__ void __launch_bounds__(kMThreads, 2) moe_small_kernel(const MoeArgs a) {
+__global__ void __launch_bounds__(kMThreads, 3) moe_small_kernel(const MoeArgs a) {
   constexpr int kBB = fmt_block_bytes<FMT>();
   extern __shared__ __align__(128) uint8_t smem[];
   const int nb = a.nb, nkc = a.nkc;
@@ -444,12 +444,15 @@ int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kMoeSmemBudget))))
       return TQ1_ERR_CUDA;
+    // Up to three CTAs share an SM: the largest shared-memory carveout.
+    if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
+      return TQ1_ERR_CUDA;
     configured[fmt == kFmtTq2][di.device] = true;
   }
   // Upper bound on the tasks: every pair on its own expert.
   const int64_t max_tasks = std::min<int64_t>(pairs, n_experts) * plan.row_blocks +
                             (pairs / kChunk) * plan.row_blocks;
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(2 * di.num_sms, max_tasks));
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(3 * di.num_sms, max_tasks));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kMThreads);
