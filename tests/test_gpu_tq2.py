@@ -44,6 +44,7 @@ SHAPES = [
     (1, 256, 1), (3, 256, 2), (7, 512, 3), (33, 1024, 4), (256, 1024, 1), (100, 2048, 4),
     (77, 6144, 5), (301, 768 * 4, 8), (64, 4096, 16), (130, 2048, 32), (45, 256 * 9, 33),
     (17, 6144, 2), (1000, 512, 1), (5, 256 * 63, 1), (299, 2304, 2),
+    (1, 256, 8), (9, 256 * 63, 6), (130, 2304, 7),
 ]
 
 
