@@ -18,7 +18,14 @@ Reported (one JSON line on rank 0):
                 one T per pass to spread clock drift
   e2e           the same metric with host buffers: pinned-host activations in,
                 outputs back to pinned host memory, every step
-  cpu_baseline  the plain fp64 CPU oracle on the same workload (bounded sample)
+  cpu_baseline  the plain fp64 CPU oracle on the same workload (bounded sample,
+                all host cores, plus a shorter one-thread sample)
+  checksum      sum_i (i + 1) * y_i of call 0's outputs, and the oracle's on the
+                same inputs (CPU leg)
+  extra lines   prefill_c5 (tensor-core path, N=14336 K=4096 T=512), moe_c4
+                (expert-routed, T = 1 and 32), dequant_c2, decode_chain_c2
+                (quantise-then-mat-vec vs the fused entry point), tq2_c2
+                (TQ2_0 weights on config 2's shape)
 
 --impl reference times that oracle as the reference arm.
 With torchrun (N > 1), every rank runs its own replica (independent
