@@ -61,7 +61,7 @@ extern "C" int tq1_mmv_id_noalloc(const void* expert_blocks, int64_t n_experts, 
                                   float* y, int64_t n, int64_t k, int64_t t, int64_t top_k, void* stream) {
   if (n < 0 || t < 0 || top_k < 0 || k <= 0 || (k % tq1::kQK) != 0 || n_experts <= 0) return TQ1_ERR_SHAPE;
   if (n == 0 || t == 0 || top_k == 0) return TQ1_OK;
-  if (n_experts > kMaxExperts || t > kMaxPairs || t * top_k > kMaxPairs) return TQ1_ERR_WORKSPACE;
+  if (n_experts > kMaxExperts || t > kMaxPairs || top_k > kMaxPairs || t * top_k > kMaxPairs) return TQ1_ERR_WORKSPACE;
   int32_t* table = route_table_address();
   if (table == nullptr) return TQ1_ERR_CUDA;
   return tq1_mmv_id(expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, table, kWords * sizeof(int32_t), stream);

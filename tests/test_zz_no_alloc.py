@@ -5,8 +5,12 @@ table lives in a fixed array inside the library instead of a caller
 workspace.
 
 Checked through the C ABI against tq1_mmv_id (which takes a workspace) on two
-calls in a row with different routings, so a table left over from the first
-call cannot leak into the second.  This file is collected last on purpose."""
+calls in a row with different routings.  Both calls route more than 32
+(token, slot) pairs, so they go through the compacted routing table that the
+fixed array holds (fewer pairs are served without a table); the second call
+routes to fewer experts than the first, so a table left over from the first
+call cannot leak into the second unnoticed.  A decode-sized call (no table)
+follows.  This file is collected last on purpose."""
 import numpy as np
 import pytest
 
@@ -25,37 +29,45 @@ def _experts_gpu(m):
     return blocks
 
 
-def _with_workspace(L, blocks, m, q8, ids):
+def _with_workspace(L, blocks, m, q8, ids, t_tok):
     t = G.torch()
-    ws_bytes = L.tq1_mmv_id_workspace_size(m.n_experts, m.t, m.top_k)
+    ws_bytes = L.tq1_mmv_id_workspace_size(m.n_experts, t_tok, m.top_k)
     ws = t.zeros(ws_bytes, dtype=t.uint8, device="cuda")
-    y = t.full((m.t, m.top_k, m.n), float("nan"), dtype=t.float32, device="cuda")
-    L.tq1_mmv_id(blocks, m.n_experts, q8, ids, y, m.n, m.k, m.t, m.top_k, ws)
+    y = t.full((t_tok, m.top_k, m.n), float("nan"), dtype=t.float32, device="cuda")
+    L.tq1_mmv_id(blocks, m.n_experts, q8, ids, y, m.n, m.k, t_tok, m.top_k, ws)
     assert L.tq1_sync_status() == 0
     return G.host(y)
 
 
-def _no_alloc(L, blocks, m, q8, ids):
+def _no_alloc(L, blocks, m, q8, ids, t_tok):
     t = G.torch()
-    y = t.full((m.t, m.top_k, m.n), float("nan"), dtype=t.float32, device="cuda")
-    L.tq1_mmv_id_noalloc(blocks, m.n_experts, q8, ids, y, m.n, m.k, m.t, m.top_k)
+    y = t.full((t_tok, m.top_k, m.n), float("nan"), dtype=t.float32, device="cuda")
+    L.tq1_mmv_id_noalloc(blocks, m.n_experts, q8, ids, y, m.n, m.k, t_tok, m.top_k)
     assert L.tq1_sync_status() == 0
     return G.host(y)
 
 
 def test_no_alloc_matches_workspace_entry_on_two_calls():
     L = G.lib()
-    m = synth.moe(n_experts=24, n=320, k=1024, t=6, top_k=4, seed=31)
+    m = synth.moe(n_experts=24, n=320, k=1024, t=12, top_k=4, seed=31)
+    assert m.t * m.top_k > 32  # the routing-table path
     blocks = _experts_gpu(m)
     q8 = G.quantize_acts(m.x)
-    routings = [m.ids.astype(np.int32),
-                np.roll(m.ids, 1, axis=0).astype(np.int32)[:, ::-1].copy()]
-    routings[1][0] = [5, 5 + 1, 23, 0]  # a different expert set for the second call
-    for ids_np in routings:
+    first = m.ids.astype(np.int32)
+    # Second call: only seven experts, each token's four ids distinct.
+    second = np.array([[c % 3, 3 + c % 2, 5, 6] for c in range(m.t)], dtype=np.int32)
+    assert all(len(set(row)) == m.top_k for row in second)
+    assert len(np.unique(second)) < len(np.unique(first))
+    for ids_np in (first, second):
         ids = G.dev(ids_np)
-        ref = _with_workspace(L, blocks, m, q8, ids)
-        got = _no_alloc(L, blocks, m, q8, ids)
+        ref = _with_workspace(L, blocks, m, q8, ids, m.t)
+        got = _no_alloc(L, blocks, m, q8, ids, m.t)
+        assert np.isfinite(got).all()
         G.assert_close(got, ref)
+    # A decode-sized call (one token, 4 pairs) after the table-sized ones.
+    q8_1 = G.quantize_acts(m.x[:1])
+    ids = G.dev(first[:1].copy())
+    G.assert_close(_no_alloc(L, blocks, m, q8_1, ids, 1), _with_workspace(L, blocks, m, q8_1, ids, 1))
 
 
 def test_no_alloc_rejects_calls_beyond_its_table():
@@ -63,3 +75,4 @@ def test_no_alloc_rejects_calls_beyond_its_table():
     fake = 1 << 20
     assert lib.tq1_mmv_id_noalloc(fake, 1025, fake, fake, fake, 16, 256, 1, 1, None) == -5
     assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 4097, 4, None) == -5
+    assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 1, 1 << 40, None) == -5
