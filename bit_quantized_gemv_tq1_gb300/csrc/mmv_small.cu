@@ -51,7 +51,20 @@ using namespace packed;
 constexpr int kMaxGroups = 64;   // row groups (mbarriers) per round
 
 // Per column count: threads per CTA, tasks pre-expanded per warp (held in
-// registers across the wait), and the weight-slab budget.
+// registers across the wait), the weight-slab budget, and pair mode.
+//
+// Pair mode: a lane holds two rows of one block column and reads each
+// activation-record word once for both.  With several columns the record
+// reads bind: a lane needs a column's whole 320-byte record for every block
+// it handles, shared memory delivers at most 128 bytes per cycle to an SM's
+// lanes, and without pairing the four lanes of a task that handle the same
+// block each read it (measured with ncu at N=5120, K=6144: ~2270 shared-memory
+// wavefronts per SM for every added column, ~1.1 us at 2.07 GHz, against
+// ~1390 warp instructions per sub-partition).  Measured per rung in the bench's
+// chained-call setting: 8 columns 14.7 -> 12.8 us at t = 8, 2 columns 5.52 ->
+// 5.36 us (TQ2_0 4.78 -> 4.40 us); slower at 1 column (3.52 -> 3.98 us: the
+// records do not bind there), at 4 columns (t = 3: 6.95 -> 7.80 us) and for
+// TQ2_0 at 8 columns (15.2 -> 19.4 us), which keep one row per lane.
 template <int C>
 struct SmallCfg;
 template <>
@@ -59,24 +72,28 @@ struct SmallCfg<1> {
   static constexpr int kThreads = 448;  // 14 warps (measured: 3% faster than 16 at N=5120, K=6144)
   static constexpr int kHeld = 2;
   static constexpr uint32_t kSlab = 96 * 1024;
+  static constexpr bool kPair = false;
 };
 template <>
 struct SmallCfg<2> {
   static constexpr int kThreads = 448;
   static constexpr int kHeld = 2;
   static constexpr uint32_t kSlab = 80 * 1024;
+  static constexpr bool kPair = true;
 };
 template <>
 struct SmallCfg<4> {
   static constexpr int kThreads = 448;
   static constexpr int kHeld = 2;
   static constexpr uint32_t kSlab = 64 * 1024;
+  static constexpr bool kPair = false;
 };
 template <>
 struct SmallCfg<8> {
   static constexpr int kThreads = 448;
   static constexpr int kHeld = 2;
   static constexpr uint32_t kSlab = 48 * 1024;
+  static constexpr bool kPair = true;
 };
 
 struct SmallArgs {
@@ -105,6 +122,11 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
   constexpr int kThreads = SmallCfg<C>::kThreads;
   constexpr int kWarps = kThreads / 32;
   constexpr int kHeld = SmallCfg<C>::kHeld;
+  // Pair mode: half-warp hsel takes task (warp + hsel * warps) and lane
+  // (r2, s) of it rows 2 r2 and 2 r2 + 1 at block s; otherwise the warp's 32
+  // lanes take one task, lane (r, s) row r at block s.
+  constexpr bool kPair = SmallCfg<C>::kPair && !(FMT == kFmtTq2 && C == 8);
+  static_assert(!kPair || kHeld == 2, "pair mode holds the two rows of one task");
   extern __shared__ __align__(128) uint8_t smem[];
   const int nb = a.nb;
   const int nkc = a.nkc;  // 8-block chunks per row
@@ -118,7 +140,8 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
   uint64_t* bars = reinterpret_cast<uint64_t*>(part + ((static_cast<size_t>(a.rows_cta) * nkc * C + 1) & ~size_t(1)));
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = lane >> 3, s = lane & 7;
+  const int hsel = kPair ? lane >> 4 : 0;
+  const int r = kPair ? ((lane >> 3) & 1) * 2 : lane >> 3, s = lane & 7;
   const int64_t r0 = (a.n * blockIdx.x) / gridDim.x;
   const int64_t r1 = (a.n * (blockIdx.x + 1)) / gridDim.x;
   const int rows = static_cast<int>(r1 - r0);
@@ -153,7 +176,7 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
   // Task `task` of round `rd`: its group, chunk and this lane's block offset.
   struct TaskPos {
     int g, kc, row;
-    bool live;
+    bool live, live2;  // live2: pair mode's second row (row + 1, at off + rowbytes)
     uint32_t off;
   };
   auto task_pos = [&](int rd, int task) {
@@ -164,6 +187,7 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
     T.row = rs + T.g * kRowsPerTask + r;
     const int b = T.kc * kLanesPerRow + s;
     T.live = T.row < rows && b < nb;
+    T.live2 = kPair && T.row + 1 < rows && b < nb;
     const uint32_t gbase = static_cast<uint32_t>(rs + T.g * kRowsPerTask) * rowbytes;
     T.off = static_cast<uint32_t>(T.g) * gstride + ((wlow + gbase) & 15u) + static_cast<uint32_t>(r) * rowbytes +
             static_cast<uint32_t>(b) * kBB;
@@ -183,13 +207,26 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
   const int ntasks0 = nrounds > 0 ? ((min(a.rows_round, rows) + kRowsPerTask - 1) / kRowsPerTask) * nkc : 0;
   Packed held[kHeld];
   bool ok = true;
-#pragma unroll
-  for (int h = 0; h < kHeld; ++h) {
-    const int task = warp + h * kWarps;
+  if constexpr (kPair) {
+    const int task = warp + hsel * kWarps;
     if (task < ntasks0) {
       const TaskPos T = task_pos(0, task);
       if (!mbar_wait(&bars[T.g], 0)) ok = false;
-      if (ok && T.live) unit_pack<FMT>(slab, T.off, held[h]);
+      if (ok && T.live) unit_pack<FMT>(slab, T.off, held[0]);
+      if (ok && T.live2)
+        unit_pack<FMT>(slab, T.off + rowbytes, held[1]);
+      else
+        held[1] = Packed{};  // a missing second row contributes zeros
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < kHeld; ++h) {
+      const int task = warp + h * kWarps;
+      if (task < ntasks0) {
+        const TaskPos T = task_pos(0, task);
+        if (!mbar_wait(&bars[T.g], 0)) ok = false;
+        if (ok && T.live) unit_pack<FMT>(slab, T.off, held[h]);
+      }
     }
   }
 
@@ -250,12 +287,43 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
     }
     finish_task(T, acc);
   };
+  // Pair mode: the two rows of this lane's task (valid: the lane's half-warp
+  // has a task), column by column; every lane of the warp calls it (shuffles).
+  auto dot_pair = [&](const TaskPos& T, bool valid, const Packed& A, const Packed& B) {
+    const bool la = valid && T.live;  // the second row is zeros where it does not exist
+    const int b = T.kc * kLanesPerRow + s;
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      if (c < a.t) {
+        float va = 0.0f, vb = 0.0f;
+        const uint32_t* rec = recs + c * rstride + b * kPRec;
+        if (la) packed_dot2(A, B, rec, va, vb);
+        va += __shfl_xor_sync(0xffffffffu, va, 1);
+        vb += __shfl_xor_sync(0xffffffffu, vb, 1);
+        va += __shfl_xor_sync(0xffffffffu, va, 2);
+        vb += __shfl_xor_sync(0xffffffffu, vb, 2);
+        va += __shfl_xor_sync(0xffffffffu, va, 4);
+        vb += __shfl_xor_sync(0xffffffffu, vb, 4);
+        if (s == 0 && valid) {
+          if (T.row < rows) part[(static_cast<size_t>(T.row) * nkc + T.kc) * C + c] = va;
+          if (T.row + 1 < rows) part[(static_cast<size_t>(T.row + 1) * nkc + T.kc) * C + c] = vb;
+        }
+      }
+    }
+  };
 
   if (!abort) {
+    if constexpr (kPair) {
+      if (warp < ntasks0) {  // warp-uniform; the lane's own task may not exist
+        const int task = warp + hsel * kWarps;
+        dot_pair(task_pos(0, task), task < ntasks0, held[0], held[1]);
+      }
+    } else {
 #pragma unroll
-    for (int h = 0; h < kHeld; ++h) {
-      const int task = warp + h * kWarps;
-      if (task < ntasks0) dot_task(task_pos(0, task), held[h]);
+      for (int h = 0; h < kHeld; ++h) {
+        const int task = warp + h * kWarps;
+        if (task < ntasks0) dot_task(task_pos(0, task), held[h]);
+      }
     }
   }
   int rd = 0;
@@ -265,15 +333,35 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
     const int ntasks = ngroups * nkc;
     const uint32_t parity = static_cast<uint32_t>(rd & 1);
     // Tasks not expanded before the wait (warp w: w + k * warps).
-    for (int task = warp + (rd == 0 ? kHeld * kWarps : 0); task < ntasks; task += kWarps) {
-      const TaskPos T = task_pos(rd, task);
-      if (!mbar_wait(&bars[T.g], parity)) {
-        ok = false;
-        break;
+    if constexpr (kPair) {
+      for (int base = warp + (rd == 0 ? 2 * kWarps : 0); base < ntasks; base += 2 * kWarps) {
+        const int task = base + hsel * kWarps;
+        const bool valid = task < ntasks;
+        const TaskPos T = task_pos(rd, valid ? task : base);
+        const bool landed = !valid || mbar_wait(&bars[T.g], parity);
+        if (__any_sync(0xffffffffu, !landed)) {
+          ok = false;
+          break;
+        }
+        Packed P0, P1;
+        if (valid && T.live) unit_pack<FMT>(slab, T.off, P0);
+        if (valid && T.live2)
+          unit_pack<FMT>(slab, T.off + rowbytes, P1);
+        else
+          P1 = Packed{};
+        dot_pair(T, valid, P0, P1);
       }
-      Packed P;
-      if (T.live) unit_pack<FMT>(slab, T.off, P);
-      dot_task(T, P);
+    } else {
+      for (int task = warp + (rd == 0 ? kHeld * kWarps : 0); task < ntasks; task += kWarps) {
+        const TaskPos T = task_pos(rd, task);
+        if (!mbar_wait(&bars[T.g], parity)) {
+          ok = false;
+          break;
+        }
+        Packed P;
+        if (T.live) unit_pack<FMT>(slab, T.off, P);
+        dot_task(T, P);
+      }
     }
     abort = __syncthreads_or(!ok) != 0;  // slab free, all tasks of the round done
     if (abort) break;

@@ -187,6 +187,59 @@ __device__ __forceinline__ float packed_dot(const Packed& P, const uint32_t* rec
   return s * P.dw;
 }
 
+// packed_dot for two blocks of the same block column (two rows) against one
+// column record: every record word read from shared memory serves both rows,
+// so a lane needs half the record bytes per row.  Each row's arithmetic is
+// exactly packed_dot's (same integer sums, same fp32 operation order).
+__device__ __forceinline__ void packed_dot2(const Packed& P, const Packed& Q, const uint32_t* rec, float& sp,
+                                            float& sq) {
+  const int4 s0 = *reinterpret_cast<const int4*>(rec + 72);
+  const int4 s1 = *reinterpret_cast<const int4*>(rec + 76);
+  int I0 = s0.x, I1 = s0.y, I2 = s0.z, I3 = s0.w, I4 = s1.x, I5 = s1.y, I6 = s1.z, I7 = s1.w;
+  int J0 = s0.x, J1 = s0.y, J2 = s0.z, J3 = s0.w, J4 = s1.x, J5 = s1.y, J6 = s1.z, J7 = s1.w;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint4 qa = *reinterpret_cast<const uint4*>(rec + 8 * w);
+    const uint4 qb = *reinterpret_cast<const uint4*>(rec + 8 * w + 4);
+    I0 = dp4a_us(P.a[w] & 0x03030303u, qa.x, I0);
+    J0 = dp4a_us(Q.a[w] & 0x03030303u, qa.x, J0);
+    I1 = dp4a_us(P.a[w] & 0x0C0C0C0Cu, qa.y, I1);
+    J1 = dp4a_us(Q.a[w] & 0x0C0C0C0Cu, qa.y, J1);
+    I2 = dp4a_us(P.a[w] & 0x30303030u, qa.z, I2);
+    J2 = dp4a_us(Q.a[w] & 0x30303030u, qa.z, J2);
+    I3 = dp4a_us(P.a[w] & 0xC0C0C0C0u, qa.w, I3);
+    J3 = dp4a_us(Q.a[w] & 0xC0C0C0C0u, qa.w, J3);
+    I4 = dp4a_us(P.b[w] & 0x03030303u, qb.x, I4);
+    J4 = dp4a_us(Q.b[w] & 0x03030303u, qb.x, J4);
+    I5 = dp4a_us(P.b[w] & 0x0C0C0C0Cu, qb.y, I5);
+    J5 = dp4a_us(Q.b[w] & 0x0C0C0C0Cu, qb.y, J5);
+    I6 = dp4a_us(P.b[w] & 0x30303030u, qb.z, I6);
+    J6 = dp4a_us(Q.b[w] & 0x30303030u, qb.z, J6);
+    I7 = dp4a_us(P.b[w] & 0xC0C0C0C0u, qb.w, I7);
+    J7 = dp4a_us(Q.b[w] & 0xC0C0C0C0u, qb.w, J7);
+  }
+  const float4 a0 = *reinterpret_cast<const float4*>(rec + 64);
+  const float4 a1 = *reinterpret_cast<const float4*>(rec + 68);
+  float s = a0.x * unbias(I0);
+  s = fmaf(a0.y, unbias(I1), s);
+  s = fmaf(a0.z, unbias(I2), s);
+  s = fmaf(a0.w, unbias(I3), s);
+  s = fmaf(a1.x, unbias(I4), s);
+  s = fmaf(a1.y, unbias(I5), s);
+  s = fmaf(a1.z, unbias(I6), s);
+  s = fmaf(a1.w, unbias(I7), s);
+  float u = a0.x * unbias(J0);
+  u = fmaf(a0.y, unbias(J1), u);
+  u = fmaf(a0.z, unbias(J2), u);
+  u = fmaf(a0.w, unbias(J3), u);
+  u = fmaf(a1.x, unbias(J4), u);
+  u = fmaf(a1.y, unbias(J5), u);
+  u = fmaf(a1.z, unbias(J6), u);
+  u = fmaf(a1.w, unbias(J7), u);
+  sp = s * P.dw;
+  sq = u * Q.dw;
+}
+
 // Quantise 32 fp32 activations (16-byte aligned, global) to one Q8_1 chunk
 // and write it as chunk j of a record, with the same operations and rounding
 // as q8_1_quantize_acts (d = amax / 127 with IEEE division, q =
