@@ -31,7 +31,7 @@ std::mutex g_mu;
 std::atomic<int> g_inject_timeout{0};  // one-shot test hook (tq1_debug_inject_wait_timeout)
 DeviceInfo g_info[kMaxDevices];
 unsigned* g_status_ptr[kMaxDevices];
-bool g_have[kMaxDevices];
+std::atomic<bool> g_have[kMaxDevices];  // set (release) once g_info / g_status_ptr hold the device
 
 thread_local char g_last_err[256] = "";
 
@@ -44,9 +44,9 @@ int current_device() {
 }
 
 bool ensure_device(int d) {
-  if (g_have[d]) return true;
+  if (g_have[d].load(std::memory_order_acquire)) return true;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_have[d]) return true;
+  if (g_have[d].load(std::memory_order_relaxed)) return true;
   DeviceInfo di{};
   di.device = d;
   int v = 0;
@@ -58,7 +58,7 @@ bool ensure_device(int d) {
   if (!cuda_ok(cudaGetSymbolAddress(&p, g_tq1_status))) return false;
   g_info[d] = di;
   g_status_ptr[d] = static_cast<unsigned*>(p);
-  g_have[d] = true;
+  g_have[d].store(true, std::memory_order_release);
   return true;
 }
 

@@ -24,6 +24,7 @@
 //    output rows: strata PR #1418 "Descricao").
 //  * Per-unit fp32 results are summed per row in a fixed order (deterministic,
 //    no atomics) and written once.
+#include <atomic>
 #include <algorithm>
 
 #include "../../include/tq1.h"
@@ -408,18 +409,18 @@ static int launch_rung(const MmvArgs& args0, int grid, cudaStream_t s) {
   if (bytes > di.max_smem_optin) return TQ1_ERR_UNSUPPORTED;
   // Allow the device's full opt-in shared memory (less the kernel's static
   // shared memory) once per device.
-  static size_t max_dyn[64] = {};
+  static std::atomic<size_t> max_dyn[64];  // per device; 0 until configured (threads may race to configure: idempotent)
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
-  if (max_dyn[di.device] == 0) {
+  if (max_dyn[di.device].load(std::memory_order_acquire) == 0) {
     cudaFuncAttributes fa{};
     if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_kernel<CMAX, MODE, FMT>))) return TQ1_ERR_CUDA;
     const size_t lim = di.max_smem_optin - fa.sharedSizeBytes;
     if (!cuda_ok(cudaFuncSetAttribute(mmv_kernel<CMAX, MODE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(lim))))
       return TQ1_ERR_CUDA;
-    max_dyn[di.device] = lim;
+    max_dyn[di.device].store(lim, std::memory_order_release);
   }
-  if (bytes > max_dyn[di.device]) return TQ1_ERR_UNSUPPORTED;
+  if (bytes > max_dyn[di.device].load(std::memory_order_acquire)) return TQ1_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

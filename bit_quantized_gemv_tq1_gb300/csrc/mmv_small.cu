@@ -35,6 +35,7 @@
 // (row r, block s).  The 8 lanes of a row combine their fp32 partials with
 // shuffles; per-(row, 8-block chunk) results are summed in a fixed order at
 // the end (no atomics: bitwise deterministic).
+#include <atomic>
 #include <algorithm>
 
 #include "../../include/tq1.h"
@@ -403,9 +404,9 @@ template <int C, bool RES, bool F32IN, int FMT>
 static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   const DeviceInfo& di = device_info();
   const size_t bytes = small_smem<C>(a.nb, a.rows_cta, a.slab_bytes);
-  static size_t max_dyn[64] = {};
+  static std::atomic<size_t> max_dyn[64];  // per device; 0 until configured (threads may race to configure: idempotent)
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
-  if (max_dyn[di.device] == 0) {
+  if (max_dyn[di.device].load(std::memory_order_acquire) == 0) {
     cudaFuncAttributes fa{};
     if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C, RES, F32IN, FMT>))) return TQ1_ERR_CUDA;
     const size_t lim = di.max_smem_optin - fa.sharedSizeBytes;
@@ -416,9 +417,9 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
     // shared-memory carveout so the L1 split never limits residency.
     if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN, FMT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
       return TQ1_ERR_CUDA;
-    max_dyn[di.device] = lim;
+    max_dyn[di.device].store(lim, std::memory_order_release);
   }
-  if (bytes > max_dyn[di.device]) return TQ1_ERR_UNSUPPORTED;
+  if (bytes > max_dyn[di.device].load(std::memory_order_acquire)) return TQ1_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(SmallCfg<C>::kThreads);

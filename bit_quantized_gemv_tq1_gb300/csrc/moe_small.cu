@@ -14,6 +14,7 @@
 // (packed 2-bit digits, masked dp4a) for every pair of the chunk, so each
 // packed weight byte is expanded once per chunk.  Outputs go to
 // y[pair][row]; sums run in a fixed order (bitwise deterministic).
+#include <atomic>
 #include <algorithm>
 
 #include "../../include/tq1.h"
@@ -368,13 +369,13 @@ int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, f
   a.slab_bytes = static_cast<uint32_t>(plan.rows / kRowsPerTask) * group_stride(rowbytes);
   const size_t smem = a.slab_bytes + static_cast<size_t>(a.nb) * kPRec * 4 + static_cast<size_t>(plan.rows) * a.nkc * 4;
   auto kern = fmt == kFmtTq2 ? moe_direct_kernel<kFmtTq2> : moe_direct_kernel<kFmtTq1>;
-  static bool configured[2][64] = {};
+  static std::atomic<bool> configured[2][64];  // per format and device (racing threads configure twice: idempotent)
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
-  if (!configured[fmt == kFmtTq2][di.device]) {
+  if (!configured[fmt == kFmtTq2][di.device].load(std::memory_order_acquire)) {
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kDSmemBudget))))
       return TQ1_ERR_CUDA;
-    configured[fmt == kFmtTq2][di.device] = true;
+    configured[fmt == kFmtTq2][di.device].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pairs * plan.row_blocks));
@@ -438,16 +439,16 @@ int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   const size_t smem = a.slab_bytes + static_cast<size_t>(kChunk) * a.nb * kPRec * 4 +
                       static_cast<size_t>(plan.rows) * a.nkc * kChunk * 4;
   auto kern = fmt == kFmtTq2 ? moe_small_kernel<kFmtTq2> : moe_small_kernel<kFmtTq1>;
-  static bool configured[2][64] = {};
+  static std::atomic<bool> configured[2][64];  // per format and device (racing threads configure twice: idempotent)
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
-  if (!configured[fmt == kFmtTq2][di.device]) {
+  if (!configured[fmt == kFmtTq2][di.device].load(std::memory_order_acquire)) {
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kMoeSmemBudget))))
       return TQ1_ERR_CUDA;
     // Up to three CTAs share an SM: the largest shared-memory carveout.
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
       return TQ1_ERR_CUDA;
-    configured[fmt == kFmtTq2][di.device] = true;
+    configured[fmt == kFmtTq2][di.device].store(true, std::memory_order_release);
   }
   // Upper bound on the tasks: every pair on its own expert.
   const int64_t max_tasks = std::min<int64_t>(pairs, n_experts) * plan.row_blocks +

@@ -63,6 +63,7 @@
 // 80-byte window still covers a block at any even offset (14 + 66 bytes), the
 // row-stride rule is the same (k a multiple of 2048), and the expansion is a
 // shift and mask per chunk word before the same byte permute to fp16.
+#include <atomic>
 #include <cuda.h>
 
 #include <algorithm>
@@ -927,14 +928,14 @@ template <int TOK, int FMT>
 int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms, cudaStream_t s) {
   using C = TileCfg<TOK>;
   const DeviceInfo& di = device_info();
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];  // per device (racing threads configure twice: idempotent)
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
   if (C::kSmem + 2048 > di.max_smem_optin) return TQ1_ERR_UNSUPPORTED;
-  if (!configured[di.device]) {
+  if (!configured[di.device].load(std::memory_order_acquire)) {
     if (!cuda_ok(cudaFuncSetAttribute(tile_kernel<TOK, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(C::kSmem))))
       return TQ1_ERR_CUDA;
-    configured[di.device] = true;
+    configured[di.device].store(true, std::memory_order_release);
   }
   a.tiles_m = (a.n + kTileRows - 1) / kTileRows;
   a.tiles_n = (a.t + TOK - 1) / TOK;
