@@ -79,6 +79,33 @@ def test_config3_every_t_sampled_rows():
         G.assert_close(y[:, rows], ref)
 
 
+def _cta_rows(n, ctas=152):
+    """Rows of a few whole CTAs (first, middle, last) of the decode kernel's
+    one-CTA-per-SM split, plus their neighbours."""
+    bounds = [(n * i) // ctas for i in range(ctas + 1)]
+    out = []
+    for i in (0, 1, ctas // 2, ctas - 1):
+        out.extend(range(bounds[i], bounds[i + 1]))
+    return np.unique(np.array(out))
+
+
+def test_decode_rungs_several_rounds_sampled_rows():
+    """N=5700, K=6144: a CTA holds 37 or 38 rows, more than the 8-column rung's
+    weight slab takes at once (36 rows: a second round) and more tasks than
+    the 2-column rung's warps pre-expand (30 > 28: tasks expanded after the
+    wait); the last 4-row group holds one or two rows (a paired lane whose
+    second row is missing).  Every rung, whole CTAs compared with the oracle."""
+    p = synth.matvec(5700, 6144, 8, p_zero=0.4, seed=57)
+    blocks = G.quantize_rows(p.w)
+    rows = _cta_rows(p.n)
+    ob = orc.tq1_encode_rows(p.w[rows])
+    for t in (1, 2, 3, 4, 6, 8):
+        x = p.x[:t]
+        q8 = G.quantize_acts(x)
+        y = G.mmv(blocks, q8, p.n, p.k, t)
+        G.assert_close(y[:, rows], orc.mmv_f64(ob, orc.q8_1_quantize(x), rows.size, p.k, t))
+
+
 def test_config3_partials_t32_sampled_rows():
     p = synth.config_matvec("c3")
     blocks, q8 = _run(p)

@@ -122,6 +122,22 @@ def test_decode_workload_full_size_sampled_rows():
         G.assert_close(y[:, rows], orc.tq2_mmv_f64(ob, orc.q8_1_quantize(x), rows.size, p.k, t))
 
 
+def test_decode_rungs_several_rounds_sampled_rows():
+    """TQ2_0 on the decode rungs where a CTA's rows need a second slab round
+    or tasks expanded after the wait (N=5700, K=6144: 37-38 rows per CTA),
+    whole CTAs compared with the oracle."""
+    p = synth.matvec(5700, 6144, 8, p_zero=0.4, seed=58)
+    blocks = _quantize_tq2(p.w)
+    bounds = [(p.n * i) // 152 for i in range(153)]
+    rows = np.unique(np.concatenate([np.arange(bounds[i], bounds[i + 1]) for i in (0, 1, 76, 151)]))
+    ob = orc.tq2_encode_rows(p.w[rows])
+    for t in (1, 2, 4, 8):
+        x = p.x[:t]
+        q8 = G.quantize_acts(x)
+        y = _mmv(blocks, q8, p.n, p.k, t)
+        G.assert_close(y[:, rows], orc.tq2_mmv_f64(ob, orc.q8_1_quantize(x), rows.size, p.k, t))
+
+
 def test_determinism():
     p = synth.matvec(700, 4096, 3, seed=4)
     blocks, q8 = _quantize_tq2(p.w), G.quantize_acts(p.x)
