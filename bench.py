@@ -64,7 +64,7 @@ def alg_bytes(n: int, k: int, t: int) -> int:
 # reported as null until it is captured again.
 DECODE_SOURCES = ("bit_quantized_gemv_tq1_gb300/csrc/mmv_small.cu", "bit_quantized_gemv_tq1_gb300/csrc/packed.cuh",
                   "bit_quantized_gemv_tq1_gb300/csrc/tq1_device.cuh")
-DECODE_TRAFFIC = {"sha256": "3c4211494f6f0926f63b02ae9160bba420dff6f11dfd418e9b212dd39b88288a", "bytes": 6694272}
+DECODE_TRAFFIC = {"sha256": "3c4211494f6f0926f63b02ae9160bba420dff6f11dfd418e9b212dd39b88288a", "bytes": 6694144}
 
 
 def decode_sources_digest() -> str:
