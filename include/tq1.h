@@ -165,7 +165,8 @@ int tq1_mmv_add(const void* blocks, const void* q8, const float* res, float* y, 
 
 /*
  * Debug entry: the exact integer partials part[c][r][j] = I_j (int32,
- * [t][n][k/32]) that tq1_mmv scales.  t <= 32.  Bit-exact by construction.
+ * [t][n][k/32]) that tq1_mmv scales, for any t (computed in slices of up to
+ * 32 columns by the general dp4a kernel).  Bit-exact by construction.
  */
 int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,
                      void* stream);
