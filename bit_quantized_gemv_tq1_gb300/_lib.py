@@ -83,6 +83,8 @@ def library() -> ctypes.CDLL:
         lib.tq1_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq1_mmv_id_slots.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq1_mmv_id_noalloc.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P]
+        lib.tq1_mmv_id_partials.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
+        lib.tq2_mmv_id_partials.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq1_dequantize_rows.argtypes = [P, P, I64, I64, ctypes.c_int, P]
         lib.tq1_get_rows.argtypes = [P, P, I64, P, I64, I64, ctypes.c_int, P]
         lib.tq1_sync_status.argtypes = [P]
@@ -90,7 +92,8 @@ def library() -> ctypes.CDLL:
                      "tq1_mmv_partials", "tq1_mmv_id", "tq1_mmv_id_slots", "tq1_mmv_id_noalloc",
                      "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status", "tq2_quantize_rows",
                      "tq2_mmv", "tq2_mmv_partials", "tq2_dequantize_rows", "tq2_get_rows", "tq2_mmv_id",
-                     "tq2_mmv_id_slots", "tq2_mmv_f32", "tq2_mmv_add"):
+                     "tq2_mmv_id_slots", "tq2_mmv_f32", "tq2_mmv_add", "tq1_mmv_id_partials",
+                     "tq2_mmv_id_partials"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -178,6 +181,22 @@ def tq1_mmv_id_slots(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, 
         ws_bytes = ws.numel() * ws.element_size()
     _check(library().tq1_mmv_id_slots(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(y), n, k, t,
                                       top_k, _addr(ws), ws_bytes, _stream(stream)), "tq1_mmv_id_slots")
+
+
+def tq1_mmv_id_partials(expert_blocks, n_experts: int, q8, ids, part, n: int, k: int, t: int, top_k: int, ws,
+                        ws_bytes: int | None = None, stream=None) -> None:
+    """Debug: the exact int32 partials part[t][top_k][n][k/32] of tq1_mmv_id."""
+    wsb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(library().tq1_mmv_id_partials(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(part), n, k,
+                                         t, top_k, _addr(ws), wsb, _stream(stream)), "tq1_mmv_id_partials")
+
+
+def tq2_mmv_id_partials(expert_blocks, n_experts: int, q8, ids, part, n: int, k: int, t: int, top_k: int, ws,
+                        ws_bytes: int | None = None, stream=None) -> None:
+    """Debug: the exact int32 partials part[t][top_k][n][k/32] of tq2_mmv_id."""
+    wsb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(library().tq2_mmv_id_partials(_addr(expert_blocks), n_experts, _addr(q8), _addr(ids), _addr(part), n, k,
+                                         t, top_k, _addr(ws), wsb, _stream(stream)), "tq2_mmv_id_partials")
 
 
 def tq1_mmv_id_noalloc(expert_blocks, n_experts: int, q8, ids, y, n: int, k: int, t: int, top_k: int,

@@ -169,6 +169,9 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
   if (k > kMaxK) return TQ1_ERR_UNSUPPORTED;
   unsigned* st = status_ptr();
   if (!st) return TQ1_ERR_CUDA;
+  // The test hook is consumed by this call whichever kernel runs; only the
+  // decode kernel acts on it.
+  const int inject = g_inject_timeout.exchange(0);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint8_t* w = static_cast<const uint8_t*>(blocks);
   const uint8_t* a = static_cast<const uint8_t*>(q8);
@@ -177,8 +180,9 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
     rc = launch_tile(w, a, y, n, k, t, s, st, res, fmt);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the dp4a kernels below
   }
-  if (y && t <= 8) {
-    rc = launch_mmv_small(w, a, y, n, k, t, s, st, res, nullptr, fmt, g_inject_timeout.exchange(0));
+  if (t <= 8) {
+    // The decode kernel: fp32 outputs, or (debug entry) its exact partials.
+    rc = launch_mmv_small(w, a, y, n, k, t, s, st, res, nullptr, fmt, y ? inject : 0, y ? nullptr : part);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
   }
   for (int64_t c0 = 0; c0 < t; c0 += 32) {
@@ -289,13 +293,14 @@ size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k) {
 
 static int mmv_id_common(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
                          int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream,
-                         bool per_slot, int fmt = kFmtTq1) {
+                         bool per_slot, int fmt = kFmtTq1, int32_t* part = nullptr) {
   int rc = check_mmv_shape(n, k, t);
   if (rc != TQ1_OK) return rc;
   if (n_experts <= 0 || top_k < 0) return TQ1_ERR_SHAPE;
   if (n == 0 || t == 0 || top_k == 0) return TQ1_OK;
-  if (!expert_blocks || !q8 || !ids || !y || !ws) return TQ1_ERR_NULL;
-  if (misaligned(expert_blocks) || misaligned(q8) || misaligned(ids) || misaligned(y) || misaligned(ws))
+  if (!expert_blocks || !q8 || !ids || (!y && !part) || !ws) return TQ1_ERR_NULL;
+  if (misaligned(expert_blocks) || misaligned(q8) || misaligned(ids) || (y && misaligned(y)) ||
+      (part && misaligned(part)) || misaligned(ws))
     return TQ1_ERR_ALIGN;
   if (ws_bytes < tq1_mmv_id_workspace_size(n_experts, t, top_k)) return TQ1_ERR_WORKSPACE;
   if (k > kMaxK || n_experts > 12288 || t * top_k > (int64_t{1} << 30)) return TQ1_ERR_UNSUPPORTED;
@@ -309,14 +314,15 @@ static int mmv_id_common(const void* expert_blocks, int64_t n_experts, const voi
   MoePlan plan{};
   // A few pairs (decode): no routing table, each CTA reads its pair's id.
   if (t * top_k <= kMoeDirectMaxPairs && moe_direct_plan(n, k, t * top_k, &plan, fmt))
-    return launch_moe_direct(w, a, ids, y, n, k, top_k, n_experts, t * top_k, plan, s, st, act_div, fmt);
+    return launch_moe_direct(w, a, ids, y, n, k, top_k, n_experts, t * top_k, plan, s, st, act_div, fmt, part);
   const bool small = moe_small_plan(n, k, t * top_k, n_experts, &plan, fmt);
+  if (part && !small) return TQ1_ERR_UNSUPPORTED;  // partials come from the routed decode kernels only
   rc = launch_moe_compact(ids, t, top_k, n_experts, small ? plan.chunk : 1, small ? plan.row_blocks : 1, table, s,
                           st);
   if (rc != TQ1_OK) return rc;
   if (small) {
-    rc = launch_moe_small(w, a, y, n, k, top_k, n_experts, t * top_k, plan, table, s, st, act_div, fmt);
-    if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
+    rc = launch_moe_small(w, a, y, n, k, top_k, n_experts, t * top_k, plan, table, s, st, act_div, fmt, part);
+    if (rc != TQ1_ERR_UNSUPPORTED || part) return rc;  // otherwise the general kernel below
   }
   return launch_mmv_id(w, n_experts, a, y, n, k, t, top_k, table, s, st, act_div, fmt);
 }
@@ -341,6 +347,22 @@ int tq2_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, con
 int tq2_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
                      int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream) {
   return mmv_id_common(expert_blocks, n_experts, q8, ids, y, n, k, t, top_k, ws, ws_bytes, stream, true, kFmtTq2);
+}
+
+int tq1_mmv_id_partials(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids,
+                        int32_t* part, int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes,
+                        void* stream) {
+  if (!part && n > 0 && t > 0 && top_k > 0 && n_experts > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;
+  return mmv_id_common(expert_blocks, n_experts, q8, ids, nullptr, n, k, t, top_k, ws, ws_bytes, stream, false,
+                       kFmtTq1, part);
+}
+
+int tq2_mmv_id_partials(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids,
+                        int32_t* part, int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes,
+                        void* stream) {
+  if (!part && n > 0 && t > 0 && top_k > 0 && n_experts > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;
+  return mmv_id_common(expert_blocks, n_experts, q8, ids, nullptr, n, k, t, top_k, ws, ws_bytes, stream, false,
+                       kFmtTq2, part);
 }
 
 int tq1_sync_status(void* stream) {

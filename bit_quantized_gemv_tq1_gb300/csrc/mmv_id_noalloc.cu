@@ -20,6 +20,7 @@
 // be cleared between calls.  Calls whose kernels may overlap on the GPU (on
 // different streams without ordering between them) race on the array and must
 // not be issued.
+#include <atomic>
 #include <mutex>
 
 #include "../../include/tq1.h"
@@ -37,24 +38,29 @@ constexpr size_t kWords =
 constexpr int kMaxDevices = 64;
 
 std::mutex g_mu;
-int32_t* g_table[kMaxDevices];
+std::atomic<int32_t*> g_table[kMaxDevices];  // published (release) once looked up
 
 }  // namespace
 
 static __device__ __align__(256) int32_t g_route_table[kWords];
 
 // Device address of g_route_table on the current device (looked up once per
-// device), or nullptr if the runtime call failed.
+// device, under a lock; later calls read the published address without it),
+// or nullptr if the runtime call failed.
 static int32_t* route_table_address() {
   int dev = 0;
   if (!tq1::cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= kMaxDevices) return nullptr;
+  int32_t* known = g_table[dev].load(std::memory_order_acquire);
+  if (known != nullptr) return known;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_table[dev] == nullptr) {
+  known = g_table[dev].load(std::memory_order_relaxed);
+  if (known == nullptr) {
     void* p = nullptr;
     if (!tq1::cuda_ok(cudaGetSymbolAddress(&p, g_route_table))) return nullptr;
-    g_table[dev] = static_cast<int32_t*>(p);
+    known = static_cast<int32_t*>(p);
+    g_table[dev].store(known, std::memory_order_release);
   }
-  return g_table[dev];
+  return known;
 }
 
 extern "C" int tq1_mmv_id_noalloc(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids,

@@ -1,6 +1,7 @@
-// mmv_small.cu -- TQ1_0 x Q8_1 mat-vec for 1, 2 and 4 token columns: the
-// decode path.  The same kernel runs TQ2_0 weights, whose 2-bit codes are
-// already in the packed-digit layout below (no expansion step).
+// mmv_small.cu -- TQ1_0 x Q8_1 mat-vec for 1 to 8 token columns (rungs of 1,
+// 2, 4 and 8 columns): the decode path.  The same kernel runs TQ2_0 weights,
+// whose 2-bit codes are already in the packed-digit layout below (no
+// expansion step).
 //
 // PrismML-Eng/llama.cpp issue #139, "Proposed approach" option 1: a kernel
 // that consumes whole 256-element blocks and iterates over packed bytes, so
@@ -35,6 +36,11 @@
 // (row r, block s).  The 8 lanes of a row combine their fp32 partials with
 // shuffles; per-(row, 8-block chunk) results are summed in a fixed order at
 // the end (no atomics: bitwise deterministic).
+//
+// Partials mode (PART, the debug entry points): the same expansion and the
+// same dp4a sums, but each lane stores its block's eight exact per-chunk
+// integer partials I_j instead of scaling them (PrismML-Eng/llama.cpp issue
+// #139, "Acceptance criteria": the kernel checked against a CPU reference).
 #include <atomic>
 #include <algorithm>
 
@@ -101,6 +107,7 @@ struct SmallArgs {
   const uint8_t* w;
   const uint8_t* q8;
   float* y;
+  int32_t* part;        // PART: exact partials [t][n][k/32] (y unused)
   const float* res;     // optional residual added to y (same layout), or nullptr
   const float* x;       // fp32 activations [t][k] quantised in the prologue (F32IN), else unused
   unsigned* status;
@@ -117,7 +124,7 @@ struct SmallArgs {
 
 }  // namespace
 
-template <int C, bool RES, bool F32IN, int FMT>
+template <int C, bool RES, bool F32IN, int FMT, bool PART = false>
 __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(const SmallArgs a) {
   constexpr int kBB = fmt_block_bytes<FMT>();
   constexpr int kThreads = SmallCfg<C>::kThreads;
@@ -276,38 +283,65 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
       for (int c = 0; c < C; ++c) part[(static_cast<size_t>(T.row) * nkc + T.kc) * C + c] = acc[c];
     }
   };
+  // Partials mode: this lane's block of row T.row (and of row T.row + 1 in
+  // pair mode), column by column, straight to global memory.
+  auto part_out = [&](int c, int row, int b) {
+    return a.part + ((static_cast<int64_t>(c) * a.n + r0 + row) * nb + b) * 8;
+  };
   auto dot_task = [&](const TaskPos& T, const Packed& P) {
-    float acc[C];
+    if constexpr (PART) {
+      if (T.live) {
+        const int b = T.kc * kLanesPerRow + s;
+        for (int c = 0; c < a.t; ++c) {
+          int I[8];
+          packed_sums(P, recs + c * rstride + b * kPRec, I);
+          store_partials(part_out(c, T.row, b), I);
+        }
+      }
+    } else {
+      float acc[C];
 #pragma unroll
-    for (int c = 0; c < C; ++c) acc[c] = 0.0f;
-    if (T.live) {
-      const int b = T.kc * kLanesPerRow + s;
+      for (int c = 0; c < C; ++c) acc[c] = 0.0f;
+      if (T.live) {
+        const int b = T.kc * kLanesPerRow + s;
 #pragma unroll
-      for (int c = 0; c < C; ++c)
-        if (c < a.t) acc[c] = packed_dot(P, recs + c * rstride + b * kPRec);
+        for (int c = 0; c < C; ++c)
+          if (c < a.t) acc[c] = packed_dot(P, recs + c * rstride + b * kPRec);
+      }
+      finish_task(T, acc);
     }
-    finish_task(T, acc);
   };
   // Pair mode: the two rows of this lane's task (valid: the lane's half-warp
   // has a task), column by column; every lane of the warp calls it (shuffles).
   auto dot_pair = [&](const TaskPos& T, bool valid, const Packed& A, const Packed& B) {
     const bool la = valid && T.live;  // the second row is zeros where it does not exist
     const int b = T.kc * kLanesPerRow + s;
+    if constexpr (PART) {
+      if (la) {
+        for (int c = 0; c < a.t; ++c) {
+          int I[8], J[8];
+          packed_sums2(A, B, recs + c * rstride + b * kPRec, I, J);
+          store_partials(part_out(c, T.row, b), I);
+          if (T.live2) store_partials(part_out(c, T.row + 1, b), J);
+        }
+      }
+    } else {
 #pragma unroll
-    for (int c = 0; c < C; ++c) {
-      if (c < a.t) {
-        float va = 0.0f, vb = 0.0f;
-        const uint32_t* rec = recs + c * rstride + b * kPRec;
-        if (la) packed_dot2(A, B, rec, va, vb);
-        va += __shfl_xor_sync(0xffffffffu, va, 1);
-        vb += __shfl_xor_sync(0xffffffffu, vb, 1);
-        va += __shfl_xor_sync(0xffffffffu, va, 2);
-        vb += __shfl_xor_sync(0xffffffffu, vb, 2);
-        va += __shfl_xor_sync(0xffffffffu, va, 4);
-        vb += __shfl_xor_sync(0xffffffffu, vb, 4);
-        if (s == 0 && valid) {
-          if (T.row < rows) part[(static_cast<size_t>(T.row) * nkc + T.kc) * C + c] = va;
-          if (T.row + 1 < rows) part[(static_cast<size_t>(T.row + 1) * nkc + T.kc) * C + c] = vb;
+      for (int c = 0; c < C; ++c) {
+        if (c < a.t) {
+          float va = 0.0f, vb = 0.0f;
+          const uint32_t* rec = recs + c * rstride + b * kPRec;
+          if (la) packed_dot2(A, B, rec, va, vb);
+          va += __shfl_xor_sync(0xffffffffu, va, 1);
+          vb += __shfl_xor_sync(0xffffffffu, vb, 1);
+          va += __shfl_xor_sync(0xffffffffu, va, 2);
+          vb += __shfl_xor_sync(0xffffffffu, vb, 2);
+          va += __shfl_xor_sync(0xffffffffu, va, 4);
+          vb += __shfl_xor_sync(0xffffffffu, vb, 4);
+          if (s == 0 && valid) {
+            if (T.row < rows) part[(static_cast<size_t>(T.row) * nkc + T.kc) * C + c] = va;
+            if (T.row + 1 < rows) part[(static_cast<size_t>(T.row + 1) * nkc + T.kc) * C + c] = vb;
+          }
         }
       }
     }
@@ -380,14 +414,16 @@ __global__ void __launch_bounds__(SmallCfg<C>::kThreads, 2) mmv_small_kernel(con
     return;
   }
 
-  // y[c][r0 + row] = sum over block chunks, in order.
-  for (int c = 0; c < a.t; ++c)
-    for (int row = tid; row < rows; row += kThreads) {
-      float v = 0.0f;
-      for (int kc = 0; kc < nkc; ++kc) v += part[(static_cast<size_t>(row) * nkc + kc) * C + c];
-      const int64_t yi = static_cast<int64_t>(c) * a.n + r0 + row;
-      a.y[yi] = RES ? v + a.res[yi] : v;
-    }
+  if constexpr (!PART) {
+    // y[c][r0 + row] = sum over block chunks, in order.
+    for (int c = 0; c < a.t; ++c)
+      for (int row = tid; row < rows; row += kThreads) {
+        float v = 0.0f;
+        for (int kc = 0; kc < nkc; ++kc) v += part[(static_cast<size_t>(row) * nkc + kc) * C + c];
+        const int64_t yi = static_cast<int64_t>(c) * a.n + r0 + row;
+        a.y[yi] = RES ? v + a.res[yi] : v;
+      }
+  }
 }
 
 template <int C>
@@ -400,7 +436,7 @@ static size_t small_smem(int nb, int rows_cta, uint32_t slab_bytes) {
   return b;
 }
 
-template <int C, bool RES, bool F32IN, int FMT>
+template <int C, bool RES, bool F32IN, int FMT, bool PART = false>
 static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   const DeviceInfo& di = device_info();
   const size_t bytes = small_smem<C>(a.nb, a.rows_cta, a.slab_bytes);
@@ -408,14 +444,14 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
   if (max_dyn[di.device].load(std::memory_order_acquire) == 0) {
     cudaFuncAttributes fa{};
-    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C, RES, F32IN, FMT>))) return TQ1_ERR_CUDA;
+    if (!cuda_ok(cudaFuncGetAttributes(&fa, mmv_small_kernel<C, RES, F32IN, FMT, PART>))) return TQ1_ERR_CUDA;
     const size_t lim = di.max_smem_optin - fa.sharedSizeBytes;
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN, FMT, PART>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(lim))))
       return TQ1_ERR_CUDA;
     // Two CTAs of consecutive calls share an SM: ask for the largest
     // shared-memory carveout so the L1 split never limits residency.
-    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN, FMT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
+    if (!cuda_ok(cudaFuncSetAttribute(mmv_small_kernel<C, RES, F32IN, FMT, PART>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
       return TQ1_ERR_CUDA;
     max_dyn[di.device].store(lim, std::memory_order_release);
   }
@@ -430,19 +466,20 @@ static int launch_small_rung(const SmallArgs& a, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_small_kernel<C, RES, F32IN, FMT>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, mmv_small_kernel<C, RES, F32IN, FMT, PART>, a)) ? TQ1_OK : TQ1_ERR_CUDA;
 }
 
 // Returns TQ1_ERR_UNSUPPORTED (launching nothing) when the shape does not
 // fit this kernel's staging; the caller then uses the general kernel.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                     unsigned* status, const float* res, const float* x, int fmt, int inject_timeout) {
-  if (t < 1 || t > 8 || (x && t > 4)) return TQ1_ERR_UNSUPPORTED;
+                     unsigned* status, const float* res, const float* x, int fmt, int inject_timeout, int32_t* part) {
+  if (t < 1 || t > 8 || (x && t > 4) || (part && (x || res))) return TQ1_ERR_UNSUPPORTED;
   const DeviceInfo& di = device_info();
   SmallArgs a = {};
   a.w = w;
   a.q8 = q8;
   a.y = y;
+  a.part = part;
   a.res = res;
   a.x = x;
   a.status = status;
@@ -469,6 +506,18 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.nkc_magic = a.nkc > 1 ? static_cast<uint32_t>(((uint64_t{1} << 32) + a.nkc - 1) / a.nkc) : 0u;
   if (static_cast<int64_t>(a.rows_round / kRowsPerTask) * a.nkc >= (int64_t{1} << 20)) return TQ1_ERR_UNSUPPORTED;
   const int g = static_cast<int>(grid);
+  if (part) {
+    switch (rung) {
+      case 1: return fmt == kFmtTq2 ? launch_small_rung<1, false, false, kFmtTq2, true>(a, g, s)
+                                    : launch_small_rung<1, false, false, kFmtTq1, true>(a, g, s);
+      case 2: return fmt == kFmtTq2 ? launch_small_rung<2, false, false, kFmtTq2, true>(a, g, s)
+                                    : launch_small_rung<2, false, false, kFmtTq1, true>(a, g, s);
+      case 4: return fmt == kFmtTq2 ? launch_small_rung<4, false, false, kFmtTq2, true>(a, g, s)
+                                    : launch_small_rung<4, false, false, kFmtTq1, true>(a, g, s);
+      default: return fmt == kFmtTq2 ? launch_small_rung<8, false, false, kFmtTq2, true>(a, g, s)
+                                     : launch_small_rung<8, false, false, kFmtTq1, true>(a, g, s);
+    }
+  }
   if (fmt == kFmtTq2) {
     switch (rung) {
       case 1: return x ? launch_small_rung<1, false, true, kFmtTq2>(a, g, s)

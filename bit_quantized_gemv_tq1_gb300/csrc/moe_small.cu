@@ -14,6 +14,10 @@
 // (packed 2-bit digits, masked dp4a) for every pair of the chunk, so each
 // packed weight byte is expanded once per chunk.  Outputs go to
 // y[pair][row]; sums run in a fixed order (bitwise deterministic).
+//
+// Both kernels have a partials mode (PART) for the debug entry points: the
+// same expansion and dp4a sums, with each lane storing its block's eight exact
+// per-chunk integer partials to part[pair][row][k/32] instead of scaling them.
 #include <atomic>
 #include <algorithm>
 
@@ -40,6 +44,7 @@ struct MoeArgs {
   const uint8_t* w;      // expert 0's first weight block
   const uint8_t* q8;     // Q8_1 activations [t][k/32]
   float* y;              // [t * top_k][n]
+  int32_t* part;         // PART: exact partials [t * top_k][n][k/32] (y unused)
   unsigned* status;
   const int32_t* table;  // compacted routing table (layout in tq1_internal.h)
   int64_t n;
@@ -53,7 +58,7 @@ struct MoeArgs {
 
 }  // namespace
 
-template <int FMT>
+template <int FMT, bool PART>
 __global__ void __launch_bounds__(kMThreads, 3) moe_small_kernel(const MoeArgs a) {
   constexpr int kBB = fmt_block_bytes<FMT>();
   extern __shared__ __align__(128) uint8_t smem[];
@@ -161,21 +166,31 @@ __global__ void __launch_bounds__(kMThreads, 3) moe_small_kernel(const MoeArgs a
         const uint32_t off = static_cast<uint32_t>(g) * gstride + ((wlow + static_cast<uint32_t>(g) * kRowsPerTask * rowbytes) & 15u) +
                              static_cast<uint32_t>(r) * rowbytes + static_cast<uint32_t>(b) * kBB;
         unit_pack<FMT>(slab, off, P);
+        if constexpr (PART) {
+          for (int c = 0; c < pc; ++c) {
+            int I[8];
+            packed_sums(P, recs + c * rstride + b * kPRec, I);
+            store_partials(a.part + ((static_cast<int64_t>(s_pair[c]) * a.n + r0 + row) * nb + b) * 8, I);
+          }
+        } else {
 #pragma unroll
-        for (int c = 0; c < kChunk; ++c)
-          if (c < pc) acc[c] = packed_dot(P, recs + c * rstride + b * kPRec);
+          for (int c = 0; c < kChunk; ++c)
+            if (c < pc) acc[c] = packed_dot(P, recs + c * rstride + b * kPRec);
+        }
       }
+      if constexpr (!PART) {
 #pragma unroll
-      for (int c = 0; c < kChunk; ++c) {
-        float v = acc[c];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        acc[c] = v;
-      }
-      if (s == 0 && row < rows) {
+        for (int c = 0; c < kChunk; ++c) {
+          float v = acc[c];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          acc[c] = v;
+        }
+        if (s == 0 && row < rows) {
 #pragma unroll
-        for (int c = 0; c < kChunk; ++c) part[(row * nkc + kc) * kChunk + c] = acc[c];
+          for (int c = 0; c < kChunk; ++c) part[(row * nkc + kc) * kChunk + c] = acc[c];
+        }
       }
     }
     if (!ok) s_abort = 1;
@@ -189,7 +204,7 @@ __global__ void __launch_bounds__(kMThreads, 3) moe_small_kernel(const MoeArgs a
       return;
     }
     // y[pair][r0 + row]: sum over the 8-block chunks, in order.
-    for (int i = tid; i < rows * pc; i += kMThreads) {
+    for (int i = tid; i < (PART ? 0 : rows * pc); i += kMThreads) {
       const int c = i / rows, row = i - (i / rows) * rows;
       float v = 0.0f;
       for (int kc = 0; kc < nkc; ++kc) v += part[(row * nkc + kc) * kChunk + c];
@@ -219,6 +234,7 @@ struct DirectArgs {
   const uint8_t* q8;     // Q8_1 activations [t][k/32]
   const int32_t* ids;    // [t][top_k]
   float* y;              // [t * top_k][n]
+  int32_t* part;         // PART: exact partials [t * top_k][n][k/32] (y unused)
   unsigned* status;
   int64_t n;
   int n_experts, top_k, nb, nkc;
@@ -228,7 +244,7 @@ struct DirectArgs {
   uint32_t slab_bytes;
 };
 
-template <int FMT>
+template <int FMT, bool PART>
 __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectArgs a) {
   constexpr int kBB = fmt_block_bytes<FMT>();
   extern __shared__ __align__(128) uint8_t smem[];
@@ -298,8 +314,15 @@ __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectAr
                            ((wlow + static_cast<uint32_t>(g) * kRowsPerTask * rowbytes) & 15u) +
                            static_cast<uint32_t>(r) * rowbytes + static_cast<uint32_t>(b) * kBB;
       unit_pack<FMT>(slab, off, P);
-      v = packed_dot(P, recs + b * kPRec);
+      if constexpr (PART) {
+        int I[8];
+        packed_sums(P, recs + b * kPRec, I);
+        store_partials(a.part + ((static_cast<int64_t>(pair) * a.n + r0 + row) * nb + b) * 8, I);
+      } else {
+        v = packed_dot(P, recs + b * kPRec);
+      }
     }
+    if (PART) continue;
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
     v += __shfl_xor_sync(0xffffffffu, v, 4);
@@ -316,7 +339,7 @@ __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectAr
     }
     return;
   }
-  if (nkc > 1) {
+  if (nkc > 1 && !PART) {
     for (int row = tid; row < rows; row += kDThreads) {
       float v = 0.0f;
       for (int kc = 0; kc < nkc; ++kc) v += part[row * nkc + kc];  // in order
@@ -349,9 +372,10 @@ bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan, int fmt
 
 int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
                       int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
-                      unsigned* status, int act_div, int fmt) {
+                      unsigned* status, int act_div, int fmt, int32_t* part) {
   const DeviceInfo& di = device_info();
   DirectArgs a = {};
+  a.part = part;
   a.act_div = act_div;
   a.w = w;
   a.q8 = q8;
@@ -368,14 +392,18 @@ int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, f
   const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes);
   a.slab_bytes = static_cast<uint32_t>(plan.rows / kRowsPerTask) * group_stride(rowbytes);
   const size_t smem = a.slab_bytes + static_cast<size_t>(a.nb) * kPRec * 4 + static_cast<size_t>(plan.rows) * a.nkc * 4;
-  auto kern = fmt == kFmtTq2 ? moe_direct_kernel<kFmtTq2> : moe_direct_kernel<kFmtTq1>;
-  static std::atomic<bool> configured[2][64];  // per format and device (racing threads configure twice: idempotent)
+  const int kv = (fmt == kFmtTq2 ? 1 : 0) + (part ? 2 : 0);
+  auto kern = kv == 0   ? moe_direct_kernel<kFmtTq1, false>
+              : kv == 1 ? moe_direct_kernel<kFmtTq2, false>
+              : kv == 2 ? moe_direct_kernel<kFmtTq1, true>
+                        : moe_direct_kernel<kFmtTq2, true>;
+  static std::atomic<bool> configured[4][64];  // per kernel variant and device (racing threads configure twice: idempotent)
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
-  if (!configured[fmt == kFmtTq2][di.device].load(std::memory_order_acquire)) {
+  if (!configured[kv][di.device].load(std::memory_order_acquire)) {
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kDSmemBudget))))
       return TQ1_ERR_CUDA;
-    configured[fmt == kFmtTq2][di.device].store(true, std::memory_order_release);
+    configured[kv][di.device].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pairs * plan.row_blocks));
@@ -417,9 +445,10 @@ bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoeP
 
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
-                     unsigned* status, int act_div, int fmt) {
+                     unsigned* status, int act_div, int fmt, int32_t* part) {
   const DeviceInfo& di = device_info();
   MoeArgs a = {};
+  a.part = part;
   a.act_div = act_div;
   a.w = w;
   a.q8 = q8;
@@ -438,17 +467,21 @@ int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   a.slab_bytes = static_cast<uint32_t>(plan.rows / kRowsPerTask) * group_stride(rowbytes);
   const size_t smem = a.slab_bytes + static_cast<size_t>(kChunk) * a.nb * kPRec * 4 +
                       static_cast<size_t>(plan.rows) * a.nkc * kChunk * 4;
-  auto kern = fmt == kFmtTq2 ? moe_small_kernel<kFmtTq2> : moe_small_kernel<kFmtTq1>;
-  static std::atomic<bool> configured[2][64];  // per format and device (racing threads configure twice: idempotent)
+  const int kv = (fmt == kFmtTq2 ? 1 : 0) + (part ? 2 : 0);
+  auto kern = kv == 0   ? moe_small_kernel<kFmtTq1, false>
+              : kv == 1 ? moe_small_kernel<kFmtTq2, false>
+              : kv == 2 ? moe_small_kernel<kFmtTq1, true>
+                        : moe_small_kernel<kFmtTq2, true>;
+  static std::atomic<bool> configured[4][64];  // per kernel variant and device (racing threads configure twice: idempotent)
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
-  if (!configured[fmt == kFmtTq2][di.device].load(std::memory_order_acquire)) {
+  if (!configured[kv][di.device].load(std::memory_order_acquire)) {
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kMoeSmemBudget))))
       return TQ1_ERR_CUDA;
     // Up to three CTAs share an SM: the largest shared-memory carveout.
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
       return TQ1_ERR_CUDA;
-    configured[fmt == kFmtTq2][di.device].store(true, std::memory_order_release);
+    configured[kv][di.device].store(true, std::memory_order_release);
   }
   // Upper bound on the tasks: every pair on its own expert.
   const int64_t max_tasks = std::min<int64_t>(pairs, n_experts) * plan.row_blocks +

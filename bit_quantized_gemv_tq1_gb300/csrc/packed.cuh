@@ -156,88 +156,109 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
-// d_w * sum_j d_a[j] * I_j for one packed block against one column record.
-__device__ __forceinline__ float packed_dot(const Packed& P, const uint32_t* rec) {
+// The eight chunk sums of one packed block against one column record, as
+// integers: I[j] = kFloatBias + 4^(j mod 4) * I_j, where I_j is chunk j's
+// exact partial sum (trit * q) (the record's seed carries -4^s * sum q and the
+// bias).  Both the fp32 mat-vec and the integer-partials debug mode start from
+// these sums.
+__device__ __forceinline__ void packed_sums(const Packed& P, const uint32_t* rec, int (&I)[8]) {
   const int4 s0 = *reinterpret_cast<const int4*>(rec + 72);
   const int4 s1 = *reinterpret_cast<const int4*>(rec + 76);
-  int I0 = s0.x, I1 = s0.y, I2 = s0.z, I3 = s0.w, I4 = s1.x, I5 = s1.y, I6 = s1.z, I7 = s1.w;
+  I[0] = s0.x; I[1] = s0.y; I[2] = s0.z; I[3] = s0.w;
+  I[4] = s1.x; I[5] = s1.y; I[6] = s1.z; I[7] = s1.w;
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     const uint4 qa = *reinterpret_cast<const uint4*>(rec + 8 * w);
     const uint4 qb = *reinterpret_cast<const uint4*>(rec + 8 * w + 4);
-    I0 = dp4a_us(P.a[w] & 0x03030303u, qa.x, I0);
-    I1 = dp4a_us(P.a[w] & 0x0C0C0C0Cu, qa.y, I1);
-    I2 = dp4a_us(P.a[w] & 0x30303030u, qa.z, I2);
-    I3 = dp4a_us(P.a[w] & 0xC0C0C0C0u, qa.w, I3);
-    I4 = dp4a_us(P.b[w] & 0x03030303u, qb.x, I4);
-    I5 = dp4a_us(P.b[w] & 0x0C0C0C0Cu, qb.y, I5);
-    I6 = dp4a_us(P.b[w] & 0x30303030u, qb.z, I6);
-    I7 = dp4a_us(P.b[w] & 0xC0C0C0C0u, qb.w, I7);
+    I[0] = dp4a_us(P.a[w] & 0x03030303u, qa.x, I[0]);
+    I[1] = dp4a_us(P.a[w] & 0x0C0C0C0Cu, qa.y, I[1]);
+    I[2] = dp4a_us(P.a[w] & 0x30303030u, qa.z, I[2]);
+    I[3] = dp4a_us(P.a[w] & 0xC0C0C0C0u, qa.w, I[3]);
+    I[4] = dp4a_us(P.b[w] & 0x03030303u, qb.x, I[4]);
+    I[5] = dp4a_us(P.b[w] & 0x0C0C0C0Cu, qb.y, I[5]);
+    I[6] = dp4a_us(P.b[w] & 0x30303030u, qb.z, I[6]);
+    I[7] = dp4a_us(P.b[w] & 0xC0C0C0C0u, qb.w, I[7]);
   }
-  const float4 a0 = *reinterpret_cast<const float4*>(rec + 64);
-  const float4 a1 = *reinterpret_cast<const float4*>(rec + 68);
-  float s = a0.x * unbias(I0);
-  s = fmaf(a0.y, unbias(I1), s);
-  s = fmaf(a0.z, unbias(I2), s);
-  s = fmaf(a0.w, unbias(I3), s);
-  s = fmaf(a1.x, unbias(I4), s);
-  s = fmaf(a1.y, unbias(I5), s);
-  s = fmaf(a1.z, unbias(I6), s);
-  s = fmaf(a1.w, unbias(I7), s);
-  return s * P.dw;
 }
 
-// packed_dot for two blocks of the same block column (two rows) against one
+// packed_sums for two blocks of the same block column (two rows) against one
 // column record: every record word read from shared memory serves both rows,
-// so a lane needs half the record bytes per row.  Each row's arithmetic is
-// exactly packed_dot's (same integer sums, same fp32 operation order).
-__device__ __forceinline__ void packed_dot2(const Packed& P, const Packed& Q, const uint32_t* rec, float& sp,
-                                            float& sq) {
+// so a lane needs half the record bytes per row.  Each row's sums are exactly
+// packed_sums'.
+__device__ __forceinline__ void packed_sums2(const Packed& P, const Packed& Q, const uint32_t* rec, int (&I)[8],
+                                             int (&J)[8]) {
   const int4 s0 = *reinterpret_cast<const int4*>(rec + 72);
   const int4 s1 = *reinterpret_cast<const int4*>(rec + 76);
-  int I0 = s0.x, I1 = s0.y, I2 = s0.z, I3 = s0.w, I4 = s1.x, I5 = s1.y, I6 = s1.z, I7 = s1.w;
-  int J0 = s0.x, J1 = s0.y, J2 = s0.z, J3 = s0.w, J4 = s1.x, J5 = s1.y, J6 = s1.z, J7 = s1.w;
+  I[0] = s0.x; I[1] = s0.y; I[2] = s0.z; I[3] = s0.w;
+  I[4] = s1.x; I[5] = s1.y; I[6] = s1.z; I[7] = s1.w;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) J[j] = I[j];
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     const uint4 qa = *reinterpret_cast<const uint4*>(rec + 8 * w);
     const uint4 qb = *reinterpret_cast<const uint4*>(rec + 8 * w + 4);
-    I0 = dp4a_us(P.a[w] & 0x03030303u, qa.x, I0);
-    J0 = dp4a_us(Q.a[w] & 0x03030303u, qa.x, J0);
-    I1 = dp4a_us(P.a[w] & 0x0C0C0C0Cu, qa.y, I1);
-    J1 = dp4a_us(Q.a[w] & 0x0C0C0C0Cu, qa.y, J1);
-    I2 = dp4a_us(P.a[w] & 0x30303030u, qa.z, I2);
-    J2 = dp4a_us(Q.a[w] & 0x30303030u, qa.z, J2);
-    I3 = dp4a_us(P.a[w] & 0xC0C0C0C0u, qa.w, I3);
-    J3 = dp4a_us(Q.a[w] & 0xC0C0C0C0u, qa.w, J3);
-    I4 = dp4a_us(P.b[w] & 0x03030303u, qb.x, I4);
-    J4 = dp4a_us(Q.b[w] & 0x03030303u, qb.x, J4);
-    I5 = dp4a_us(P.b[w] & 0x0C0C0C0Cu, qb.y, I5);
-    J5 = dp4a_us(Q.b[w] & 0x0C0C0C0Cu, qb.y, J5);
-    I6 = dp4a_us(P.b[w] & 0x30303030u, qb.z, I6);
-    J6 = dp4a_us(Q.b[w] & 0x30303030u, qb.z, J6);
-    I7 = dp4a_us(P.b[w] & 0xC0C0C0C0u, qb.w, I7);
-    J7 = dp4a_us(Q.b[w] & 0xC0C0C0C0u, qb.w, J7);
+    I[0] = dp4a_us(P.a[w] & 0x03030303u, qa.x, I[0]);
+    J[0] = dp4a_us(Q.a[w] & 0x03030303u, qa.x, J[0]);
+    I[1] = dp4a_us(P.a[w] & 0x0C0C0C0Cu, qa.y, I[1]);
+    J[1] = dp4a_us(Q.a[w] & 0x0C0C0C0Cu, qa.y, J[1]);
+    I[2] = dp4a_us(P.a[w] & 0x30303030u, qa.z, I[2]);
+    J[2] = dp4a_us(Q.a[w] & 0x30303030u, qa.z, J[2]);
+    I[3] = dp4a_us(P.a[w] & 0xC0C0C0C0u, qa.w, I[3]);
+    J[3] = dp4a_us(Q.a[w] & 0xC0C0C0C0u, qa.w, J[3]);
+    I[4] = dp4a_us(P.b[w] & 0x03030303u, qb.x, I[4]);
+    J[4] = dp4a_us(Q.b[w] & 0x03030303u, qb.x, J[4]);
+    I[5] = dp4a_us(P.b[w] & 0x0C0C0C0Cu, qb.y, I[5]);
+    J[5] = dp4a_us(Q.b[w] & 0x0C0C0C0Cu, qb.y, J[5]);
+    I[6] = dp4a_us(P.b[w] & 0x30303030u, qb.z, I[6]);
+    J[6] = dp4a_us(Q.b[w] & 0x30303030u, qb.z, J[6]);
+    I[7] = dp4a_us(P.b[w] & 0xC0C0C0C0u, qb.w, I[7]);
+    J[7] = dp4a_us(Q.b[w] & 0xC0C0C0C0u, qb.w, J[7]);
   }
+}
+
+// d_w * sum_j d_a[j] * I_j from packed_sums' integers: kFloatBias + 4^s * I_j
+// is the bit pattern of 1.5 * 2^23 + 4^s * I_j, one subtraction gives
+// 4^s * I_j exactly, and the record's chunk scale is d_a / 4^s.
+__device__ __forceinline__ float packed_scale(const int (&I)[8], const uint32_t* rec, float dw) {
   const float4 a0 = *reinterpret_cast<const float4*>(rec + 64);
   const float4 a1 = *reinterpret_cast<const float4*>(rec + 68);
-  float s = a0.x * unbias(I0);
-  s = fmaf(a0.y, unbias(I1), s);
-  s = fmaf(a0.z, unbias(I2), s);
-  s = fmaf(a0.w, unbias(I3), s);
-  s = fmaf(a1.x, unbias(I4), s);
-  s = fmaf(a1.y, unbias(I5), s);
-  s = fmaf(a1.z, unbias(I6), s);
-  s = fmaf(a1.w, unbias(I7), s);
-  float u = a0.x * unbias(J0);
-  u = fmaf(a0.y, unbias(J1), u);
-  u = fmaf(a0.z, unbias(J2), u);
-  u = fmaf(a0.w, unbias(J3), u);
-  u = fmaf(a1.x, unbias(J4), u);
-  u = fmaf(a1.y, unbias(J5), u);
-  u = fmaf(a1.z, unbias(J6), u);
-  u = fmaf(a1.w, unbias(J7), u);
-  sp = s * P.dw;
-  sq = u * Q.dw;
+  float s = a0.x * unbias(I[0]);
+  s = fmaf(a0.y, unbias(I[1]), s);
+  s = fmaf(a0.z, unbias(I[2]), s);
+  s = fmaf(a0.w, unbias(I[3]), s);
+  s = fmaf(a1.x, unbias(I[4]), s);
+  s = fmaf(a1.y, unbias(I[5]), s);
+  s = fmaf(a1.z, unbias(I[6]), s);
+  s = fmaf(a1.w, unbias(I[7]), s);
+  return s * dw;
+}
+
+// The exact partial I_j of chunk j from packed_sums' integer (4^s * I_j is a
+// multiple of 4^s, so the arithmetic shift is exact).
+__device__ __forceinline__ int packed_partial(int v, int j) { return (v - kFloatBias) >> (2 * (j & 3)); }
+
+// Store a block's eight exact partials (int32, 16-byte aligned destination).
+__device__ __forceinline__ void store_partials(int32_t* dst, const int (&I)[8]) {
+  reinterpret_cast<int4*>(dst)[0] =
+      make_int4(packed_partial(I[0], 0), packed_partial(I[1], 1), packed_partial(I[2], 2), packed_partial(I[3], 3));
+  reinterpret_cast<int4*>(dst)[1] =
+      make_int4(packed_partial(I[4], 4), packed_partial(I[5], 5), packed_partial(I[6], 6), packed_partial(I[7], 7));
+}
+
+// d_w * sum_j d_a[j] * I_j for one packed block against one column record.
+__device__ __forceinline__ float packed_dot(const Packed& P, const uint32_t* rec) {
+  int I[8];
+  packed_sums(P, rec, I);
+  return packed_scale(I, rec, P.dw);
+}
+
+// packed_dot for two rows of the same block column (one record read for both).
+__device__ __forceinline__ void packed_dot2(const Packed& P, const Packed& Q, const uint32_t* rec, float& sp,
+                                            float& sq) {
+  int I[8], J[8];
+  packed_sums2(P, Q, rec, I, J);
+  sp = packed_scale(I, rec, P.dw);
+  sq = packed_scale(J, rec, Q.dw);
 }
 
 // Quantise 32 fp32 activations (16-byte aligned, global) to one Q8_1 chunk

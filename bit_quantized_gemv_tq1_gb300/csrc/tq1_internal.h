@@ -32,15 +32,17 @@ int launch_quantize_acts(const float* x, uint8_t* q8, int64_t t, int64_t k, cuda
 int launch_mmv(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int64_t n, int64_t k, int64_t t,
                cudaStream_t s, unsigned* status, const float* res = nullptr, int fmt = 0);
 
-// Decode-path kernel for 1 <= t <= 4 columns.  Returns TQ1_ERR_UNSUPPORTED
+// Decode-path kernel for 1 <= t <= 8 columns.  Returns TQ1_ERR_UNSUPPORTED
 // without launching when the shape does not fit its staging.
 // With `x` (fp32 activations [t][k]) the kernel quantises them to Q8_1 in its
 // prologue and `q8` is unused.
 // `inject_timeout` (test hook): CTA 0 issues no copy for its first row group,
 // so its waits give up and the call reports a timeout.
+// With `part` (int32 [t][n][k/32], y unused) the kernel stores its exact
+// per-chunk integer partials instead of the fp32 outputs.
 int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
                      unsigned* status, const float* res = nullptr, const float* x = nullptr, int fmt = 0,
-                     int inject_timeout = 0);
+                     int inject_timeout = 0, int32_t* part = nullptr);
 
 // Expert-routed mat-vec over a compacted routing table in `ws` (general
 // dp4a kernel).
@@ -92,11 +94,13 @@ bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoeP
 // (pair, row range) reads its expert id itself.  `plan` gives the rows per
 // CTA and the row ranges per pair.
 bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan, int fmt = 0);
+// With `part` (int32 [pairs][n][k/32], y unused) both kernels store their
+// exact per-chunk integer partials instead of the fp32 outputs.
 int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
                       int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
-                      unsigned* status, int act_div, int fmt = 0);
+                      unsigned* status, int act_div, int fmt = 0, int32_t* part = nullptr);
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
-                     unsigned* status, int act_div, int fmt = 0);
+                     unsigned* status, int act_div, int fmt = 0, int32_t* part = nullptr);
 
 }  // namespace tq1

@@ -73,7 +73,8 @@ enum tq1_status {
   TQ1_ERR_BAD_ID = -8       /* a routing id was outside [0, n_experts) (device status) */
 };
 
-/* Text for a status code (static storage). */
+/* Text for a status code (static storage).  No passage: a convention of this
+ * library (the pages define no API). */
 const char* tq1_status_string(int status);
 
 /* Library version, e.g. "0.1.0". */
@@ -81,13 +82,13 @@ const char* tq1_version(void);
 
 /*
  * Test hook for the error path of the bounded transfer waits.  The next
- * tq1_mmv / tq1_mmv_add / tq2_mmv / tq2_mmv_add call that runs the decode
- * kernel (1 <= t <= 8) has its first CTA issue no copy (and no byte count)
- * for its first 4-row group, so every wait on that group gives up after about
- * 2 s: the call then reports TQ1_ERR_TIMEOUT through tq1_sync_status, its
- * outputs are unspecified, and the device and the library stay usable.  The
- * hook is one-shot: the call that consumes it clears it.  Nothing faults,
- * traps or hangs.
+ * tq1_mmv / tq1_mmv_add / tq2_mmv / tq2_mmv_add call consumes the hook,
+ * whichever kernel it runs; when that call runs the decode kernel
+ * (1 <= t <= 8), its first CTA issues no copy (and no byte count) for its
+ * first 4-row group, so every wait on that group gives up after about 2 s:
+ * the call then reports TQ1_ERR_TIMEOUT through tq1_sync_status, its outputs
+ * are unspecified, and the device and the library stay usable.  Nothing
+ * faults, traps or hangs.  No passage: a convention of this library.
  */
 void tq1_debug_inject_wait_timeout(void);
 
@@ -165,8 +166,14 @@ int tq1_mmv_add(const void* blocks, const void* q8, const float* res, float* y, 
 
 /*
  * Debug entry: the exact integer partials part[c][r][j] = I_j (int32,
- * [t][n][k/32]) that tq1_mmv scales, for any t (computed in slices of up to
- * 32 columns by the general dp4a kernel).  Bit-exact by construction.
+ * [t][n][k/32]) that tq1_mmv scales, for any t.  For 1 <= t <= 8 they come
+ * from the decode kernel itself (its expansion and dp4a sums, stored before
+ * scaling; shapes whose staging does not fit it take the general kernel),
+ * for larger t from the general dp4a kernel in slices of up to 32 columns.
+ * Bit-exact by construction.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Acceptance criteria" (the new
+ * kernel checked case by case against a CPU reference), and the per-32-block
+ * integer dot product of "Current behavior" that the kernels compute.
  */
 int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,
                      void* stream);
@@ -196,7 +203,11 @@ int tq1_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void
                  int out_f16, void* stream);
 
 /*
- * Workspace bytes tq1_mmv_id needs for n_experts experts and t*top_k routed pairs.
+ * Workspace bytes tq1_mmv_id needs for n_experts experts and t*top_k routed
+ * pairs (the compacted routing table: n_active, expert bounds, active
+ * experts, sorted pairs, task offsets).
+ * Source: AMD-Ecosystem/llama.cpp PR #76, "Summary" (ids -> expert_bounds ->
+ * compacted grid: the table this workspace holds).
  */
 size_t tq1_mmv_id_workspace_size(int64_t n_experts, int64_t t, int64_t top_k);
 
@@ -234,6 +245,24 @@ int tq1_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q
                      int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Debug entry: the exact integer partials part[c][s][r][j] = I_j (int32,
+ * [t][top_k][n][k/32]) that tq1_mmv_id / tq2_mmv_id scale, from the routed
+ * decode kernels themselves (their expansion and dp4a sums, stored before
+ * scaling): direct mode for up to 32 routed pairs, the compacted mode above.
+ * Arguments, workspace and errors as tq1_mmv_id (part replaces y); shapes
+ * that only the general kernel can stage return TQ1_ERR_UNSUPPORTED.
+ * Source: AMD-Ecosystem/llama.cpp PR #76, "Summary" (the expert-routed grid
+ * these kernels run); PrismML-Eng/llama.cpp issue #139, "Acceptance criteria"
+ * (MUL_MAT_ID checked against a CPU reference).
+ */
+int tq1_mmv_id_partials(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids,
+                        int32_t* part, int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes,
+                        void* stream);
+int tq2_mmv_id_partials(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids,
+                        int32_t* part, int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
  * tq1_mmv_id without a workspace argument, for callers that cannot allocate
  * device memory (inside a stream capture, under a fixed memory budget, in a
  * latency-critical loop, or from plain C with no allocator at hand).  The
@@ -254,7 +283,8 @@ int tq1_mmv_id_noalloc(const void* expert_blocks, int64_t n_experts, const void*
 /*
  * Synchronise `stream`, then return and clear the device status word:
  * TQ1_OK, TQ1_ERR_TIMEOUT or TQ1_ERR_BAD_ID (or TQ1_ERR_CUDA if the stream
- * itself reported an error).
+ * itself reported an error).  No passage: a convention of this library (the
+ * pages define no error reporting).
  */
 int tq1_sync_status(void* stream);
 

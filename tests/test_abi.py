@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     for want in ("tq1_quantize_rows", "q8_1_quantize_acts", "tq1_mmv", "tq1_mmv_id", "tq1_mmv_partials",
                  "tq1_mmv_id_workspace_size", "tq1_sync_status", "tq1_status_string", "tq1_dequantize_rows",
                  "tq1_get_rows", "tq2_quantize_rows", "tq2_mmv", "tq2_mmv_partials", "tq2_blocks_bytes", "tq2_dequantize_rows", "tq2_get_rows", "tq2_mmv_id",
-                 "tq2_mmv_id_slots", "tq2_mmv_f32", "tq2_mmv_add"):
+                 "tq2_mmv_id_slots", "tq2_mmv_f32", "tq2_mmv_add", "tq1_mmv_id_partials",
+                 "tq2_mmv_id_partials", "tq1_mmv_id_noalloc"):
         assert want in names
 
 
@@ -150,3 +151,22 @@ def test_tq2_fused_entry_host_checks(lib):
     assert lib.tq2_mmv_f32(FAKE, None, FAKE, 10, 256, 1, None) == -1
     assert lib.tq2_mmv_add(FAKE, FAKE, None, FAKE, 10, 256, 1, None) == -1
     assert lib.tq2_mmv_add(FAKE, FAKE, FAKE + 4, FAKE, 10, 256, 1, None) == -3
+
+
+def test_mmv_id_partials_host_checks(lib):
+    ws = L.tq1_mmv_id_workspace_size(8, 2, 2)
+    for fn in (lib.tq1_mmv_id_partials, lib.tq2_mmv_id_partials):
+        assert fn(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 2, 2, FAKE, ws - 1, None) == -5
+        assert fn(FAKE, 8, FAKE, FAKE, None, 16, 256, 2, 2, FAKE, ws, None) == -1
+        assert fn(FAKE, 8, FAKE, FAKE, FAKE + 4, 16, 256, 2, 2, FAKE, ws, None) == -3
+        assert fn(FAKE, 0, FAKE, FAKE, FAKE, 16, 256, 2, 2, FAKE, ws, None) == -2
+        assert fn(FAKE, 8, FAKE, FAKE, FAKE, 16, 256, 0, 2, FAKE, ws, None) == 0
+
+
+def test_no_alloc_rejects_calls_beyond_its_table(lib):
+    # tq1_mmv_id_noalloc's fixed routing table holds 1024 experts and 16384
+    # routed pairs; larger calls are refused on the host, before any launch.
+    fake = 1 << 20
+    assert lib.tq1_mmv_id_noalloc(fake, 1025, fake, fake, fake, 16, 256, 1, 1, None) == -5
+    assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 4097, 4, None) == -5
+    assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 1, 1 << 40, None) == -5

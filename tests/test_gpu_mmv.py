@@ -135,22 +135,72 @@ def test_extreme_partials():
     assert part[0, 0, 0] == 4064 and part[0, 1, 0] == -4064
 
 
-def test_one_hot_layout_probes():
-    # Weight element e = +1 of row e, everything else 0; activation one-hot at
-    # e' in column e'.  y[e'][e] != 0 exactly when e == e'.  Covers all 256.
-    k = 256
+def _one_hot_columns(k, cols):
+    x = np.zeros((len(cols), k), np.float32)
+    x[np.arange(len(cols)), cols] = 1.0
+    return x
+
+
+# Layout probes on every route: weight row e holds +1 at element e and zeros
+# elsewhere; activation column c is one-hot at element e'_c.  y[c][e] != 0
+# exactly when e == e'_c, and (where partials exist) the only nonzero partial
+# of row e'_c is 127 at chunk e'_c / 32.  A transposed element order, a wrong
+# digit or a chunk mapped to the wrong activation word fails these.
+# (k, t, cols): k = 256 with t = 32 runs the general kernel (k not a multiple
+# of 2048); k = 2048 with t <= 8 the decode rungs; k = 2048 with t >= 9 the
+# tensor-core tile path.  cols: every element of the first and the last block.
+ONE_HOT = [(256, 32, range(256)), (2048, 1, list(range(0, 256, 5)) + list(range(1792, 2048, 7))),
+           (2048, 2, list(range(256)) + list(range(1792, 2048))), (2048, 4, range(0, 256, 3)),
+           (2048, 8, list(range(256)) + list(range(1792, 2048))), (2048, 32, list(range(256)) + list(range(1792, 2048)))]
+
+
+@pytest.mark.parametrize("k,t,cols", ONE_HOT, ids=[f"k{k}-t{t}" for k, t, _ in ONE_HOT])
+def test_one_hot_layout_probes(k, t, cols):
+    cols = np.array(list(cols))
+    cols = np.concatenate([cols, cols[:(-len(cols)) % t]])  # whole groups of t columns
     w = np.eye(k, dtype=np.float32)
-    x = np.eye(k, dtype=np.float32)[:32]
     blocks = G.quantize_rows(w)
-    for c0 in range(0, k, 32):
-        xs = np.eye(k, dtype=np.float32)[c0:c0 + 32]
-        y = G.mmv(blocks, G.quantize_acts(xs), k, k, 32)
-        nz = y != 0
-        expect = np.zeros_like(nz)
-        for c in range(32):
-            expect[c, c0 + c] = True
-        np.testing.assert_array_equal(nz, expect)
-    del x
+    for g in range(0, len(cols), t):
+        cg = cols[g:g + t]
+        q8 = G.quantize_acts(_one_hot_columns(k, cg))
+        y = G.mmv(blocks, q8, k, k, t)
+        expect = np.zeros((t, k), bool)
+        expect[np.arange(t), cg] = True
+        np.testing.assert_array_equal(y != 0, expect)
+        if t <= 8:
+            part = G.partials(blocks, q8, k, k, t)
+            ref = np.zeros_like(part)
+            ref[np.arange(t), cg, cg // 32] = 127
+            np.testing.assert_array_equal(part, ref)
+
+
+def test_decode_kernel_partials_c3_whole_ctas():
+    """The decode kernel's own integer partials (every rung, pair mode
+    included) against the oracle's, bit for bit, on whole CTAs of config 3's
+    shape (N=5120, K=6144) at t = 1..8."""
+    p = synth.config_matvec("c3")
+    blocks = G.quantize_rows(p.w)
+    rows = _cta_rows(p.n)
+    ob = orc.tq1_encode_rows(p.w[rows])
+    for t in range(1, 9):
+        x = p.x[:t]
+        q8 = G.quantize_acts(x)
+        part = G.partials(blocks, q8, p.n, p.k, t)
+        np.testing.assert_array_equal(part[:, rows], orc.mmv_partials(ob, orc.q8_1_quantize(x), rows.size, p.k, t))
+
+
+def test_decode_kernel_partials_several_rounds():
+    """Partials through the decode kernel where a CTA's rows take a second
+    slab round and a paired lane has no second row (N=5700, K=6144)."""
+    p = synth.matvec(5700, 6144, 8, p_zero=0.4, seed=58)
+    blocks = G.quantize_rows(p.w)
+    rows = _cta_rows(p.n)
+    ob = orc.tq1_encode_rows(p.w[rows])
+    for t in (1, 2, 3, 5, 8):
+        x = p.x[:t]
+        q8 = G.quantize_acts(x)
+        part = G.partials(blocks, q8, p.n, p.k, t)
+        np.testing.assert_array_equal(part[:, rows], orc.mmv_partials(ob, orc.q8_1_quantize(x), rows.size, p.k, t))
 
 
 @pytest.mark.parametrize("t", [2, 3, 4, 8, 32])

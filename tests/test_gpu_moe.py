@@ -28,6 +28,36 @@ def _mmv_id(blocks, m, ids, q8, fill=float("nan")):
     return y, L.tq1_sync_status()
 
 
+def _mmv_id_partials(blocks, m, ids, q8, fmt="tq1"):
+    L = G.lib()
+    t = G.torch()
+    ws_bytes = L.tq1_mmv_id_workspace_size(m.n_experts, m.t, m.top_k)
+    ws = t.zeros(ws_bytes, dtype=t.uint8, device="cuda")
+    part = t.full((m.t, m.top_k, m.n, m.k // 32), -2 ** 31, dtype=t.int32, device="cuda")
+    fn = L.tq1_mmv_id_partials if fmt == "tq1" else L.tq2_mmv_id_partials
+    fn(blocks, m.n_experts, q8, G.dev(ids.astype(np.int32)), part, m.n, m.k, m.t, m.top_k, ws)
+    assert L.tq1_sync_status() == 0
+    return G.host(part)
+
+
+def _oracle_id_partials(m, ids, rows, fmt="tq1"):
+    """Per routed (token, slot) pair: the oracle's dense partials of that
+    expert's sampled rows against the token's activations (the routed
+    product reduces to per-expert mat-vecs)."""
+    enc = orc.tq1_encode_rows if fmt == "tq1" else orc.tq2_encode_rows
+    dense = orc.mmv_partials if fmt == "tq1" else orc.tq2_mmv_partials
+    oq = orc.q8_1_quantize(m.x).reshape(m.t, -1)
+    cache = {}
+    out = np.zeros((m.t, m.top_k, len(rows), m.k // 32), np.int32)
+    for c in range(m.t):
+        for s in range(m.top_k):
+            e = int(ids[c, s])
+            if e not in cache:
+                cache[e] = enc(m.expert_weights(e)[rows])
+            out[c, s] = dense(cache[e], oq[c], len(rows), m.k, 1)[0]
+    return out
+
+
 def _oracle_blocks(m, experts):
     eb = m.n * (m.k // 256) * 54
     out = np.zeros((m.n_experts, eb), np.uint8)
@@ -48,6 +78,18 @@ def test_config4_sampled_rows(t):
     rows = np.unique(np.concatenate([[0, m.n - 1], np.random.default_rng(t).integers(0, m.n, 62)]))
     ref = orc.mmv_id_f64_rows(ob, m.n_experts, orc.q8_1_quantize(m.x), m.ids, m.n, m.k, m.t, m.top_k, rows)
     G.assert_close(G.host(y)[:, :, rows], ref)
+
+
+@pytest.mark.parametrize("t", [1, 32])
+def test_config4_partials_sampled_rows(t):
+    """The routed decode kernels' own integer partials (direct mode at T=1,
+    the compacted mode at T=32) against the oracle's, bit for bit."""
+    m = synth.config_moe(t)
+    blocks = _experts_gpu(m)
+    q8 = G.quantize_acts(m.x)
+    part = _mmv_id_partials(blocks, m, m.ids, q8)
+    rows = np.unique(np.concatenate([[0, 1, m.n - 1], np.random.default_rng(t + 5).integers(0, m.n, 45)]))
+    np.testing.assert_array_equal(part[:, :, rows], _oracle_id_partials(m, m.ids, rows))
 
 
 ROUTINGS = {
@@ -72,6 +114,8 @@ def test_small_routings_full(name):
     ob = _oracle_blocks(m, range(7))
     ref = orc.mmv_id_f64(ob, 7, orc.q8_1_quantize(m.x), ids, m.n, m.k, t, top_k)
     G.assert_close(G.host(y), ref)
+    part = _mmv_id_partials(blocks, m, ids, q8)
+    np.testing.assert_array_equal(part, _oracle_id_partials(m, ids, np.arange(m.n)))
 
 
 def test_many_tokens_one_expert_beyond_32_columns():
@@ -184,10 +228,15 @@ def _tq2_id(blocks, m, ids, q8, slots=False, t=None):
 def test_tq2_config4_sampled_rows(t):
     # Direct mode (t = 1: 8 pairs) and the compacted path (t = 32: 256 pairs).
     m = synth.config_moe(t)
-    y = _tq2_id(_experts_gpu_tq2(m), m, m.ids, G.quantize_acts(m.x))
+    blocks = _experts_gpu_tq2(m)
+    q8 = G.quantize_acts(m.x)
+    y = _tq2_id(blocks, m, m.ids, q8)
     ob = _oracle_blocks_tq2(m, np.unique(m.ids))
     ref = orc.tq2_mmv_id_f64(ob, m.n_experts, orc.q8_1_quantize(m.x), m.ids, m.n, m.k, m.t, m.top_k)
     G.assert_close(y, ref)
+    part = _mmv_id_partials(blocks, m, m.ids, q8, fmt="tq2")
+    rows = np.unique(np.concatenate([[0, m.n - 1], np.random.default_rng(t + 9).integers(0, m.n, 30)]))
+    np.testing.assert_array_equal(part[:, :, rows], _oracle_id_partials(m, m.ids, rows, fmt="tq2"))
 
 
 def test_tq2_routings_long_rows():

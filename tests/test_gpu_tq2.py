@@ -138,6 +138,22 @@ def test_decode_rungs_several_rounds_sampled_rows():
         G.assert_close(y[:, rows], orc.tq2_mmv_f64(ob, orc.q8_1_quantize(x), rows.size, p.k, t))
 
 
+def test_decode_kernel_partials_whole_ctas():
+    """The decode kernel's own integer partials on TQ2_0 weights (every rung)
+    against the oracle's, bit for bit, on whole CTAs of N=5120, K=6144."""
+    p = synth.matvec(5120, 6144, 8, seed=61)
+    blocks = _quantize_tq2(p.w)
+    ctas = 152
+    bounds = [(p.n * i) // ctas for i in range(ctas + 1)]
+    rows = np.unique(np.concatenate([np.arange(bounds[i], bounds[i + 1]) for i in (0, 75, ctas - 1)]))
+    ob = orc.tq2_encode_rows(p.w[rows])
+    for t in range(1, 9):
+        x = p.x[:t]
+        q8 = G.quantize_acts(x)
+        part = _partials(blocks, q8, p.n, p.k, t)
+        np.testing.assert_array_equal(part[:, rows], orc.tq2_mmv_partials(ob, orc.q8_1_quantize(x), rows.size, p.k, t))
+
+
 def test_determinism():
     p = synth.matvec(700, 4096, 3, seed=4)
     blocks, q8 = _quantize_tq2(p.w), G.quantize_acts(p.x)

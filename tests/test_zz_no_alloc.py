@@ -4,8 +4,9 @@ latency-critical loops, plain C callers without an allocator).  Its routing
 table lives in a fixed array inside the library instead of a caller
 workspace.
 
-Checked through the C ABI against tq1_mmv_id (which takes a workspace) on two
-calls in a row with different routings.  Both calls route more than 32
+Checked through the C ABI against tq1_mmv_id (which takes a workspace) and
+against the oracle's per-slot products, on two calls in a row with different
+routings.  Both calls route more than 32
 (token, slot) pairs, so they go through the compacted routing table that the
 fixed array holds (fewer pairs are served without a table); the second call
 routes to fewer experts than the first, so a table left over from the first
@@ -14,6 +15,7 @@ follows.  This file is collected last on purpose."""
 import numpy as np
 import pytest
 
+from oracle import oracle as orc
 from bit_quantized_gemv_tq1_gb300 import synth
 from tests import gpu_util as G
 
@@ -53,6 +55,8 @@ def test_no_alloc_matches_workspace_entry_on_two_calls():
     assert m.t * m.top_k > 32  # the routing-table path
     blocks = _experts_gpu(m)
     q8 = G.quantize_acts(m.x)
+    oq = orc.q8_1_quantize(m.x)
+    ob = np.stack([orc.tq1_encode_rows(m.expert_weights(e)).reshape(-1) for e in range(m.n_experts)])
     first = m.ids.astype(np.int32)
     # Second call: only seven experts, each token's four ids distinct.
     second = np.array([[c % 3, 3 + c % 2, 5, 6] for c in range(m.t)], dtype=np.int32)
@@ -64,15 +68,8 @@ def test_no_alloc_matches_workspace_entry_on_two_calls():
         got = _no_alloc(L, blocks, m, q8, ids, m.t)
         assert np.isfinite(got).all()
         G.assert_close(got, ref)
+        G.assert_close(got, orc.mmv_id_f64(ob, m.n_experts, oq, ids_np, m.n, m.k, m.t, m.top_k))
     # A decode-sized call (one token, 4 pairs) after the table-sized ones.
     q8_1 = G.quantize_acts(m.x[:1])
     ids = G.dev(first[:1].copy())
     G.assert_close(_no_alloc(L, blocks, m, q8_1, ids, 1), _with_workspace(L, blocks, m, q8_1, ids, 1))
-
-
-def test_no_alloc_rejects_calls_beyond_its_table():
-    lib = G.lib().library()
-    fake = 1 << 20
-    assert lib.tq1_mmv_id_noalloc(fake, 1025, fake, fake, fake, 16, 256, 1, 1, None) == -5
-    assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 4097, 4, None) == -5
-    assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 1, 1 << 40, None) == -5
