@@ -470,23 +470,38 @@ def prefill_bench(lib, L, synth, dev, stream, capture, args) -> dict:
     y = torch.empty((t, n), dtype=torch.float32, device=dev)
     L.q8_1_quantize_acts(x, q8, t, k)
     bp, qp, yp = blocks.data_ptr(), q8.data_ptr(), y.data_ptr()
+    ws_bytes = L.tq1_mmv_workspace_size(n, k, t)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    wsp = ws.data_ptr()
 
-    def calls(s):
+    def calls_ws(s):  # the tcgen05 tile path, scratch in the caller's workspace
+        for l in range(copies):
+            assert lib.tq1_mmv_ws(bp + l * wbytes, qp, None, yp, n, k, t, wsp, ws_bytes, s) == 0
+
+    def calls_noalloc(s):  # tq1_mmv: the warp-level tensor-core rungs in 32-column slices, no workspace
         for l in range(copies):
             assert lib.tq1_mmv(bp + l * wbytes, qp, yp, n, k, t, s) == 0
 
-    g = capture(calls)
-    ms = _time_graph(g, stream, 5) / copies
-    assert lib.tq1_sync_status(stream.cuda_stream) == 0
     flops = 2.0 * n * k * t
     peaks = measured_peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
-    del g, blocks
-    return {"workload": "c5: N=14336 K=4096 T=512", "us_per_call": round(ms * 1e3, 2),
+    g = capture(calls_ws)
+    ms = _time_graph(g, stream, 5) / copies
+    assert lib.tq1_sync_status(stream.cuda_stream) == 0
+    del g
+    g = capture(calls_noalloc)
+    ms_na = _time_graph(g, stream, 3) / copies
+    assert lib.tq1_sync_status(stream.cuda_stream) == 0
+    del g, blocks, ws
+    return {"workload": "c5: N=14336 K=4096 T=512", "entry": "tq1_mmv_ws (tcgen05 tile path)",
+            "workspace_bytes": ws_bytes, "us_per_call": round(ms * 1e3, 2),
             "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
             "tensor_tflops_issued": round(2 * flops / (ms * 1e-3) / 1e12, 1),
             "peak_tflops": peak, "frac": round(flops / (ms * 1e-3) / 1e12 / peak, 4),
-            "note": "tflops counts the method's MACs once; the kernel issues each twice (fp16 hi and lo "
+            "tq1_mmv_no_workspace": {"us_per_call": round(ms_na * 1e3, 2),
+                                     "tflops": round(flops / (ms_na * 1e-3) / 1e12, 1),
+                                     "path": "warp-level tensor-core rungs, 16 slices of 32 columns"},
+            "note": "tflops counts the method's MACs once; the tile kernel issues each twice (fp16 hi and lo "
                     "parts of the activations); peak = measured bf16 dense (fp16 runs at the same rate)"}
 
 
@@ -727,9 +742,12 @@ def run_profile_case(args, local):
         q8 = torch.empty(t * (k // QK8) * Q8_BYTES, dtype=torch.uint8, device=dev)
         y = torch.empty((t, n), dtype=torch.float32, device=dev)
         L.q8_1_quantize_acts(x, q8, t, k)
+        ws_bytes = L.tq1_mmv_workspace_size(n, k, t)  # > 0: the tcgen05 tile path (prefill)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         for i in range(args.profile_calls):
             l = i % copies
-            assert lib.tq1_mmv(blocks.data_ptr() + l * wbytes, q8.data_ptr(), y.data_ptr(), n, k, t, s) == 0
+            assert lib.tq1_mmv_ws(blocks.data_ptr() + l * wbytes, q8.data_ptr(), None, y.data_ptr(), n, k, t,
+                                  ws.data_ptr(), ws_bytes, s) == 0
     elif case.startswith("tq2c2"):
         # TQ2_0 on config 2's shape: tq2c2 (T=1) or tq2c2t<T>.
         c = synth.CONFIGS["c2"]

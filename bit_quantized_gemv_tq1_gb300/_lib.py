@@ -83,6 +83,10 @@ def library() -> ctypes.CDLL:
         lib.tq1_mmv_id.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq1_mmv_id_slots.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq1_mmv_id_noalloc.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P]
+        lib.tq1_mmv_workspace_size.restype = SZ
+        lib.tq1_mmv_workspace_size.argtypes = [I64, I64, I64]
+        lib.tq1_mmv_ws.argtypes = [P, P, P, P, I64, I64, I64, P, SZ, P]
+        lib.tq2_mmv_ws.argtypes = [P, P, P, P, I64, I64, I64, P, SZ, P]
         lib.tq1_mmv_id_partials.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq2_mmv_id_partials.argtypes = [P, I64, P, P, P, I64, I64, I64, I64, P, SZ, P]
         lib.tq1_dequantize_rows.argtypes = [P, P, I64, I64, ctypes.c_int, P]
@@ -93,7 +97,7 @@ def library() -> ctypes.CDLL:
                      "tq1_dequantize_rows", "tq1_get_rows", "tq1_sync_status", "tq2_quantize_rows",
                      "tq2_mmv", "tq2_mmv_partials", "tq2_dequantize_rows", "tq2_get_rows", "tq2_mmv_id",
                      "tq2_mmv_id_slots", "tq2_mmv_f32", "tq2_mmv_add", "tq1_mmv_id_partials",
-                     "tq2_mmv_id_partials"):
+                     "tq2_mmv_id_partials", "tq1_mmv_ws", "tq2_mmv_ws"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -155,6 +159,26 @@ def tq1_mmv_add(blocks, q8, res, y, n: int, k: int, t: int, stream=None) -> None
     """y = res + W x (res may be y itself)."""
     _check(library().tq1_mmv_add(_addr(blocks), _addr(q8), _addr(res), _addr(y), n, k, t, _stream(stream)),
            "tq1_mmv_add")
+
+
+def tq1_mmv_workspace_size(n: int, k: int, t: int) -> int:
+    """Bytes tq1_mmv_ws / tq2_mmv_ws need (0: the call takes the allocation-free kernels)."""
+    return int(library().tq1_mmv_workspace_size(n, k, t))
+
+
+def tq1_mmv_ws(blocks, q8, y, n: int, k: int, t: int, ws, ws_bytes: int | None = None, res=None,
+               stream=None) -> None:
+    """tq1_mmv (res None) or tq1_mmv_add with a caller workspace: the tcgen05 tile path at prefill-sized t."""
+    wsb = ws_bytes if ws_bytes is not None else (0 if ws is None else ws.numel() * ws.element_size())
+    _check(library().tq1_mmv_ws(_addr(blocks), _addr(q8), _addr(res), _addr(y), n, k, t, _addr(ws), wsb,
+                                _stream(stream)), "tq1_mmv_ws")
+
+
+def tq2_mmv_ws(blocks, q8, y, n: int, k: int, t: int, ws, ws_bytes: int | None = None, res=None,
+               stream=None) -> None:
+    wsb = ws_bytes if ws_bytes is not None else (0 if ws is None else ws.numel() * ws.element_size())
+    _check(library().tq2_mmv_ws(_addr(blocks), _addr(q8), _addr(res), _addr(y), n, k, t, _addr(ws), wsb,
+                                _stream(stream)), "tq2_mmv_ws")
 
 
 def tq1_mmv_partials(blocks, q8, part, n: int, k: int, t: int, stream=None) -> None:

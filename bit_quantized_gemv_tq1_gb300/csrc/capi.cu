@@ -17,12 +17,23 @@ namespace tq1 {
 namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxK = 62720;  // activation records of one column must fit the staging budget
-// Columns from which tq1_mmv runs on the tensor cores; fewer columns take the
-// dp4a kernels (measured crossover on GB300 at N=5120, K=6144: the dp4a
-// kernel's cost grows with every column, the tile path's barely does).
-#ifndef TQ1_TILE_MIN_T
-#define TQ1_TILE_MIN_T 9
+// The mat-vec ladder (tq1_mmv and its variants), from the crossovers measured
+// on GB300 at N=5120, K=6144 (us per call in a chain of dependent calls):
+//   t <  kMmaMinT:   the dp4a decode kernel, rungs of 1/2/4/8 columns (its
+//                    cost grows ~1.1-1.5 us per column: 11.7 us at t = 7)
+//   t >= kMmaMinT:   the warp-level tensor-core kernel, rungs of 8/16/24/32
+//                    columns (12.5 us at t = 8, 13.6 at 16, 19.2 at 32), in
+//                    slices of 32 columns above 32
+//   t >= kTileMinT with a caller workspace (tq1_mmv_ws): the tcgen05 tile
+//                    path (prefill)
+// Shapes a kernel cannot stage fall through to the general dp4a kernel.
+#ifndef TQ1_MMA_MIN_T
+#define TQ1_MMA_MIN_T 8
 #endif
+#ifndef TQ1_TILE_MIN_T
+#define TQ1_TILE_MIN_T 33
+#endif
+constexpr int64_t kMmaMinT = TQ1_MMA_MIN_T;
 constexpr int64_t kTileMinT = TQ1_TILE_MIN_T;
 // Routed pairs up to which tq1_mmv_id skips the routing table (each pair's
 // rows are then read once per pair, not once per distinct expert).
@@ -157,15 +168,25 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
   return launch_quantize_acts(x, static_cast<uint8_t*>(q8), t, k, static_cast<cudaStream_t>(stream));
 }
 
+// Workspace bytes the tile path needs for this call (0: the call runs the
+// allocation-free kernels).
+static size_t mmv_ws_bytes(int64_t n, int64_t k, int64_t t, int fmt) {
+  if (n < 1 || t < kTileMinT || k <= 0 || (k % kQK) != 0 || k > kMaxK) return 0;
+  return tile_workspace_bytes(n, k, t, fmt);
+}
+
 static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* part, int64_t n, int64_t k,
-                      int64_t t, void* stream, const float* res = nullptr, int fmt = kFmtTq1) {
+                      int64_t t, void* stream, const float* res = nullptr, int fmt = kFmtTq1, void* ws = nullptr,
+                      size_t ws_bytes = 0) {
   int rc = check_mmv_shape(n, k, t);
   if (rc != TQ1_OK) return rc;
   if (n == 0 || t == 0) return TQ1_OK;
   if (!blocks || !q8 || (!y && !part)) return TQ1_ERR_NULL;
   if (misaligned(blocks) || misaligned(q8) || (y && misaligned(y)) || (part && misaligned(part)) ||
-      (res && misaligned(res)))
+      (res && misaligned(res)) || (ws && misaligned(ws)))
     return TQ1_ERR_ALIGN;
+  const size_t need_ws = y && ws ? mmv_ws_bytes(n, k, t, fmt) : 0;
+  if (need_ws && ws_bytes < need_ws) return TQ1_ERR_WORKSPACE;
   if (k > kMaxK) return TQ1_ERR_UNSUPPORTED;
   unsigned* st = status_ptr();
   if (!st) return TQ1_ERR_CUDA;
@@ -176,14 +197,26 @@ static int mmv_common(const void* blocks, const void* q8, float* y, int32_t* par
   const uint8_t* w = static_cast<const uint8_t*>(blocks);
   const uint8_t* a = static_cast<const uint8_t*>(q8);
   const int64_t q8_row = (k / kQK8) * kQ8Bytes;
-  if (y && t >= kTileMinT) {
-    rc = launch_tile(w, a, y, n, k, t, s, st, res, fmt);
-    if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the dp4a kernels below
+  if (need_ws) {
+    rc = launch_tile(w, a, y, n, k, t, s, st, res, fmt, ws, ws_bytes);
+    if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the kernels below
   }
-  if (t <= 8) {
+  if (t < kMmaMinT && t <= 8) {
     // The decode kernel: fp32 outputs, or (debug entry) its exact partials.
     rc = launch_mmv_small(w, a, y, n, k, t, s, st, res, nullptr, fmt, y ? inject : 0, y ? nullptr : part);
     if (rc != TQ1_ERR_UNSUPPORTED) return rc;  // otherwise the general kernel below
+  } else {
+    // The warp-level tensor-core rungs, 32 columns at a time: fp32 outputs or
+    // (debug entry) their exact partials.
+    bool all = true;
+    for (int64_t c0 = 0; c0 < t && all; c0 += 32) {
+      const int64_t tc = t - c0 < 32 ? t - c0 : 32;
+      rc = launch_mmv_mma(w, a + c0 * q8_row, y ? y + c0 * n : nullptr, part ? part + c0 * n * (k / kQK8) : nullptr,
+                          n, k, tc, s, st, res ? res + c0 * n : nullptr, fmt);
+      if (rc == TQ1_ERR_UNSUPPORTED && c0 == 0) all = false;  // shape too large: the general kernel below
+      else if (rc != TQ1_OK) return rc;
+    }
+    if (all) return TQ1_OK;
   }
   for (int64_t c0 = 0; c0 < t; c0 += 32) {
     const int64_t tc = t - c0 < 32 ? t - c0 : 32;
@@ -240,6 +273,23 @@ int tq2_mmv_add(const void* blocks, const void* q8, const float* res, float* y, 
                 void* stream) {
   if (!res && n > 0 && t > 0 && check_mmv_shape(n, k, t) == TQ1_OK) return TQ1_ERR_NULL;
   return mmv_common(blocks, q8, y, nullptr, n, k, t, stream, res, kFmtTq2);
+}
+
+size_t tq1_mmv_workspace_size(int64_t n, int64_t k, int64_t t) {
+  // The tile path's scratch does not depend on the weight format, nor does
+  // whether it runs (both formats' row strides are multiples of 16 bytes for
+  // the same k).
+  return mmv_ws_bytes(n, k, t, kFmtTq1);
+}
+
+int tq1_mmv_ws(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
+               void* ws, size_t ws_bytes, void* stream) {
+  return mmv_common(blocks, q8, y, nullptr, n, k, t, stream, res, kFmtTq1, ws, ws_bytes);
+}
+
+int tq2_mmv_ws(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
+               void* ws, size_t ws_bytes, void* stream) {
+  return mmv_common(blocks, q8, y, nullptr, n, k, t, stream, res, kFmtTq2, ws, ws_bytes);
 }
 
 int tq1_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t n, int64_t k, int64_t t,

@@ -903,29 +903,18 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, const
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Library-owned pool for the prep kernel's scratch: stream-ordered
-// allocations that keep their memory cached between calls.
-cudaMemPool_t scratch_pool(int dev) {
-  static std::mutex mu;
-  static cudaMemPool_t pools[64] = {};
-  if (dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!pools[dev]) {
-    cudaMemPoolProps props = {};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t p = nullptr;
-    if (!cuda_ok(cudaMemPoolCreate(&p, &props))) return nullptr;
-    uint64_t keep = ~uint64_t{0};
-    if (!cuda_ok(cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep))) return nullptr;
-    pools[dev] = p;
-  }
-  return pools[dev];
+// Scratch of one call: fp16 hi and lo activation rows [t_pad][k] each, then
+// the per-token scales [t_pad], rounded up to 256 bytes.
+template <int TOK>
+size_t tile_scratch_bytes(int64_t k, int64_t t) {
+  const int64_t t_pad = ((t + TOK - 1) / TOK) * TOK;
+  const size_t b = 2 * static_cast<size_t>(t_pad) * k * sizeof(uint16_t) + static_cast<size_t>(t_pad) * sizeof(float);
+  return (b + 255) & ~size_t(255);
 }
 
 template <int TOK, int FMT>
-int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms, cudaStream_t s) {
+int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms, cudaStream_t s, void* ws,
+                    size_t ws_bytes) {
   using C = TileCfg<TOK>;
   const DeviceInfo& di = device_info();
   static std::atomic<bool> configured[64];  // per device (racing threads configure twice: idempotent)
@@ -943,16 +932,12 @@ int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms
   const int nb = a.k / kQK;
   const uint64_t rowbytes = static_cast<uint64_t>(nb) * fmt_block_bytes<FMT>();
   const size_t hilo_bytes = 2 * static_cast<size_t>(a.t_pad) * a.k * sizeof(uint16_t);
-  const size_t ws_bytes = hilo_bytes + static_cast<size_t>(a.t_pad) * sizeof(float);
+  if (ws == nullptr || ws_bytes < tile_scratch_bytes<TOK>(a.k, a.t)) return TQ1_ERR_WORKSPACE;
 
   CUtensorMap tmw;
   if (!make_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, rowbytes, static_cast<uint64_t>(a.n), kWinBytes, kTileRows,
                 CU_TENSOR_MAP_SWIZZLE_NONE))
     return TQ1_ERR_UNSUPPORTED;
-  cudaMemPool_t pool = scratch_pool(di.device);
-  if (!pool) return TQ1_ERR_CUDA;
-  void* ws = nullptr;
-  if (!cuda_ok(cudaMallocFromPoolAsync(&ws, ws_bytes, pool, s))) return TQ1_ERR_CUDA;
   uint16_t* hilo = static_cast<uint16_t*>(ws);
   float* scale = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + hilo_bytes);
   a.scale = scale;
@@ -999,14 +984,12 @@ int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms
     cfg.numAttrs = na;
     if (!cuda_ok(cudaLaunchKernelEx(&cfg, tile_kernel<TOK, FMT>, a, tmw, tmb))) rc = TQ1_ERR_CUDA;
   }
-  // The scratch goes back to the pool once the kernels above have finished.
-  if (!cuda_ok(cudaFreeAsync(ws, s)) && rc == TQ1_OK) rc = TQ1_ERR_CUDA;
   return rc;
 }
 
 template <int FMT>
 int launch_tile_fmt(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t,
-                           cudaStream_t s, unsigned* status, const float* res) {
+                    cudaStream_t s, unsigned* status, const float* res, void* ws, size_t ws_bytes) {
   if (n > (int64_t{1} << 30) || t > (int64_t{1} << 24) || k > (int64_t{1} << 30)) return TQ1_ERR_UNSUPPORTED;
   // The weight map's row stride must be a multiple of 16 bytes.
   if (((k / kQK) * fmt_block_bytes<FMT>()) % 16 != 0) return TQ1_ERR_UNSUPPORTED;
@@ -1018,18 +1001,27 @@ int launch_tile_fmt(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, in
   a.n = static_cast<int>(n);
   a.k = static_cast<int>(k);
   a.t = static_cast<int>(t);
-  if (t <= 8) return launch_tile_tok<8, FMT>(w, q8, a, di.num_sms, s);
-  if (t <= 16) return launch_tile_tok<16, FMT>(w, q8, a, di.num_sms, s);
-  if (t <= 32) return launch_tile_tok<32, FMT>(w, q8, a, di.num_sms, s);
-  return launch_tile_tok<64, FMT>(w, q8, a, di.num_sms, s);
+  if (t <= 8) return launch_tile_tok<8, FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
+  if (t <= 16) return launch_tile_tok<16, FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
+  if (t <= 32) return launch_tile_tok<32, FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
+  return launch_tile_tok<64, FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
 }
 
 }  // namespace
 
 int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                unsigned* status, const float* res, int fmt) {
-  return fmt == kFmtTq2 ? launch_tile_fmt<kFmtTq2>(w, q8, y, n, k, t, s, status, res)
-                        : launch_tile_fmt<kFmtTq1>(w, q8, y, n, k, t, s, status, res);
+                unsigned* status, const float* res, int fmt, void* ws, size_t ws_bytes) {
+  return fmt == kFmtTq2 ? launch_tile_fmt<kFmtTq2>(w, q8, y, n, k, t, s, status, res, ws, ws_bytes)
+                        : launch_tile_fmt<kFmtTq1>(w, q8, y, n, k, t, s, status, res, ws, ws_bytes);
+}
+
+size_t tile_workspace_bytes(int64_t n, int64_t k, int64_t t, int fmt) {
+  if (n < 1 || t < 1 || k < kQK || n > (int64_t{1} << 30) || t > (int64_t{1} << 24) || k > (int64_t{1} << 30)) return 0;
+  if (((k / kQK) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes)) % 16 != 0) return 0;  // the dp4a/mma kernels
+  if (t <= 8) return tile_scratch_bytes<8>(k, t);
+  if (t <= 16) return tile_scratch_bytes<16>(k, t);
+  if (t <= 32) return tile_scratch_bytes<32>(k, t);
+  return tile_scratch_bytes<64>(k, t);
 }
 
 }  // namespace tq1

@@ -44,6 +44,13 @@ int launch_mmv_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
                      unsigned* status, const float* res = nullptr, const float* x = nullptr, int fmt = 0,
                      int inject_timeout = 0, int32_t* part = nullptr);
 
+// 1 <= t <= 32 columns on the warp-level tensor cores (mma.sync, fp16
+// operands exact, fp32 accumulation): y[c][r] (+ res), or the exact int32
+// partials part[c][r][k/32] when `part` is given.  Returns TQ1_ERR_UNSUPPORTED
+// (launching nothing) when the shape does not fit its shared memory.
+int launch_mmv_mma(const uint8_t* w, const uint8_t* q8, float* y, int32_t* part, int64_t n, int64_t k, int64_t t,
+                   cudaStream_t s, unsigned* status, const float* res = nullptr, int fmt = 0);
+
 // Expert-routed mat-vec over a compacted routing table in `ws` (general
 // dp4a kernel).
 // `act_div`: the activation row of routed pair p is p / act_div (top_k: one
@@ -54,9 +61,16 @@ int launch_mmv_id(const uint8_t* w, int64_t n_experts, const uint8_t* q8, float*
 
 // y[c][r] for any t on the tensor cores (tcgen05): 128-row tiles, split-K
 // over a thread-block cluster when the tiles alone cannot fill the GPU.
-// `fmt`: kFmtTq1 or kFmtTq2 weight blocks.
+// `fmt`: kFmtTq1 or kFmtTq2 weight blocks.  `ws` (caller-owned device memory
+// of at least tile_workspace_bytes(n, k, t, fmt) bytes) holds the exact fp16
+// hi/lo split of the activations between the prep and tile kernels
+// (TQ1_ERR_WORKSPACE when absent or too small).  Returns TQ1_ERR_UNSUPPORTED
+// (launching nothing) for shapes the weight tensor map cannot describe.
 int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
-                unsigned* status, const float* res = nullptr, int fmt = 0);
+                unsigned* status, const float* res, int fmt, void* ws, size_t ws_bytes);
+// Scratch bytes of launch_tile for this shape; 0 when the tile path cannot
+// run it (row stride not a multiple of 16 bytes, or sizes out of range).
+size_t tile_workspace_bytes(int64_t n, int64_t k, int64_t t, int fmt);
 
 // Rows of TQ1_0 (fmt kFmtTq1) or TQ2_0 blocks to fp32 (f16 = false) or fp16
 // values: out row i is source row row_ids[i] (row_ids == nullptr: row i).

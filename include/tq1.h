@@ -34,11 +34,10 @@
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller and must be
  *     16-byte aligned (TQ1_ERR_ALIGN otherwise).  The library never
- *     synchronises; work is enqueued on `stream` (a cudaStream_t, NULL for
- *     the legacy default stream) on the current device.  The only memory it
- *     takes is the tensor-core path's activation scratch (the mat-vec entry
- *     points at t >= 9 with k a multiple of 2048), stream-ordered from its
- *     own memory pool (see tq1_mmv).
+ *     synchronises and allocates no device memory; work is enqueued on
+ *     `stream` (a cudaStream_t, NULL for the legacy default stream) on the
+ *     current device.  Scratch, where a path needs any, is a caller-owned
+ *     workspace with a size query (tq1_mmv_ws, tq1_mmv_id).
  *   - Arguments are checked on the host before anything is launched; a
  *     failed check returns its negative code and launches nothing.
  *   - Shapes: k must be a positive multiple of 256; n, t >= 0 (0 means there
@@ -124,15 +123,15 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
  * w = d_w * trit and x = d_a * q, accumulated as
  *   sum_blocks d_w * sum_{chunks j} d_a[j] * I_j,   I_j = sum (trit * q) (exact int32)
  * in fp32.  blocks [n][k/256] TQ1_0, q8 [t][k/32] Q8_1, y fp32 [t][n].
- * t <= 8 runs the byte-major dp4a decode kernel (rungs of 1/2/4/8 columns;
- * shapes whose staging does not fit it take a general dp4a kernel);
- * t >= 9 (prefill included) runs the tensor-core path: a prep kernel splits
- * the activations into exact fp16 hi/lo parts in scratch taken from a
- * library-owned stream-ordered memory pool (cudaMallocFromPoolAsync /
- * cudaFreeAsync on `stream`: no synchronisation, capturable), then a tcgen05
- * kernel contracts them with the expanded weights (k a multiple of 2048;
- * other k stay on the dp4a kernels).  Deterministic: repeated calls give
- * identical bits.
+ * The ladder: t <= 7 runs the byte-major dp4a decode kernel (rungs of
+ * 1/2/4/8 columns); t >= 8 runs the warp-level tensor-core kernel (mma.sync
+ * on exact fp16 operands: d_w*trit and the int8 q, fp32 accumulation of each
+ * 32-element chunk, which is exact) with rungs of 8/16/24/32 token columns,
+ * in slices of 32 columns above 32; shapes either cannot stage take a
+ * general dp4a kernel.  Nothing
+ * is allocated; for prefill-sized t, tq1_mmv_ws with a workspace runs the
+ * tcgen05 tile path instead.  Deterministic: repeated calls give identical
+ * bits.
  * Source: PrismML-Eng/llama.cpp issue #139, "Proposed approach" (a dedicated
  * whole-block kernel that iterates over packed bytes); laddered column
  * counts: Neroued/ninfer issue #293.
@@ -140,12 +139,46 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
 int tq1_mmv(const void* blocks, const void* q8, float* y, int64_t n, int64_t k, int64_t t, void* stream);
 
 /*
+ * Workspace bytes tq1_mmv_ws / tq2_mmv_ws need for an n x k matrix and t
+ * columns: the tcgen05 tile path's exact fp16 hi/lo split of the activations
+ * (2 * 2 * t_pad * k + 4 * t_pad bytes, t_pad = t rounded up to the token
+ * tile, rounded up to 256).  0 when the call takes the allocation-free
+ * kernels (t below the tile path's threshold, or a row stride that is not a
+ * multiple of 16 bytes, i.e. k not a multiple of 2048).
+ * Source: PrismML-Eng/llama.cpp issue #139, "Measured impact" (prefill, pp512,
+ * is the case the dense tensor-core path serves); the workspace itself is a
+ * convention of this library.
+ */
+size_t tq1_mmv_workspace_size(int64_t n, int64_t k, int64_t t);
+
+/*
+ * tq1_mmv / tq1_mmv_add with a caller-owned workspace: where
+ * tq1_mmv_workspace_size(n, k, t) > 0 (prefill-sized t), a prep kernel
+ * splits the activations into exact fp16 hi/lo rows in `ws` and a tcgen05
+ * kernel (A: the weights expanded straight into tensor memory; B: the hi/lo
+ * rows by TMA; fp32 accumulators in tensor memory) contracts them; otherwise
+ * the call equals tq1_mmv (res == NULL) or tq1_mmv_add.  res may be NULL or
+ * y itself.  ws: device, 16-byte aligned, at least
+ * tq1_mmv_workspace_size(n, k, t) bytes (TQ1_ERR_WORKSPACE otherwise; checked
+ * before any launch), or NULL (then the allocation-free kernels run).  The
+ * workspace is in use until the call's kernels finish on `stream`.
+ * tq2_mmv_ws: the same for TQ2_0 weights.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Measured impact" and
+ * "Proposed approach" (prefill through a dedicated whole-block kernel).
+ */
+int tq1_mmv_ws(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
+               void* ws, size_t ws_bytes, void* stream);
+int tq2_mmv_ws(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
+               void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Decode mat-vec straight from fp32 activations: the Q8_1 quantisation of x
- * (the same operations and rounding as q8_1_quantize_acts) runs in the
- * mat-vec kernel's prologue, so a decode step needs one launch per mat-vec
+ * (the same operations and rounding as q8_1_quantize_acts) runs in the dp4a
+ * decode kernel's prologue, so a decode step needs one launch per mat-vec
  * instead of two.  y equals, bit for bit, q8_1_quantize_acts followed by
- * tq1_mmv.  x: fp32 [t][k], device, 16-byte aligned.  1 <= t <= 4 (larger t:
- * TQ1_ERR_UNSUPPORTED; quantise once and call tq1_mmv).  Errors as tq1_mmv.
+ * tq1_mmv (the same decode kernel on the same records).  x: fp32 [t][k],
+ * device, 16-byte aligned.  1 <= t <= 4 (larger t: TQ1_ERR_UNSUPPORTED; quantise
+ * once and call tq1_mmv).  Errors as tq1_mmv.
  * Source: PrismML-Eng/llama.cpp issue #139, "Current behavior" (activations
  * are quantised to Q8_1 before the MMVQ kernel: here inside it).
  */
@@ -166,11 +199,11 @@ int tq1_mmv_add(const void* blocks, const void* q8, const float* res, float* y, 
 
 /*
  * Debug entry: the exact integer partials part[c][r][j] = I_j (int32,
- * [t][n][k/32]) that tq1_mmv scales, for any t.  For 1 <= t <= 8 they come
- * from the decode kernel itself (its expansion and dp4a sums, stored before
- * scaling; shapes whose staging does not fit it take the general kernel),
- * for larger t from the general dp4a kernel in slices of up to 32 columns.
- * Bit-exact by construction.
+ * [t][n][k/32]) that tq1_mmv scales, for any t, from the kernel tq1_mmv runs
+ * for that t: the dp4a decode kernel at t <= 7 (its dp4a sums, stored before
+ * scaling), the tensor-core rungs at t >= 8 (each chunk's accumulator with
+ * the unscaled trit table, which is exactly I_j); shapes neither can stage
+ * take the general kernel.  Bit-exact by construction.
  * Source: PrismML-Eng/llama.cpp issue #139, "Acceptance criteria" (the new
  * kernel checked case by case against a CPU reference), and the per-32-block
  * integer dot product of "Current behavior" that the kernels compute.
@@ -297,11 +330,11 @@ int tq1_sync_status(void* stream);
  *
  * tq2_mmv: y[c][r] = sum_k w[r][k] * x[c][k] for TQ2_0 blocks [n][k/256] and
  * Q8_1 q8 [t][k/32], accumulated exactly as tq1_mmv (exact int32 per-32
- * partials, fp32 scale-and-sum per block).  t <= 8 runs the decode kernel
- * (the codes already are its packed-digit registers: masked dp4a, no
- * expansion); larger t runs the tensor-core tile path when k is a multiple
- * of 2048 (activation scratch as tq1_mmv), else the general dp4a kernel in
- * chunks of up to 32 columns.  Deterministic.
+ * partials, fp32 scale-and-sum per block).  The same ladder as tq1_mmv:
+ * t <= 7 runs the decode kernel (the codes already are its packed-digit
+ * registers: masked dp4a, no expansion), t >= 8 the warp-level tensor-core
+ * rungs (the codes select fp16 trit values by a byte permute), with the
+ * tcgen05 tile path through tq2_mmv_ws.  Deterministic; allocates nothing.
  *
  * tq2_mmv_partials: the exact int32 partials part[c][r][k/32] of tq2_mmv
  * (debug, as tq1_mmv_partials).

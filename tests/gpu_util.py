@@ -55,6 +55,20 @@ def mmv(blocks, q8, n, k, t):
     return host(y)
 
 
+def mmv_ws(blocks, q8, n, k, t, fmt="tq1", res=None):
+    """tq1_mmv_ws / tq2_mmv_ws with a workspace of the size the library asks
+    for (the tcgen05 tile path wherever that size is nonzero)."""
+    L = lib()
+    tt = torch()
+    ws_bytes = L.tq1_mmv_workspace_size(n, k, t)
+    ws = tt.empty(max(ws_bytes, 16), dtype=tt.uint8, device="cuda")
+    y = tt.full((t, n), float("nan"), dtype=tt.float32, device="cuda")
+    fn = L.tq1_mmv_ws if fmt == "tq1" else L.tq2_mmv_ws
+    fn(blocks, q8, y, n, k, t, ws, ws_bytes, res=res)
+    assert L.tq1_sync_status() == 0
+    return host(y)
+
+
 def partials(blocks, q8, n, k, t):
     L = lib()
     p = torch().full((t, n, k // QK8), -2 ** 31, dtype=torch().int32, device="cuda")

@@ -170,3 +170,19 @@ def test_no_alloc_rejects_calls_beyond_its_table(lib):
     assert lib.tq1_mmv_id_noalloc(fake, 1025, fake, fake, fake, 16, 256, 1, 1, None) == -5
     assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 4097, 4, None) == -5
     assert lib.tq1_mmv_id_noalloc(fake, 8, fake, fake, fake, 16, 256, 1, 1 << 40, None) == -5
+
+
+def test_mmv_ws_host_checks(lib):
+    # The tile path's workspace: asked for only where the tile path runs (k a
+    # multiple of 2048, t at its threshold or above), refused when too small
+    # or misaligned, before anything is launched.
+    assert L.tq1_mmv_workspace_size(300, 2048, 1) == 0
+    assert L.tq1_mmv_workspace_size(300, 1280, 512) == 0
+    need = L.tq1_mmv_workspace_size(300, 2048, 512)
+    assert need >= 2 * 2 * 512 * 2048 + 4 * 512 and need % 256 == 0
+    for fn in (lib.tq1_mmv_ws, lib.tq2_mmv_ws):
+        assert fn(FAKE, FAKE, None, FAKE, 300, 2048, 512, FAKE, need - 1, None) == -5
+        assert fn(FAKE, FAKE, None, FAKE, 300, 2048, 512, FAKE + 8, need, None) == -3
+        assert fn(FAKE, FAKE, None, None, 300, 2048, 512, FAKE, need, None) == -1
+        assert fn(FAKE, FAKE, None, FAKE, 300, 2000, 512, FAKE, need, None) == -2
+        assert fn(FAKE, FAKE, None, FAKE, 0, 2048, 512, FAKE, need, None) == 0

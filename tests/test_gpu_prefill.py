@@ -1,5 +1,6 @@
-"""Prefill (t >= 256) on the tensor cores vs the oracle: fp32 outputs within
-max(1e-3 |ref|, 1e-4) on ragged and full-size shapes."""
+"""Prefill (t >= 256) vs the oracle: fp32 outputs within max(1e-3 |ref|,
+1e-4) on ragged and full-size shapes, through the tcgen05 tile path
+(tq1_mmv_ws with a workspace) and through the allocation-free tq1_mmv."""
 import numpy as np
 import pytest
 
@@ -15,18 +16,18 @@ pytestmark = pytest.mark.gpu
 def test_prefill_small_full(n, k, t):
     p = synth.matvec(n, k, t, seed=n + 3 * t)
     blocks, q8 = G.quantize_rows(p.w), G.quantize_acts(p.x)
-    y = G.mmv(blocks, q8, n, k, t)
     ref = orc.mmv_f64(orc.tq1_encode_rows(p.w), orc.q8_1_quantize(p.x), n, k, t)
-    G.assert_close(y, ref)
+    G.assert_close(G.mmv_ws(blocks, q8, n, k, t), ref)
+    G.assert_close(G.mmv(blocks, q8, n, k, t), ref)
 
 
 def test_config5_sampled_rows():
     p = synth.config_matvec("c5")
     blocks, q8 = G.quantize_rows(p.w), G.quantize_acts(p.x)
-    y = G.mmv(blocks, q8, p.n, p.k, p.t)
     rows = np.unique(np.concatenate([[0, 127, 128, p.n - 1], np.random.default_rng(5).integers(0, p.n, 44)]))
     ref = orc.mmv_f64(orc.tq1_encode_rows(p.w[rows]), orc.q8_1_quantize(p.x), rows.size, p.k, p.t)
-    G.assert_close(y[:, rows], ref)
+    G.assert_close(G.mmv_ws(blocks, q8, p.n, p.k, p.t)[:, rows], ref)
+    G.assert_close(G.mmv(blocks, q8, p.n, p.k, p.t)[:, rows], ref)
 
 
 def test_prefill_large_and_tiny_activations():
@@ -39,10 +40,10 @@ def test_prefill_large_and_tiny_activations():
     x[5] = 0.0
     x[6] *= 1e-6
     blocks, q8 = G.quantize_rows(p.w), G.quantize_acts(x)
-    y = G.mmv(blocks, q8, p.n, p.k, p.t)
     ref = orc.mmv_f64(orc.tq1_encode_rows(p.w), orc.q8_1_quantize(x), p.n, p.k, p.t)
-    G.assert_close(y, ref)
-    assert np.all(y[5] == 0.0)
+    for y in (G.mmv_ws(blocks, q8, p.n, p.k, p.t), G.mmv(blocks, q8, p.n, p.k, p.t)):
+        G.assert_close(y, ref)
+        assert np.all(y[5] == 0.0)
 
 
 def test_prefill_zero_weight_rows_and_determinism():
@@ -51,8 +52,8 @@ def test_prefill_zero_weight_rows_and_determinism():
     w[10] = 0.0
     w[200:256] = 0.0
     blocks, q8 = G.quantize_rows(w), G.quantize_acts(p.x)
-    a = G.mmv(blocks, q8, p.n, p.k, p.t)
-    b = G.mmv(blocks, q8, p.n, p.k, p.t)
+    a = G.mmv_ws(blocks, q8, p.n, p.k, p.t)
+    b = G.mmv_ws(blocks, q8, p.n, p.k, p.t)
     np.testing.assert_array_equal(a, b)
     assert np.all(a[:, 10] == 0.0) and np.all(a[:, 200:] == 0.0)
     ref = orc.mmv_f64(orc.tq1_encode_rows(w), orc.q8_1_quantize(p.x), p.n, p.k, p.t)

@@ -1,9 +1,8 @@
 """TQ2_0 (2-bit ternary codes) on the GPU vs the oracle: encoder bytes
 bit-exact, integer partials bit-exact, fp32 outputs within max(1e-3 |ref|,
-1e-4), over the decode rungs (t <= 4), the general kernel (t > 4 where k is
-not a multiple of 2048, chunks of 32 columns), the tensor-core tile path
-(t >= 7, k a multiple of 2048) and the full-size decode and prefill shapes
-(sampled rows)."""
+1e-4), over the decode kernel (t = 1 and the fused-quantisation entry), the
+tensor-core rungs (t >= 2), the tcgen05 tile path (tq2_mmv_ws with a
+workspace) and the full-size decode and prefill shapes (sampled rows)."""
 import numpy as np
 import pytest
 
@@ -162,7 +161,8 @@ def test_determinism():
         np.testing.assert_array_equal(_mmv(blocks, q8, 700, 4096, 3), y0)
 
 
-# t >= 7 with k a multiple of 2048 runs the tensor-core tile path.
+# tq2_mmv runs the tensor-core rungs; tq2_mmv_ws with a workspace runs the
+# tcgen05 tile path where tq1_mmv_workspace_size asks for one.
 TILE = [(300, 2048, 7), (129, 4096, 12), (640, 6144, 16), (257, 2048, 33), (1000, 4096, 64), (200, 2048, 100)]
 
 
@@ -172,19 +172,22 @@ def test_tile_path(n, k, t):
     blocks, q8 = _quantize_tq2(p.w), G.quantize_acts(p.x)
     ref = orc.tq2_mmv_f64(orc.tq2_encode_rows(p.w), orc.q8_1_quantize(p.x), n, k, t)
     G.assert_close(_mmv(blocks, q8, n, k, t), ref)
+    G.assert_close(G.mmv_ws(blocks, q8, n, k, t, fmt="tq2"), ref)
 
 
 def test_tile_path_code_three():
     # Raw blocks with every code, including the unused 3 (+2 d), through the
     # fp16 table of the tensor-core expansion.
-    n, k, t = 130, 2048, 9
+    n, k, t = 130, 2048, 40
     rng = np.random.default_rng(19)
     raw = rng.integers(0, 256, size=(n, k // 256, TQ2_BYTES), dtype=np.uint8)
     d = rng.uniform(0.01, 0.1, size=(n, k // 256)).astype(np.float16)
     raw[:, :, 64:66] = d.view(np.uint8).reshape(n, k // 256, 2)
     x = synth.matvec(1, k, t, seed=2).x
-    y = _mmv(G.dev(raw.reshape(-1)), G.quantize_acts(x), n, k, t)
-    G.assert_close(y, orc.tq2_mmv_f64(raw, orc.q8_1_quantize(x), n, k, t))
+    ref = orc.tq2_mmv_f64(raw, orc.q8_1_quantize(x), n, k, t)
+    rb, q8 = G.dev(raw.reshape(-1)), G.quantize_acts(x)
+    G.assert_close(_mmv(rb, q8, n, k, t), ref)                   # tensor-core rungs
+    G.assert_close(G.mmv_ws(rb, q8, n, k, t, fmt="tq2"), ref)     # tcgen05 tile path
 
 
 def test_prefill_shape_sampled_rows():
@@ -193,15 +196,16 @@ def test_prefill_shape_sampled_rows():
     blocks = _quantize_tq2(p.w)
     rng = np.random.default_rng(55)
     rows = np.unique(np.concatenate([[0, 127, 128, p.n - 1], rng.integers(0, p.n, 60)]))
-    y = _mmv(blocks, G.quantize_acts(p.x), p.n, p.k, p.t)
+    q8 = G.quantize_acts(p.x)
     ref = orc.tq2_mmv_f64(orc.tq2_encode_rows(p.w[rows]), orc.q8_1_quantize(p.x), rows.size, p.k, p.t)
-    G.assert_close(y[:, rows], ref)
+    G.assert_close(_mmv(blocks, q8, p.n, p.k, p.t)[:, rows], ref)
+    G.assert_close(G.mmv_ws(blocks, q8, p.n, p.k, p.t, fmt="tq2")[:, rows], ref)
 
 
 @pytest.mark.parametrize("n,k,t", [(5120, 6144, 1), (300, 2048, 2), (77, 1024, 3), (129, 4096, 4)])
 def test_fused_quantisation_matches_two_step(n, k, t):
     # tq2_mmv_f32 quantises in the decode kernel's prologue with the same
-    # operations as q8_1_quantize_acts: bit-identical outputs.
+    # operations as q8_1_quantize_acts: bit-identical per column.
     p = synth.matvec(n, k, t, seed=n + 3 * t)
     blocks = _quantize_tq2(p.w)
     two = _mmv(blocks, G.quantize_acts(p.x), n, k, t)
@@ -209,7 +213,13 @@ def test_fused_quantisation_matches_two_step(n, k, t):
     y = tt.full((t, n), float("nan"), dtype=tt.float32, device="cuda")
     G.lib().tq2_mmv_f32(blocks, G.dev(p.x.astype(np.float32)), y, n, k, t)
     assert G.lib().tq1_sync_status() == 0
-    np.testing.assert_array_equal(G.host(y), two)
+    np.testing.assert_array_equal(G.host(y), two)  # the same decode kernel on the same records
+    if t > 1:
+        for c in range(t):  # each column equals its own one-column two-step call, bitwise
+            one = _mmv(blocks, G.quantize_acts(p.x[c:c + 1]), n, k, 1)
+            y1 = tt.full((1, n), float("nan"), dtype=tt.float32, device="cuda")
+            G.lib().tq2_mmv_f32(blocks, G.dev(p.x[c:c + 1].astype(np.float32)), y1, n, k, 1)
+            np.testing.assert_array_equal(G.host(y1), one)
 
 
 @pytest.mark.parametrize("n,k,t", [(640, 2048, 1), (300, 2304, 3), (257, 2048, 9), (100, 2304, 40)])
