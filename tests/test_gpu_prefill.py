@@ -58,3 +58,21 @@ def test_prefill_zero_weight_rows_and_determinism():
     assert np.all(a[:, 10] == 0.0) and np.all(a[:, 200:] == 0.0)
     ref = orc.mmv_f64(orc.tq1_encode_rows(w), orc.q8_1_quantize(p.x), p.n, p.k, p.t)
     G.assert_close(a, ref)
+
+
+def test_config5_partials_sampled_rows():
+    """The exact integer partials of config 5 (N=14336, K=4096, T=512) through
+    the debug entry: tq1_mmv's kernel for this t (16 slices of 32 columns on the
+    tensor-core rungs), bit for bit against the oracle on sampled rows."""
+    p = synth.config_matvec("c5")
+    blocks, q8 = G.quantize_rows(p.w), G.quantize_acts(p.x)
+    rows = np.unique(np.concatenate([[0, 15, 16, p.n - 1], np.random.default_rng(55).integers(0, p.n, 20)]))
+    L, torch = G.lib(), G.torch()
+    part = torch.full((p.t, p.n, p.k // 32), -2 ** 31, dtype=torch.int32, device="cuda")  # 3.5 GiB
+    L.tq1_mmv_partials(blocks, q8, part, p.n, p.k, p.t)
+    assert L.tq1_sync_status() == 0
+    got = G.host(part[:, torch.from_numpy(rows).cuda()])  # only the sampled rows come back
+    del part
+    ref = orc.mmv_partials(orc.tq1_encode_rows(p.w[rows]), orc.q8_1_quantize(p.x), rows.size, p.k, p.t)
+    np.testing.assert_array_equal(got, ref)
+
