@@ -186,3 +186,11 @@ def test_mmv_ws_host_checks(lib):
         assert fn(FAKE, FAKE, None, None, 300, 2048, 512, FAKE, need, None) == -1
         assert fn(FAKE, FAKE, None, FAKE, 300, 2000, 512, FAKE, need, None) == -2
         assert fn(FAKE, FAKE, None, FAKE, 0, 2048, 512, FAKE, need, None) == 0
+
+
+def test_k_past_the_limit_is_refused(lib):
+    # 62720 (245 blocks) is the largest k the mat-vec entries accept.
+    assert lib.tq1_mmv(FAKE, FAKE, FAKE, 4, 62720 + 256, 1, None) == -4
+    assert lib.tq1_mmv_partials(FAKE, FAKE, FAKE, 4, 62720 + 256, 1, None) == -4
+    assert lib.tq2_mmv(FAKE, FAKE, FAKE, 4, 62720 + 256, 9, None) == -4
+
