@@ -1,11 +1,10 @@
 // tile.cu -- TQ1_0 x Q8_1 contraction on the 5th-generation tensor cores
-// (tcgen05, operands and accumulators in tensor memory) for 5 to hundreds of
-// token columns.
+// (tcgen05, operands and accumulators in tensor memory) for prefill-sized
+// token counts (tens to thousands of columns).
 //
-// Once a call carries more than a few columns, the dp4a mat-vec spends its
-// time on integer dot products that grow with T, while the tensor cores
-// finish them almost for free; what is left is the weights' base-3
-// expansion, which does not grow with T.  sm_103a has no integer MMA kind, so
+// With many columns the contraction itself dominates: the tensor cores run
+// it, and the weights' base-3 expansion (which does not grow with T) is
+// shared by a 64-token tile.  sm_103a has no integer MMA kind, so
 // the contraction runs in kind::f16 on operands that reproduce the method's
 // products exactly (PrismML-Eng/llama.cpp issue #139 "Proposed approach":
 // expand each packed byte once, reuse the activation fragment across rows and
@@ -23,10 +22,8 @@
 // A call runs two kernels:
 //  1. tile_prep_kernel turns the Q8_1 activations into the B operand once:
 //     fp16 hi rows [t_pad][k], then lo rows [t_pad][k], and the per-token
-//     scales 2^e_t, in a scratch buffer taken from a library-owned,
-//     stream-ordered memory pool (no synchronisation; capturable in CUDA
-//     graphs).  Padding tokens are zero.
-//  2. tile_kernel: one tile = 128 weight rows (TMEM lanes) x TOK tokens; K
+//     scales 2^e_t, in the caller's workspace.  Padding tokens are zero.
+//  2. tile_kernel: one tile = 128 weight rows (TMEM lanes) x 64 tokens; K
 //     advances in stages of 64 (a quarter of a 256-block).
 //     * a weight producer thread brings, per 256-block, the packed weights of
 //       all 128 rows into a shared-memory ring with one 2-D TMA copy (an
@@ -34,26 +31,21 @@
 //       rows past n arrive as zeros);
 //     * a B producer thread copies each stage's hi and lo rows (128-byte
 //       swizzled, K-major: the MMA's operand layout) with 2-D TMA;
-//     * A warps 0-15: group g = w/4 expands whole blocks g, g+4, g+8, ...
+//     * A warps 0-11: group g = w/4 expands whole blocks g, g+3, g+6, ...
 //       for rows 32*(w%4) .. +31 into fp16 +-d_w and stores each quarter
 //       straight into tensor memory (tcgen05.st; a warp may only reach its
 //       own quarter of the TMEM lanes, which is exactly its rows), so the
 //       16-bit A operand never touches shared memory;
-//     * epilogue warps 16-19: TMEM -> registers -> y (or split-K partials);
-//     * warp 20: TMEM allocation; its lane 0 issues the MMAs (A from TMEM).
-//     The four groups work on four blocks at once; the MMA takes their
-//     stages round-robin (block 4i + g, quarter q at position 16i + 4q + g of
-//     the tile's K order), so every ring slot belongs to one group and every
-//     mbarrier parity wait is answered by the phase it waits for.
-// Small T (decode batches) cannot fill the GPU with 128-row tiles alone, so a
-// tile's K range is split over a cluster of S CTAs; each rank leaves its fp32
-// partial tile in shared memory and, after a cluster barrier, each rank sums
-// a slice of rows over all ranks in rank order through distributed shared
-// memory (deterministic).  Larger T runs persistent CTAs over tiles with two
-// TMEM accumulators, so the epilogue of one tile overlaps the next.  Every
-// wait is bounded; the first timeout sets a shared abort flag that releases
-// every other wait, the status word records it, and the CTA lets its issued
-// copies and MMAs finish before it leaves.
+//     * epilogue warps 12-15: TMEM -> registers -> y;
+//     * warp 16: TMEM allocation; its lane 0 issues the MMAs (A from TMEM);
+//     * warps 17 and 18: the weight and the activation copies.
+//     The three groups work on three blocks at once and every ring slot
+//     belongs to one group, so every mbarrier parity wait is answered by the
+//     phase it waits for.
+// Persistent CTAs (at most one per SM) walk the tiles.  Every wait is
+// bounded; the first timeout sets a shared abort flag that releases every
+// other wait, the status word records it, and the CTA lets its issued copies
+// and MMAs finish before it leaves.
 //
 // Requires the weight row stride (k/256 * 54 bytes) to be a multiple of 16
 // (k a multiple of 2048): the launcher returns TQ1_ERR_UNSUPPORTED otherwise
@@ -87,43 +79,28 @@ constexpr int kRW = kGroups * kWSlotsPerGroup;  // raw weight ring: three blocks
 constexpr int kAWarps = 4 * kGroups, kEWarps = 4;
 constexpr int kEWarp0 = kAWarps, kMWarp = kEWarp0 + kEWarps, kPWarpW = kMWarp + 1, kPWarpB = kMWarp + 2;
 constexpr int kTThreads = (kPWarpB + 1) * 32;
-constexpr int kMaxSplit = 8;
 constexpr int kPrepThreads = 256;
 constexpr int kBlockCols = 4 * 32;  // TMEM columns of one block of A (4 quarters x 32)
 
-template <int TOK>
+constexpr int TOK = 64;                                // tokens per tile
 struct TileCfg {
   static constexpr int N = 2 * TOK;                      // B rows: hi of TOK tokens, then lo
   static constexpr uint32_t kBTile = N * 128;            // bytes of one quarter (K = 64) of B
   static constexpr uint32_t kBBlock = 4 * kBTile;        // bytes of one block of B
   // A block slots live in tensor memory (one per A warp group, so a slot has
   // a single owner), B block slots in shared memory (a plain ring).
-  static constexpr int kRB = TOK >= 64 ? 2 : 3;
-  static constexpr int kAccs = TOK >= 64 ? 1 : 2;        // TMEM accumulators (tiles in flight)
-  static constexpr int kAccCols = N < 32 ? 32 : N;
-  // Independent partial accumulators per tile: consecutive MMAs alternate
-  // between them, so an MMA need not wait for the previous one's result
-  // (at small N the chain through one accumulator, not the tensor pipe,
-  // sets the pace).  The epilogue adds them.
-  static constexpr int kPart = N <= 32 ? 2 : 1;
-  static constexpr int kAccStride = kPart * kAccCols;     // TMEM columns per tile accumulator
-  static constexpr int kA0 = kAccs * kAccStride;         // first TMEM column of the A slots
+  static constexpr int kRB = 2;
+  static constexpr int kAccCols = N;                     // TMEM columns of the tile accumulator
+  static constexpr int kA0 = kAccCols;                   // first TMEM column of the A slots
   static constexpr int kTmemCols = 512;
   static_assert(kA0 + kGroups * kBlockCols <= kTmemCols, "tensor memory budget");
-  static constexpr bool kSplitOk = TOK <= 32;            // split-K partials fit the B ring
-  static_assert(!kSplitOk || kRB * kBBlock >= kTileRows * TOK * 4, "split-K partials");
   static constexpr uint32_t kOffW = kRB * kBBlock;
-  // Split-K partials pushed by every rank into the rank that owns the rows:
-  // [source rank][row of the owner's slice][token], at most ceil(128 / S)
-  // rows per slice.
-  static constexpr uint32_t kOffRed = kOffW + kRW * kWRawBytes;
-  static constexpr uint32_t kRedBytes = kSplitOk ? (kTileRows + kMaxSplit) * TOK * 4 : 0;
-  static constexpr uint32_t kSmem = kOffRed + kRedBytes + 1024;
+  static constexpr uint32_t kSmem = kOffW + kRW * kWRawBytes + 1024;
   static_assert(kSmem + 2048 <= 232448, "shared memory budget");
   // Instruction descriptor: D fp32, A and B fp16, K-major, N, M = 128.
   static constexpr uint32_t kIdesc =
       (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(kTileRows) >> 4) << 24);
-  static constexpr int kChunk = TOK < 32 ? TOK : 32;     // TMEM columns per epilogue load
+  static constexpr int kChunk = 32;                      // TMEM columns per epilogue load
 };
 
 struct TileArgs {
@@ -133,7 +110,7 @@ struct TileArgs {
   unsigned* status;
   int n, k, t, t_pad;
   int tiles_m, tiles_n;
-  int split;  // S: CTAs (one cluster) sharing one tile's K range; 1 = persistent over tiles
+  int nblk;  // 256-blocks per weight row (k / 256)
 };
 
 // ------------------------------------------------------------- helpers --
@@ -251,22 +228,6 @@ template <int NC>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[NC]);
 
 template <>
-__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&v)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-               : "r"(taddr));
-}
-
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr));
-}
-
-template <>
 __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
@@ -276,10 +237,6 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
         "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // P_k = floor(b * 3^k / 256) of the four bytes held in 16-bit lanes lo
@@ -484,16 +441,16 @@ __global__ void __launch_bounds__(kPrepThreads) tile_prep_kernel(const uint8_t* 
   }
 }
 
-template <int TOK, int FMT>
+template <int FMT>
 __global__ void __launch_bounds__(kTThreads, 1)
     tile_kernel(const TileArgs a, const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmb) {
-  using C = TileCfg<TOK>;
+  using C = TileCfg;
   constexpr int kBB = fmt_block_bytes<FMT>();
   extern __shared__ __align__(1024) uint8_t tsmem_raw[];
   __shared__ __align__(8) uint64_t afull_bar[kGroups], aempty_bar[kGroups];
   __shared__ __align__(8) uint64_t bfull_bar[C::kRB], bempty_bar[C::kRB];
   __shared__ __align__(8) uint64_t wfull_bar[kRW], wempty_bar[kRW];
-  __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
+  __shared__ __align__(8) uint64_t accf_bar, acce_bar;  // the tile accumulator: full, free
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   volatile int* abort_flag = &s_abort;
@@ -508,23 +465,20 @@ __global__ void __launch_bounds__(kTThreads, 1)
   uint8_t* sm = tsmem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_addr(sm);
   uint8_t* wraw = sm + C::kOffW;
-  float* red = reinterpret_cast<float*>(sm + C::kOffRed);  // split-K partials (owner side)
   __shared__ float s_tscale[kEWarps][TOK];  // per-token scales, one copy per epilogue warp
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nb = a.k / kQK;
-  const int S = a.split;
+  const int nblk = a.nblk;  // blocks per tile
   const int ntiles = a.tiles_m * a.tiles_n;
-  const int rank = S > 1 ? static_cast<int>(blockIdx.x % S) : 0;
-  const int kb0 = S > 1 ? (nb * rank) / S : 0;
-  const int kb1 = S > 1 ? (nb * (rank + 1)) / S : nb;
-  const int nblk = kb1 - kb0;  // blocks per tile (the same for every tile of this CTA)
   // Tile of this CTA's unit u (>= ntiles: no more units).  Block j of the
   // CTA (counted over all its units) is block j % nblk of unit j / nblk.
-  auto unit_tile = [&](int u) -> int {
-    if (S > 1) return u == 0 ? static_cast<int>(blockIdx.x / S) : ntiles;
-    return static_cast<int>(blockIdx.x) + u * static_cast<int>(gridDim.x);
-  };
+  // The grid stride passes through an empty asm so that the compiler keeps
+  // the walk over units as written: given the stride it can see, it reshapes
+  // the role loops around a closed-form unit count, and the prefill shape
+  // (N=14336, K=4096, T=512) measured 116 instead of 110 us per call.
+  int gstride = static_cast<int>(gridDim.x);
+  asm("" : "+r"(gstride));
+  auto unit_tile = [&](int u) -> int { return static_cast<int>(blockIdx.x) + u * gstride; };
   int nunits = 0;
   while (unit_tile(nunits) < ntiles) ++nunits;
   const uint32_t nall = static_cast<uint32_t>(nunits * nblk);  // blocks of this CTA
@@ -534,7 +488,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const int bi = static_cast<int>(j % nblk);
     const int row0 = (unit_tile(static_cast<int>(j / nblk)) / a.tiles_n) * kTileRows;
     mbar_arrive_expect_tx(&wfull_bar[ws], kWRawBytes);
-    tma_load_2d(wraw + ws * kWRawBytes, &tmw, ((kb0 + bi) * kBB) & ~15, row0, &wfull_bar[ws]);
+    tma_load_2d(wraw + ws * kWRawBytes, &tmw, (bi * kBB) & ~15, row0, &wfull_bar[ws]);
   };
   const uint32_t nfirst = nall < static_cast<uint32_t>(kRW) ? nall : static_cast<uint32_t>(kRW);
 
@@ -551,10 +505,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
       mbar_init(&wfull_bar[i], 1);
       mbar_init(&wempty_bar[i], 4);  // the 4 warps of the slot's A group
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&accf_bar[i], 1);
-      mbar_init(&acce_bar[i], kEWarps);
-    }
+    mbar_init(&accf_bar, 1);
+    mbar_init(&acce_bar, kEWarps);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -605,7 +557,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty_bar[ws]);
-      const uint32_t off = static_cast<uint32_t>((kb0 + bi) * kBB) & 15u;
+      const uint32_t off = static_cast<uint32_t>(bi * kBB) & 15u;
       const uint32_t sh = (off & 2u) * 8u;
       uint32_t out[32];
       if (FMT == kFmtTq2) {
@@ -662,74 +614,38 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const int quarter = warp & 3;  // TMEM lane quarter this warp may read
     const int rl = quarter * 32 + lane;
     float* tsc = s_tscale[warp - kEWarp0];
-    // Split-K: the value of (row rl, token tl) goes to the rank owning row
-    // rl's slice, into that rank's partials at [this rank][row in slice][tl].
-    const int owner = ((rl + 1) * S - 1) / kTileRows;
-    const int slice_max = (kTileRows + S - 1) / S;
-    uint32_t red_dst = 0;
-    if (S > 1) {
-      const int oslot = (rank * slice_max + (rl - (kTileRows * owner) / S)) * TOK;
-      uint32_t la = smem_addr(red + oslot);
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(red_dst) : "r"(la), "r"(owner));
-    }
     pdl_wait();  // the scales are written by the prep kernel
     for (int u = 0; u < nunits; ++u) {
       const int tile = unit_tile(u);
       const int row = (tile / a.tiles_n) * kTileRows + rl;
       const int tok0 = (tile % a.tiles_n) * TOK;
-      const int acc = u % C::kAccs;
-      const uint32_t aph = static_cast<uint32_t>(u / C::kAccs) & 1u;
+      const uint32_t aph = static_cast<uint32_t>(u) & 1u;
       // Scales of this tile's tokens, fetched while the MMAs run.
       __syncwarp();
       for (int tl = lane; tl < TOK; tl += 32) tsc[tl] = __ldg(a.scale + tok0 + tl);
       __syncwarp();
-      if (!warp_wait(&accf_bar[acc], aph, abort_flag)) break;
+      if (!warp_wait(&accf_bar, aph, abort_flag)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * C::kAccStride);
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
       for (int c0 = 0; c0 < TOK; c0 += C::kChunk) {
         uint32_t vh[C::kChunk], vl[C::kChunk];
         tmem_ld<C::kChunk>(tbase + c0, vh);
         tmem_ld<C::kChunk>(tbase + TOK + c0, vl);
-        if (C::kPart == 2) {
-          uint32_t wh[C::kChunk], wl[C::kChunk];
-          tmem_ld<C::kChunk>(tbase + C::kAccCols + c0, wh);
-          tmem_ld<C::kChunk>(tbase + C::kAccCols + TOK + c0, wl);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-          for (int jj = 0; jj < C::kChunk; ++jj) {
-            vh[jj] = __float_as_uint(__uint_as_float(vh[jj]) + __uint_as_float(wh[jj]));
-            vl[jj] = __float_as_uint(__uint_as_float(vl[jj]) + __uint_as_float(wl[jj]));
-          }
-        }
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (S > 1) {
-          // Four tokens per 16-byte store into the owner's partials.
 #pragma unroll
-          for (int jj = 0; jj < C::kChunk; jj += 4) {
-            const int tl = c0 + jj;
-            float v[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = (__uint_as_float(vh[jj + e]) + __uint_as_float(vl[jj + e])) * tsc[tl + e];
-            asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red_dst + 4u * tl), "f"(v[0]),
-                         "f"(v[1]), "f"(v[2]), "f"(v[3])
-                         : "memory");
-          }
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < C::kChunk; ++jj) {
-            const int tl = c0 + jj, tok = tok0 + tl;
-            const float v = (__uint_as_float(vh[jj]) + __uint_as_float(vl[jj])) * tsc[tl];
-            if (row < a.n && tok < a.t) {
-              const int64_t yi = static_cast<int64_t>(tok) * a.n + row;
-              a.y[yi] = a.res ? v + a.res[yi] : v;
-            }
+        for (int jj = 0; jj < C::kChunk; ++jj) {
+          const int tl = c0 + jj, tok = tok0 + tl;
+          const float v = (__uint_as_float(vh[jj]) + __uint_as_float(vl[jj])) * tsc[tl];
+          if (row < a.n && tok < a.t) {
+            const int64_t yi = static_cast<int64_t>(tok) * a.n + row;
+            a.y[yi] = a.res ? v + a.res[yi] : v;
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_bar[acc]);
+      if (lane == 0) mbar_arrive(&acce_bar);
     }
   } else if (warp == kMWarp) {
     // -------------------------------------------------------------- MMA --
@@ -743,11 +659,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
       const uint64_t d0 = umma_desc_sw128(sbase);
       uint32_t ga = 0, pa = 0, rb = 0, pb = 0;  // A group slot, B ring slot and their phases
       for (int u = 0; u < nunits && ok; ++u) {
-        const int acc = u % C::kAccs;
-        const uint32_t aph = static_cast<uint32_t>(u / C::kAccs) & 1u;
-        if (!spin_wait_or_abort(&acce_bar[acc], aph ^ 1u, abort_flag)) break;
+        const uint32_t aph = static_cast<uint32_t>(u) & 1u;
+        if (!spin_wait_or_abort(&acce_bar, aph ^ 1u, abort_flag)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + static_cast<uint32_t>(acc * C::kAccStride);
+        const uint32_t dt = tmem;
         for (int bi = 0; bi < nblk; ++bi) {
           if (!spin_wait_or_abort(&afull_bar[ga], pa, abort_flag) ||
               !spin_wait_or_abort(&bfull_bar[rb], pb, abort_flag)) {
@@ -762,9 +677,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
 #pragma unroll
             for (int ks = 0; ks < kStageK / 16; ++ks) {
               const int step = q * (kStageK / 16) + ks;  // 0..15 within the block
-              const uint32_t part = static_cast<uint32_t>(step % C::kPart);
-              umma_ts(dt + part * C::kAccCols, at + 32u * q + 8u * ks, db + ((q * C::kBTile + 32u * ks) >> 4),
-                      C::kIdesc, (bi > 0 || step >= C::kPart) ? 1u : 0u);
+              umma_ts(dt, at + 32u * q + 8u * ks, db + ((q * C::kBTile + 32u * ks) >> 4), C::kIdesc,
+                      (bi > 0 || step > 0) ? 1u : 0u);
             }
           umma_commit(&aempty_bar[ga]);
           umma_commit(&bempty_bar[rb]);
@@ -775,7 +689,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
           if (++rb == C::kRB) { rb = 0; pb ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(&accf_bar[acc]);
+        umma_commit(&accf_bar);
       }
       // After an abort, let the MMAs already issued finish (bounded) before
       // the tensor memory is released.
@@ -821,7 +735,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
       if (!ok) break;
       if (lane < 8) {
         const int q = lane >> 1, hl = lane & 1;
-        tma_load_2d(sm + rb * C::kBBlock + q * C::kBTile + hl * TOK * 128, &tmb, (kb0 + bi) * kQK + q * kStageK,
+        tma_load_2d(sm + rb * C::kBBlock + q * C::kBTile + hl * TOK * 128, &tmb, bi * kQK + q * kStageK,
                     hl * a.t_pad + tok0, &bfull_bar[rb]);
       }
       __syncwarp();
@@ -837,31 +751,6 @@ __global__ void __launch_bounds__(kTThreads, 1)
   }
   __syncthreads();
   if (tid == 0 && *abort_flag) raise_status(a.status, kStatusTimeout);
-  if (S > 1) {
-    __syncwarp();
-    cluster_sync_all();  // every rank's partials are in their owners' shared memory
-    if (!*abort_flag) {
-      // Every thread of the CTA sums a strided share of this rank's slice:
-      // thread -> (row of the slice, token) with the row fastest, so that
-      // the y stores of a warp are contiguous.
-      const int tile = static_cast<int>(blockIdx.x / S);
-      const int row0 = (tile / a.tiles_n) * kTileRows, tok0 = (tile % a.tiles_n) * TOK;
-      const int r_lo = (kTileRows * rank) / S, r_hi = (kTileRows * (rank + 1)) / S;
-      const int nr = r_hi - r_lo, slice_max = (kTileRows + S - 1) / S;
-      const int ntok = min(TOK, a.t - tok0), nrow = min(nr, a.n - (row0 + r_lo));
-      static_assert(kTThreads >= 512, "reduction mapping");
-      for (int ri = tid % 64; tid < 512 && ri < nrow; ri += 64) {
-        for (int tl = tid / 64; tl < ntok; tl += 8) {
-          float v = 0.0f;
-#pragma unroll
-          for (int src = 0; src < kMaxSplit; ++src)  // rank order
-            if (src < S) v += red[(src * slice_max + ri) * TOK + tl];
-          const int64_t yi = static_cast<int64_t>(tok0 + tl) * a.n + row0 + r_lo + ri;
-          a.y[yi] = a.res ? v + a.res[yi] : v;
-        }
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
   if (warp == kMWarp) {
@@ -905,23 +794,22 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esize, const
 
 // Scratch of one call: fp16 hi and lo activation rows [t_pad][k] each, then
 // the per-token scales [t_pad], rounded up to 256 bytes.
-template <int TOK>
 size_t tile_scratch_bytes(int64_t k, int64_t t) {
   const int64_t t_pad = ((t + TOK - 1) / TOK) * TOK;
   const size_t b = 2 * static_cast<size_t>(t_pad) * k * sizeof(uint16_t) + static_cast<size_t>(t_pad) * sizeof(float);
   return (b + 255) & ~size_t(255);
 }
 
-template <int TOK, int FMT>
-int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms, cudaStream_t s, void* ws,
+template <int FMT>
+int launch_tile_fmt(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms, cudaStream_t s, void* ws,
                     size_t ws_bytes) {
-  using C = TileCfg<TOK>;
+  using C = TileCfg;
   const DeviceInfo& di = device_info();
   static std::atomic<bool> configured[64];  // per device (racing threads configure twice: idempotent)
   if (di.device < 0 || di.device >= 64) return TQ1_ERR_CUDA;
   if (C::kSmem + 2048 > di.max_smem_optin) return TQ1_ERR_UNSUPPORTED;
   if (!configured[di.device].load(std::memory_order_acquire)) {
-    if (!cuda_ok(cudaFuncSetAttribute(tile_kernel<TOK, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!cuda_ok(cudaFuncSetAttribute(tile_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(C::kSmem))))
       return TQ1_ERR_CUDA;
     configured[di.device].store(true, std::memory_order_release);
@@ -932,7 +820,7 @@ int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms
   const int nb = a.k / kQK;
   const uint64_t rowbytes = static_cast<uint64_t>(nb) * fmt_block_bytes<FMT>();
   const size_t hilo_bytes = 2 * static_cast<size_t>(a.t_pad) * a.k * sizeof(uint16_t);
-  if (ws == nullptr || ws_bytes < tile_scratch_bytes<TOK>(a.k, a.t)) return TQ1_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < tile_scratch_bytes(a.k, a.t)) return TQ1_ERR_WORKSPACE;
 
   CUtensorMap tmw;
   if (!make_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, rowbytes, static_cast<uint64_t>(a.n), kWinBytes, kTileRows,
@@ -960,36 +848,22 @@ int launch_tile_tok(const uint8_t* w, const uint8_t* q8, TileArgs a, int num_sms
   }
   if (rc == TQ1_OK) {
     const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
-    int split = 1;
-    if (C::kSplitOk && 2 * tiles <= num_sms)
-      split = static_cast<int>(std::min<int64_t>({kMaxSplit, nb, num_sms / tiles}));
-    a.split = split;
-    const int64_t grid = split > 1 ? tiles * split : std::min<int64_t>(tiles, num_sms);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(tiles, num_sms)));
     cfg.blockDim = dim3(kTThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0] = pdl[0];
-    int na = 1;
-    if (split > 1) {
-      attr[na].id = cudaLaunchAttributeClusterDimension;
-      attr[na].val.clusterDim.x = static_cast<unsigned>(split);
-      attr[na].val.clusterDim.y = 1;
-      attr[na].val.clusterDim.z = 1;
-      ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    if (!cuda_ok(cudaLaunchKernelEx(&cfg, tile_kernel<TOK, FMT>, a, tmw, tmb))) rc = TQ1_ERR_CUDA;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    a.nblk = nb;
+    if (!cuda_ok(cudaLaunchKernelEx(&cfg, tile_kernel<FMT>, a, tmw, tmb))) rc = TQ1_ERR_CUDA;
   }
   return rc;
 }
 
 template <int FMT>
-int launch_tile_fmt(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t,
-                    cudaStream_t s, unsigned* status, const float* res, void* ws, size_t ws_bytes) {
+int launch_tile_checked(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t,
+                        cudaStream_t s, unsigned* status, const float* res, void* ws, size_t ws_bytes) {
   if (n > (int64_t{1} << 30) || t > (int64_t{1} << 24) || k > (int64_t{1} << 30)) return TQ1_ERR_UNSUPPORTED;
   // The weight map's row stride must be a multiple of 16 bytes.
   if (((k / kQK) * fmt_block_bytes<FMT>()) % 16 != 0) return TQ1_ERR_UNSUPPORTED;
@@ -1001,27 +875,21 @@ int launch_tile_fmt(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, in
   a.n = static_cast<int>(n);
   a.k = static_cast<int>(k);
   a.t = static_cast<int>(t);
-  if (t <= 8) return launch_tile_tok<8, FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
-  if (t <= 16) return launch_tile_tok<16, FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
-  if (t <= 32) return launch_tile_tok<32, FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
-  return launch_tile_tok<64, FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
+  return launch_tile_fmt<FMT>(w, q8, a, di.num_sms, s, ws, ws_bytes);
 }
 
 }  // namespace
 
 int launch_tile(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t t, cudaStream_t s,
                 unsigned* status, const float* res, int fmt, void* ws, size_t ws_bytes) {
-  return fmt == kFmtTq2 ? launch_tile_fmt<kFmtTq2>(w, q8, y, n, k, t, s, status, res, ws, ws_bytes)
-                        : launch_tile_fmt<kFmtTq1>(w, q8, y, n, k, t, s, status, res, ws, ws_bytes);
+  return fmt == kFmtTq2 ? launch_tile_checked<kFmtTq2>(w, q8, y, n, k, t, s, status, res, ws, ws_bytes)
+                        : launch_tile_checked<kFmtTq1>(w, q8, y, n, k, t, s, status, res, ws, ws_bytes);
 }
 
 size_t tile_workspace_bytes(int64_t n, int64_t k, int64_t t, int fmt) {
   if (n < 1 || t < 1 || k < kQK || n > (int64_t{1} << 30) || t > (int64_t{1} << 24) || k > (int64_t{1} << 30)) return 0;
   if (((k / kQK) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes)) % 16 != 0) return 0;  // the dp4a/mma kernels
-  if (t <= 8) return tile_scratch_bytes<8>(k, t);
-  if (t <= 16) return tile_scratch_bytes<16>(k, t);
-  if (t <= 32) return tile_scratch_bytes<32>(k, t);
-  return tile_scratch_bytes<64>(k, t);
+  return tile_scratch_bytes(k, t);
 }
 
 }  // namespace tq1

@@ -1,8 +1,8 @@
 """The tcgen05 tile path (tq1_mmv_ws with a workspace, t >= its threshold) vs
 the oracle: fp32 outputs within max(1e-3 |ref|, 1e-4).  The shapes pick
-64-column token tiles, split-K clusters, ragged row and token tiles, several
-persistent tiles per CTA, and two shapes whose row stride keeps them on the
-allocation-free kernels (no workspace asked for)."""
+single and ragged row tiles, ragged 64-token tiles, several persistent tiles
+per CTA, and two shapes whose row stride keeps them on the allocation-free
+kernels (no workspace asked for)."""
 import numpy as np
 import pytest
 
@@ -13,10 +13,10 @@ from tests import gpu_util as G
 pytestmark = pytest.mark.gpu
 
 SHAPES = [
-    (1, 2048, 33),      # one row; split over a cluster, one block per rank
+    (1, 2048, 33),      # one row, one tile: 127 zero-filled rows
     (129, 2048, 40),    # two row tiles
-    (77, 6144, 48),     # three blocks per rank
-    (256, 4096, 33),    # 64-column tiles, persistent
+    (77, 6144, 48),     # 24 blocks per tile, a partial row tile
+    (256, 4096, 33),    # two row tiles, 31 padding tokens
     (64, 2048, 64),
     (200, 2048, 65),    # two token tiles
     (130, 4096, 129),   # three token tiles, ragged
