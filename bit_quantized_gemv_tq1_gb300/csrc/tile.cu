@@ -4,7 +4,7 @@
 //
 // With many columns the contraction itself dominates: the tensor cores run
 // it, and the weights' base-3 expansion (which does not grow with T) is
-// shared by a 64-token tile.  sm_103a has no integer MMA kind, so
+// shared by a 128-token tile.  sm_103a has no integer MMA kind, so
 // the contraction runs in kind::f16 on operands that reproduce the method's
 // products exactly (PrismML-Eng/llama.cpp issue #139 "Proposed approach":
 // expand each packed byte once, reuse the activation fragment across rows and
@@ -23,25 +23,34 @@
 //  1. tile_prep_kernel turns the Q8_1 activations into the B operand once:
 //     fp16 hi rows [t_pad][k], then lo rows [t_pad][k], and the per-token
 //     scales 2^e_t, in the caller's workspace.  Padding tokens are zero.
-//  2. tile_kernel: one tile = 128 weight rows (TMEM lanes) x 64 tokens; K
-//     advances in stages of 64 (a quarter of a 256-block).
+//  2. tile_kernel: one tile = 128 weight rows (TMEM lanes) x 128 tokens; K
+//     advances in stages of 64 (a quarter of a 256-block).  Each MMA is
+//     M = 128, N = 256 (the hi rows of the 128 tokens, then their lo rows),
+//     K = 16: the 256-column fp32 accumulator and two 128-column A block
+//     slots fill the 512 columns of tensor memory.
 //     * a weight producer thread brings, per 256-block, the packed weights of
 //       all 128 rows into a shared-memory ring with one 2-D TMA copy (an
 //       80-byte, 16-byte-aligned window around each row's 54-byte block;
 //       rows past n arrive as zeros);
-//     * a B producer thread copies each stage's hi and lo rows (128-byte
-//       swizzled, K-major: the MMA's operand layout) with 2-D TMA;
-//     * A warps 0-11: group g = w/4 expands whole blocks g, g+3, g+6, ...
+//     * a B producer warp copies each stage's hi and lo rows (128-byte
+//       swizzled, K-major: the MMA's operand layout) with 2-D TMA into a ring
+//       of quarter-block slots (32 KB each);
+//     * A warps 0-7: group g = w/4 expands whole blocks g, g+2, g+4, ...
 //       for rows 32*(w%4) .. +31 into fp16 +-d_w and stores each quarter
 //       straight into tensor memory (tcgen05.st; a warp may only reach its
 //       own quarter of the TMEM lanes, which is exactly its rows), so the
 //       16-bit A operand never touches shared memory;
-//     * epilogue warps 12-15: TMEM -> registers -> y;
-//     * warp 16: TMEM allocation; its lane 0 issues the MMAs (A from TMEM);
-//     * warps 17 and 18: the weight and the activation copies.
-//     The three groups work on three blocks at once and every ring slot
-//     belongs to one group, so every mbarrier parity wait is answered by the
-//     phase it waits for.
+//     * epilogue warps 8-11: TMEM -> registers -> y;
+//     * warp 12: TMEM allocation; its lane 0 issues the MMAs (A from TMEM);
+//     * warps 13 and 14: the weight and the activation copies.
+//     The two groups work on two blocks at once and every ring slot belongs
+//     to one group, so every mbarrier parity wait is answered by the phase it
+//     waits for.
+//     Why 128 tokens and N = 256 rather than 64 tokens and N = 128: the A
+//     warps' integer work competes for issue slots with the thread that
+//     feeds the (shallow) MMA queue, and an N = 256 MMA keeps the tensor pipe
+//     busy twice as long per issue and per expanded weight (measured on the
+//     prefill shape N=14336, K=4096, T=512: 110.8 -> 84.6 us per call).
 // Persistent CTAs (at most one per SM) walk the tiles.  Every wait is
 // bounded; the first timeout sets a shared abort flag that releases every
 // other wait, the status word records it, and the CTA lets its issued copies
@@ -73,7 +82,7 @@ constexpr int kTileRows = 128;  // weight rows per tile = TMEM lanes
 constexpr int kStageK = 64;     // K per MMA stage (a quarter of a 256-block)
 constexpr int kWinBytes = 80;   // raw weight window per row and block (16-byte aligned)
 constexpr uint32_t kWRawBytes = kTileRows * kWinBytes;
-constexpr int kGroups = 3;      // A warp groups = tensor-memory block slots
+constexpr int kGroups = 2;      // A warp groups = tensor-memory block slots
 constexpr int kWSlotsPerGroup = 3;
 constexpr int kRW = kGroups * kWSlotsPerGroup;  // raw weight ring: three blocks per A group
 constexpr int kAWarps = 4 * kGroups, kEWarps = 4;
@@ -82,19 +91,19 @@ constexpr int kTThreads = (kPWarpB + 1) * 32;
 constexpr int kPrepThreads = 256;
 constexpr int kBlockCols = 4 * 32;  // TMEM columns of one block of A (4 quarters x 32)
 
-constexpr int TOK = 64;                                // tokens per tile
+constexpr int TOK = 128;                               // tokens per tile
 struct TileCfg {
-  static constexpr int N = 2 * TOK;                      // B rows: hi of TOK tokens, then lo
+  static constexpr int N = 2 * TOK;                      // B rows: hi of TOK tokens, then lo (MMA N = 256)
   static constexpr uint32_t kBTile = N * 128;            // bytes of one quarter (K = 64) of B
-  static constexpr uint32_t kBBlock = 4 * kBTile;        // bytes of one block of B
   // A block slots live in tensor memory (one per A warp group, so a slot has
-  // a single owner), B block slots in shared memory (a plain ring).
-  static constexpr int kRB = 2;
+  // a single owner); B lives in shared memory as a ring of quarter-block
+  // slots (a whole block of B is 128 KB).
+  static constexpr int kRB = 5;
   static constexpr int kAccCols = N;                     // TMEM columns of the tile accumulator
   static constexpr int kA0 = kAccCols;                   // first TMEM column of the A slots
   static constexpr int kTmemCols = 512;
   static_assert(kA0 + kGroups * kBlockCols <= kTmemCols, "tensor memory budget");
-  static constexpr uint32_t kOffW = kRB * kBBlock;
+  static constexpr uint32_t kOffW = kRB * kBTile;
   static constexpr uint32_t kSmem = kOffW + kRW * kWRawBytes + 1024;
   static_assert(kSmem + 2048 <= 232448, "shared memory budget");
   // Instruction descriptor: D fp32, A and B fp16, K-major, N, M = 128.
@@ -663,30 +672,32 @@ __global__ void __launch_bounds__(kTThreads, 1)
         if (!spin_wait_or_abort(&acce_bar, aph ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t dt = tmem;
-        for (int bi = 0; bi < nblk; ++bi) {
-          if (!spin_wait_or_abort(&afull_bar[ga], pa, abort_flag) ||
-              !spin_wait_or_abort(&bfull_bar[rb], pb, abort_flag)) {
+        for (int bi = 0; bi < nblk && ok; ++bi) {
+          if (!spin_wait_or_abort(&afull_bar[ga], pa, abort_flag)) {
             ok = false;
             break;
           }
-          tc_fence_after();
           const uint32_t at = tmem + C::kA0 + ga * kBlockCols;
-          const uint64_t db = d0 + ((rb * C::kBBlock) >> 4);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int ks = 0; ks < kStageK / 16; ++ks) {
-              const int step = q * (kStageK / 16) + ks;  // 0..15 within the block
-              umma_ts(dt, at + 32u * q + 8u * ks, db + ((q * C::kBTile + 32u * ks) >> 4), C::kIdesc,
-                      (bi > 0 || step > 0) ? 1u : 0u);
+          for (int q = 0; q < 4; ++q) {
+            if (!spin_wait_or_abort(&bfull_bar[rb], pb, abort_flag)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
+            const uint64_t db = d0 + ((rb * C::kBTile) >> 4);
+#pragma unroll
+            for (int ks = 0; ks < kStageK / 16; ++ks)
+              umma_ts(dt, at + 32u * q + 8u * ks, db + ((32u * ks) >> 4), C::kIdesc, (bi > 0 || q > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(&bempty_bar[rb]);
+            issued = true;
+            last_bar = &bempty_bar[rb];
+            last_ph = pb;
+            if (++rb == C::kRB) { rb = 0; pb ^= 1u; }
+          }
+          // The A slot is released only after all four quarters' MMAs were
+          // issued (on an abort, those issued so far).
           umma_commit(&aempty_bar[ga]);
-          umma_commit(&bempty_bar[rb]);
-          issued = true;
-          last_bar = &bempty_bar[rb];
-          last_ph = pb;
           if (++ga == kGroups) { ga = 0; pa ^= 1u; }
-          if (++rb == C::kRB) { rb = 0; pb ^= 1u; }
         }
         if (!ok) break;
         umma_commit(&accf_bar);
@@ -718,30 +729,35 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
   } else {
     // ------------------------------------------------ activation copies --
-    // Lane 0 waits for a free slot and posts the byte count; lanes 0-7 then
-    // issue the block's eight copies (4 quarters x hi/lo rows) at once.
+    // Lane 0 waits for a free quarter slot and posts the byte count; lanes 0
+    // and 1 then issue the quarter's two copies (hi and lo rows) at once.
     pdl_wait();  // the B operand is written by the prep kernel
     int last_slot = -1;
     uint32_t last_ph = 0, rb = 0, pb = 0;
     int bi = 0, u = 0;
     int tok0 = nunits > 0 ? (unit_tile(0) % a.tiles_n) * TOK : 0;
     for (uint32_t j = 0; j < nall; ++j) {
-      int ok = 1;
-      if (lane == 0) {
-        ok = wait_or_abort(&bempty_bar[rb], pb ^ 1u, abort_flag) ? 1 : 0;
-        if (ok) mbar_arrive_expect_tx(&bfull_bar[rb], C::kBBlock);
+      bool stop = false;
+      for (int q = 0; q < 4; ++q) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = wait_or_abort(&bempty_bar[rb], pb ^ 1u, abort_flag) ? 1 : 0;
+          if (ok) mbar_arrive_expect_tx(&bfull_bar[rb], C::kBTile);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          stop = true;
+          break;
+        }
+        if (lane < 2)
+          tma_load_2d(sm + rb * C::kBTile + lane * TOK * 128, &tmb, bi * kQK + q * kStageK, lane * a.t_pad + tok0,
+                      &bfull_bar[rb]);
+        __syncwarp();
+        last_slot = static_cast<int>(rb);
+        last_ph = pb;
+        if (++rb == C::kRB) { rb = 0; pb ^= 1u; }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane < 8) {
-        const int q = lane >> 1, hl = lane & 1;
-        tma_load_2d(sm + rb * C::kBBlock + q * C::kBTile + hl * TOK * 128, &tmb, bi * kQK + q * kStageK,
-                    hl * a.t_pad + tok0, &bfull_bar[rb]);
-      }
-      __syncwarp();
-      last_slot = static_cast<int>(rb);
-      last_ph = pb;
-      if (++rb == C::kRB) { rb = 0; pb ^= 1u; }
+      if (stop) break;
       if (++bi == nblk) {
         bi = 0;
         if (++u < nunits) tok0 = (unit_tile(u) % a.tiles_n) * TOK;
