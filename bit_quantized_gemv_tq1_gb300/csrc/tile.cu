@@ -34,7 +34,8 @@
 //       rows past n arrive as zeros);
 //     * a B producer warp copies each stage's hi and lo rows (128-byte
 //       swizzled, K-major: the MMA's operand layout) with 2-D TMA into a ring
-//       of quarter-block slots (32 KB each);
+//       of three half-block slots (64 KB each; fewer, larger slots mean fewer
+//       barrier waits and commits on the MMA thread);
 //     * A warps 0-7: group g = w/4 expands whole blocks g, g+2, g+4, ...
 //       for rows 32*(w%4) .. +31 into fp16 +-d_w and stores each quarter
 //       straight into tensor memory (tcgen05.st; a warp may only reach its
@@ -83,27 +84,33 @@ constexpr int kStageK = 64;     // K per MMA stage (a quarter of a 256-block)
 constexpr int kWinBytes = 80;   // raw weight window per row and block (16-byte aligned)
 constexpr uint32_t kWRawBytes = kTileRows * kWinBytes;
 constexpr int kGroups = 2;      // A warp groups = tensor-memory block slots
-constexpr int kWSlotsPerGroup = 3;
-constexpr int kRW = kGroups * kWSlotsPerGroup;  // raw weight ring: three blocks per A group
+constexpr int kWSlotsPerGroup = 1;
+// Raw weight ring: one block per A group.  A group copies its block's raw
+// weights to registers first and frees the slot at once, so the next copy has
+// the group's whole expansion and its wait for a free A slot to land in (the
+// shared memory goes to the B ring instead).
+constexpr int kRW = kGroups * kWSlotsPerGroup;
 constexpr int kAWarps = 4 * kGroups, kEWarps = 4;
 constexpr int kEWarp0 = kAWarps, kMWarp = kEWarp0 + kEWarps, kPWarpW = kMWarp + 1, kPWarpB = kMWarp + 2;
 constexpr int kTThreads = (kPWarpB + 1) * 32;
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 128;
+constexpr int kPrepHeld = 2;  // Q8_1 blocks a prep thread keeps in registers (k <= 8192: one pass over q8)
 constexpr int kBlockCols = 4 * 32;  // TMEM columns of one block of A (4 quarters x 32)
 
 constexpr int TOK = 128;                               // tokens per tile
 struct TileCfg {
   static constexpr int N = 2 * TOK;                      // B rows: hi of TOK tokens, then lo (MMA N = 256)
   static constexpr uint32_t kBTile = N * 128;            // bytes of one quarter (K = 64) of B
+  static constexpr uint32_t kBSlot = 2 * kBTile;         // a B ring slot: half a block (K = 128)
   // A block slots live in tensor memory (one per A warp group, so a slot has
-  // a single owner); B lives in shared memory as a ring of quarter-block
-  // slots (a whole block of B is 128 KB).
-  static constexpr int kRB = 5;
+  // a single owner); B lives in shared memory as a ring of half-block slots
+  // (a whole block of B is 128 KB).
+  static constexpr int kRB = 3;
   static constexpr int kAccCols = N;                     // TMEM columns of the tile accumulator
   static constexpr int kA0 = kAccCols;                   // first TMEM column of the A slots
   static constexpr int kTmemCols = 512;
   static_assert(kA0 + kGroups * kBlockCols <= kTmemCols, "tensor memory budget");
-  static constexpr uint32_t kOffW = kRB * kBTile;
+  static constexpr uint32_t kOffW = kRB * kBSlot;
   static constexpr uint32_t kSmem = kOffW + kRW * kWRawBytes + 1024;
   static_assert(kSmem + 2048 <= 232448, "shared memory budget");
   // Instruction descriptor: D fp32, A and B fp16, K-major, N, M = 128.
@@ -418,9 +425,27 @@ __global__ void __launch_bounds__(kPrepThreads) tile_prep_kernel(const uint8_t* 
     return;
   }
   const uint8_t* qr = q8 + static_cast<int64_t>(tok) * nq * kQ8Bytes;
+  // Up to kPrepHeld whole blocks per thread are read once, into registers,
+  // before the token's maximum scale is known; larger k reads the scales
+  // first and the blocks again afterwards.
+  const bool held = nq <= kPrepHeld * kPrepThreads;
+  uint32_t blk[kPrepHeld][9];
   float m = 0.0f;
-  for (int j = tid; j < nq; j += kPrepThreads)
-    m = fmaxf(m, fabsf(__half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(qr + j * kQ8Bytes))))));
+  if (held) {
+#pragma unroll
+    for (int i = 0; i < kPrepHeld; ++i) {
+      const int j = tid + i * kPrepThreads;
+      if (j < nq) {
+        const uint32_t* b = reinterpret_cast<const uint32_t*>(qr + j * kQ8Bytes);
+#pragma unroll
+        for (int w = 0; w < 9; ++w) blk[i][w] = __ldg(b + w);
+        m = fmaxf(m, fabsf(__half2float(__ushort_as_half(static_cast<unsigned short>(blk[i][0] & 0xFFFFu)))));
+      }
+    }
+  } else {
+    for (int j = tid; j < nq; j += kPrepThreads)
+      m = fmaxf(m, fabsf(__half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(qr + j * kQ8Bytes))))));
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((tid & 31) == 0) s_red[tid >> 5] = m;
@@ -436,16 +461,30 @@ __global__ void __launch_bounds__(kPrepThreads) tile_prep_kernel(const uint8_t* 
   }
   __syncthreads();
   const float inv = s_inv;
-  for (int j = tid; j < nq; j += kPrepThreads) {
-    const uint32_t* b = reinterpret_cast<const uint32_t*>(qr + j * kQ8Bytes);
-    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(__ldg(b) & 0xFFFFu))) * inv;
+  auto convert = [&](int j, const uint32_t (&b)[9]) {
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(b[0] & 0xFFFFu))) * inv;
     const __half2 d2 = __float2half2_rn(d);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       uint4 hv, lv;
-      acts_to_hilo(__ldg(b + 1 + 2 * g), __ldg(b + 2 + 2 * g), d2, hv, lv);
+      acts_to_hilo(b[1 + 2 * g], b[2 + 2 * g], d2, hv, lv);
       reinterpret_cast<uint4*>(hrow + kQK8 * j)[g] = hv;
       reinterpret_cast<uint4*>(lrow + kQK8 * j)[g] = lv;
+    }
+  };
+  if (held) {
+#pragma unroll
+    for (int i = 0; i < kPrepHeld; ++i) {
+      const int j = tid + i * kPrepThreads;
+      if (j < nq) convert(j, blk[i]);
+    }
+  } else {
+    for (int j = tid; j < nq; j += kPrepThreads) {
+      const uint32_t* b = reinterpret_cast<const uint32_t*>(qr + j * kQ8Bytes);
+      uint32_t r[9];
+#pragma unroll
+      for (int w = 0; w < 9; ++w) r[w] = __ldg(b + w);
+      convert(j, r);
     }
   }
 }
@@ -678,24 +717,27 @@ __global__ void __launch_bounds__(kTThreads, 1)
             break;
           }
           const uint32_t at = tmem + C::kA0 + ga * kBlockCols;
-          for (int q = 0; q < 4; ++q) {
+          for (int h = 0; h < 2; ++h) {
             if (!spin_wait_or_abort(&bfull_bar[rb], pb, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t db = d0 + ((rb * C::kBTile) >> 4);
+            const uint64_t db = d0 + ((rb * C::kBSlot) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < kStageK / 16; ++ks)
-              umma_ts(dt, at + 32u * q + 8u * ks, db + ((32u * ks) >> 4), C::kIdesc, (bi > 0 || q > 0 || ks > 0) ? 1u : 0u);
+            for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+              for (int ks = 0; ks < kStageK / 16; ++ks)
+                umma_ts(dt, at + 32u * (2 * h + qq) + 8u * ks, db + ((qq * C::kBTile + 32u * ks) >> 4), C::kIdesc,
+                        (bi > 0 || h > 0 || qq > 0 || ks > 0) ? 1u : 0u);
             umma_commit(&bempty_bar[rb]);
             issued = true;
             last_bar = &bempty_bar[rb];
             last_ph = pb;
             if (++rb == C::kRB) { rb = 0; pb ^= 1u; }
           }
-          // The A slot is released only after all four quarters' MMAs were
-          // issued (on an abort, those issued so far).
+          // The A slot is released only after both halves' MMAs were issued
+          // (on an abort, those issued so far).
           umma_commit(&aempty_bar[ga]);
           if (++ga == kGroups) { ga = 0; pa ^= 1u; }
         }
@@ -729,8 +771,9 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
   } else {
     // ------------------------------------------------ activation copies --
-    // Lane 0 waits for a free quarter slot and posts the byte count; lanes 0
-    // and 1 then issue the quarter's two copies (hi and lo rows) at once.
+    // Lane 0 waits for a free half-block slot and posts the byte count;
+    // lanes 0-3 then issue the half's four copies (two quarters x hi and lo
+    // rows) at once.
     pdl_wait();  // the B operand is written by the prep kernel
     int last_slot = -1;
     uint32_t last_ph = 0, rb = 0, pb = 0;
@@ -738,20 +781,22 @@ __global__ void __launch_bounds__(kTThreads, 1)
     int tok0 = nunits > 0 ? (unit_tile(0) % a.tiles_n) * TOK : 0;
     for (uint32_t j = 0; j < nall; ++j) {
       bool stop = false;
-      for (int q = 0; q < 4; ++q) {
+      for (int h = 0; h < 2; ++h) {
         int ok = 1;
         if (lane == 0) {
           ok = wait_or_abort(&bempty_bar[rb], pb ^ 1u, abort_flag) ? 1 : 0;
-          if (ok) mbar_arrive_expect_tx(&bfull_bar[rb], C::kBTile);
+          if (ok) mbar_arrive_expect_tx(&bfull_bar[rb], C::kBSlot);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           stop = true;
           break;
         }
-        if (lane < 2)
-          tma_load_2d(sm + rb * C::kBTile + lane * TOK * 128, &tmb, bi * kQK + q * kStageK, lane * a.t_pad + tok0,
-                      &bfull_bar[rb]);
+        if (lane < 4) {
+          const int qq = lane >> 1, hl = lane & 1;
+          tma_load_2d(sm + rb * C::kBSlot + qq * C::kBTile + hl * TOK * 128, &tmb, bi * kQK + (2 * h + qq) * kStageK,
+                      hl * a.t_pad + tok0, &bfull_bar[rb]);
+        }
         __syncwarp();
         last_slot = static_cast<int>(rb);
         last_ph = pb;

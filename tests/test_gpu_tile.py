@@ -22,6 +22,7 @@ SHAPES = [
     (130, 4096, 129),   # three token tiles, ragged
     (2000, 2048, 200),
     (5000, 2048, 520),  # more tiles than SMs: two tiles per CTA, accumulators reused
+    (300, 10240, 40),   # k > 8192: the prep kernel reads each token's blocks twice
     (300, 1280, 40),    # row stride not a multiple of 16 bytes: no workspace, other kernels
     (1000, 768, 37),
 ]
