@@ -36,17 +36,24 @@
 //       swizzled, K-major: the MMA's operand layout) with 2-D TMA into a ring
 //       of three half-block slots (64 KB each; fewer, larger slots mean fewer
 //       barrier waits and commits on the MMA thread);
-//     * A warps 0-7: group g = w/4 expands whole blocks g, g+2, g+4, ...
-//       for rows 32*(w%4) .. +31 into fp16 +-d_w and stores each quarter
+//     * A warps 0-7: group g = w/4 expands quarters 2g and 2g+1 of every
+//       block for rows 32*(w%4) .. +31 into fp16 +-d_w and stores them
 //       straight into tensor memory (tcgen05.st; a warp may only reach its
 //       own quarter of the TMEM lanes, which is exactly its rows), so the
-//       16-bit A operand never touches shared memory;
+//       16-bit A operand never touches shared memory.  Block j uses A slot
+//       j % 2, so a slot is free only once block j - 2's MMAs are done: both
+//       groups work on every block to halve the time from a slot's release
+//       to the block being ready (measured: one group per block 77.6 us, both
+//       75.3 us; four groups of one quarter each crowd the thread that issues
+//       the MMAs: 94.2 us);
 //     * epilogue warps 8-11: TMEM -> registers -> y;
 //     * warp 12: TMEM allocation; its lane 0 issues the MMAs (A from TMEM);
 //     * warps 13 and 14: the weight and the activation copies.
-//     The two groups work on two blocks at once and every ring slot belongs
-//     to one group, so every mbarrier parity wait is answered by the phase it
-//     waits for.
+//     A group reaches block j only after block j - 2's MMAs completed, which
+//     needed both groups' arrivals for j - 2, and a raw-weight slot is
+//     reloaded only after all A warps released it: no warp can run a phase
+//     ahead on a shared barrier, so every mbarrier parity wait is answered by
+//     the phase it waits for.
 //     Why 128 tokens and N = 256 rather than 64 tokens and N = 128: the A
 //     warps' integer work competes for issue slots with the thread that
 //     feeds the (shallow) MMA queue, and an N = 256 MMA keeps the tensor pipe
@@ -83,13 +90,13 @@ constexpr int kTileRows = 128;  // weight rows per tile = TMEM lanes
 constexpr int kStageK = 64;     // K per MMA stage (a quarter of a 256-block)
 constexpr int kWinBytes = 80;   // raw weight window per row and block (16-byte aligned)
 constexpr uint32_t kWRawBytes = kTileRows * kWinBytes;
-constexpr int kGroups = 2;      // A warp groups = tensor-memory block slots
-constexpr int kWSlotsPerGroup = 1;
-// Raw weight ring: one block per A group.  A group copies its block's raw
-// weights to registers first and frees the slot at once, so the next copy has
-// the group's whole expansion and its wait for a free A slot to land in (the
+constexpr int kGroups = 2;      // A warp groups: group g expands quarters 2g and 2g + 1 of every block
+constexpr int kASlots = 2;      // tensor-memory A block slots (block j uses slot j % 2)
+// Raw weight ring: one block per A slot.  Every A warp copies its row's raw
+// weights to registers first and releases the slot at once, so the next copy
+// has the block's expansion and the wait for a free A slot to land in (the
 // shared memory goes to the B ring instead).
-constexpr int kRW = kGroups * kWSlotsPerGroup;
+constexpr int kRW = kASlots;
 constexpr int kAWarps = 4 * kGroups, kEWarps = 4;
 constexpr int kEWarp0 = kAWarps, kMWarp = kEWarp0 + kEWarps, kPWarpW = kMWarp + 1, kPWarpB = kMWarp + 2;
 constexpr int kTThreads = (kPWarpB + 1) * 32;
@@ -109,7 +116,7 @@ struct TileCfg {
   static constexpr int kAccCols = N;                     // TMEM columns of the tile accumulator
   static constexpr int kA0 = kAccCols;                   // first TMEM column of the A slots
   static constexpr int kTmemCols = 512;
-  static_assert(kA0 + kGroups * kBlockCols <= kTmemCols, "tensor memory budget");
+  static_assert(kA0 + kASlots * kBlockCols <= kTmemCols, "tensor memory budget");
   static constexpr uint32_t kOffW = kRB * kBSlot;
   static constexpr uint32_t kSmem = kOffW + kRW * kWRawBytes + 1024;
   static_assert(kSmem + 2048 <= 232448, "shared memory budget");
@@ -495,7 +502,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   using C = TileCfg;
   constexpr int kBB = fmt_block_bytes<FMT>();
   extern __shared__ __align__(1024) uint8_t tsmem_raw[];
-  __shared__ __align__(8) uint64_t afull_bar[kGroups], aempty_bar[kGroups];
+  __shared__ __align__(8) uint64_t afull_bar[kASlots], aempty_bar[kASlots];
   __shared__ __align__(8) uint64_t bfull_bar[C::kRB], bempty_bar[C::kRB];
   __shared__ __align__(8) uint64_t wfull_bar[kRW], wempty_bar[kRW];
   __shared__ __align__(8) uint64_t accf_bar, acce_bar;  // the tile accumulator: full, free
@@ -530,8 +537,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
   int nunits = 0;
   while (unit_tile(nunits) < ntiles) ++nunits;
   const uint32_t nall = static_cast<uint32_t>(nunits * nblk);  // blocks of this CTA
-  // Block j goes to A group j % kGroups as that group's block c = j / kGroups;
-  // its raw weights use ring slot g * kWSlotsPerGroup + c % kWSlotsPerGroup.
+  // Block j of the CTA uses raw-weight slot (and A slot) j % 2, the slot's
+  // use number j / 2.
   auto issue_weights = [&](uint32_t j, uint32_t ws) {
     const int bi = static_cast<int>(j % nblk);
     const int row0 = (unit_tile(static_cast<int>(j / nblk)) / a.tiles_n) * kTileRows;
@@ -541,8 +548,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
   const uint32_t nfirst = nall < static_cast<uint32_t>(kRW) ? nall : static_cast<uint32_t>(kRW);
 
   if (tid == 0) {
-    for (int i = 0; i < kGroups; ++i) {
-      mbar_init(&afull_bar[i], 4);  // the 4 warps of the slot's A group
+    for (int i = 0; i < kASlots; ++i) {
+      mbar_init(&afull_bar[i], kAWarps);  // every A warp expands part of every block
       mbar_init(&aempty_bar[i], 1);
     }
     for (int i = 0; i < C::kRB; ++i) {
@@ -551,7 +558,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
     for (int i = 0; i < kRW; ++i) {
       mbar_init(&wfull_bar[i], 1);
-      mbar_init(&wempty_bar[i], 4);  // the 4 warps of the slot's A group
+      mbar_init(&wempty_bar[i], kAWarps);
     }
     mbar_init(&accf_bar, 1);
     mbar_init(&acce_bar, kEWarps);
@@ -563,7 +570,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   if (warp == 0) {
     __syncwarp();
     const uint32_t j = static_cast<uint32_t>(lane);
-    if (j < nfirst) issue_weights(j, (j % kGroups) * kWSlotsPerGroup + (j / kGroups) % kWSlotsPerGroup);
+    if (j < nfirst) issue_weights(j, j % kRW);
   }
   if (warp == kMWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_tmem)),
@@ -578,23 +585,20 @@ __global__ void __launch_bounds__(kTThreads, 1)
 
   if (warp < kAWarps) {
     // ---------------------------------------------------------------- A --
-    // Group g expands blocks j = g, g + 3, ... of the CTA into A slot g.
+    // Both groups work on every block j (A slot and raw-weight slot j % 2):
+    // group g expands quarters 2g and 2g + 1, so a block is ready in half the
+    // time one group would take (the two tensor-memory slots leave little
+    // time between a slot's release and the block's MMAs).
     const int g = warp >> 2;
     const int quarter = warp & 3;  // TMEM lane quarter = rows 32*quarter ..
     const int rl = (quarter << 5) | lane;
-    const uint32_t tslot = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kA0 + g * kBlockCols;
-    uint32_t c = 0;  // this group's blocks so far
-    int bi = g;      // j % nblk, advanced without a division
-    while (bi >= nblk && nblk > 0) bi -= nblk;
-    for (uint32_t j = g; j < nall; j += kGroups, ++c) {
-      if (c > 0) {
-        bi += kGroups;
-        while (bi >= nblk) bi -= nblk;
-      }
-      const uint32_t ws = static_cast<uint32_t>(g * kWSlotsPerGroup) + (c % kWSlotsPerGroup);
-      if (!warp_wait(&wfull_bar[ws], (c / kWSlotsPerGroup) & 1u, abort_flag)) break;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kA0 + static_cast<uint32_t>(64 * g);
+    int bi = 0;  // j % nblk, advanced without a division
+    for (uint32_t j = 0; j < nall; ++j, bi = bi + 1 == nblk ? 0 : bi + 1) {
+      const uint32_t sl = j & 1u, ph = (j >> 1) & 1u;
+      if (!warp_wait(&wfull_bar[sl], ph, abort_flag)) break;
       uint32_t W[20];
-      const uint4* src = reinterpret_cast<const uint4*>(wraw + ws * kWRawBytes + rl * kWinBytes);
+      const uint4* src = reinterpret_cast<const uint4*>(wraw + sl * kWRawBytes + rl * kWinBytes);
 #pragma unroll
       for (int cc = 0; cc < 5; ++cc) {
         const uint4 v = src[cc];
@@ -604,9 +608,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
         W[4 * cc + 3] = v.w;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&wempty_bar[ws]);
+      if (lane == 0) mbar_arrive(&wempty_bar[sl]);
       const uint32_t off = static_cast<uint32_t>(bi * kBB) & 15u;
       const uint32_t sh = (off & 2u) * 8u;
+      const uint32_t tslot = tlane + sl * kBlockCols;
       uint32_t out[32];
       if (FMT == kFmtTq2) {
         uint32_t wv[16], h;
@@ -620,16 +625,19 @@ __global__ void __launch_bounds__(kTThreads, 1)
         const uint32_t h2 = __half_as_ushort(__float2half_rn(2.0f * __half2float(__ushort_as_half(
                                 static_cast<unsigned short>(h)))));
         const uint32_t thi = h | (h2 << 16);  // bytes 4-5: +d_w, bytes 6-7: +2 d_w
-        if (!warp_wait(&aempty_bar[g], (c & 1u) ^ 1u, abort_flag)) break;
+        if (!warp_wait(&aempty_bar[sl], ph ^ 1u, abort_flag)) break;
         tc_fence_after();
-        expand_quarter_tq2<0>(wv, tlo, thi, out);
-        tmem_st32(tslot + 0 * 32, out);
-        expand_quarter_tq2<1>(wv, tlo, thi, out);
-        tmem_st32(tslot + 1 * 32, out);
-        expand_quarter_tq2<2>(wv, tlo, thi, out);
-        tmem_st32(tslot + 2 * 32, out);
-        expand_quarter_tq2<3>(wv, tlo, thi, out);
-        tmem_st32(tslot + 3 * 32, out);
+        if (g == 0) {
+          expand_quarter_tq2<0>(wv, tlo, thi, out);
+          tmem_st32(tslot + 0 * 32, out);
+          expand_quarter_tq2<1>(wv, tlo, thi, out);
+          tmem_st32(tslot + 1 * 32, out);
+        } else {
+          expand_quarter_tq2<2>(wv, tlo, thi, out);
+          tmem_st32(tslot + 0 * 32, out);
+          expand_quarter_tq2<3>(wv, tlo, thi, out);
+          tmem_st32(tslot + 1 * 32, out);
+        }
       } else {
         uint32_t wv[13], h;
         switch (off >> 2) {
@@ -640,22 +648,25 @@ __global__ void __launch_bounds__(kTThreads, 1)
         }
         const uint32_t tlo = h ^ 0x8000u;  // bytes 0-1: -d_w, bytes 2-3: 0
         const uint32_t thi = h;            // bytes 4-5: +d_w
-        // The slot is free once the MMAs of this group's previous block are done.
-        if (!warp_wait(&aempty_bar[g], (c & 1u) ^ 1u, abort_flag)) break;
+        // The slot is free once the MMAs of the block two before are done.
+        if (!warp_wait(&aempty_bar[sl], ph ^ 1u, abort_flag)) break;
         tc_fence_after();
-        expand_quarter<0>(wv, tlo, thi, out);
-        tmem_st32(tslot + 0 * 32, out);
-        expand_quarter<1>(wv, tlo, thi, out);
-        tmem_st32(tslot + 1 * 32, out);
-        expand_quarter<2>(wv, tlo, thi, out);
-        tmem_st32(tslot + 2 * 32, out);
-        expand_quarter<3>(wv, tlo, thi, out);
-        tmem_st32(tslot + 3 * 32, out);
+        if (g == 0) {
+          expand_quarter<0>(wv, tlo, thi, out);
+          tmem_st32(tslot + 0 * 32, out);
+          expand_quarter<1>(wv, tlo, thi, out);
+          tmem_st32(tslot + 1 * 32, out);
+        } else {
+          expand_quarter<2>(wv, tlo, thi, out);
+          tmem_st32(tslot + 0 * 32, out);
+          expand_quarter<3>(wv, tlo, thi, out);
+          tmem_st32(tslot + 1 * 32, out);
+        }
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull_bar[g]);
+      if (lane == 0) mbar_arrive(&afull_bar[sl]);
     }
   } else if (warp < kMWarp) {
     // --------------------------------------------------------- epilogue --
@@ -739,7 +750,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
           // The A slot is released only after both halves' MMAs were issued
           // (on an abort, those issued so far).
           umma_commit(&aempty_bar[ga]);
-          if (++ga == kGroups) { ga = 0; pa ^= 1u; }
+          if (++ga == kASlots) { ga = 0; pa ^= 1u; }
         }
         if (!ok) break;
         umma_commit(&accf_bar);
@@ -754,9 +765,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
       int last_slot = -1;
       uint32_t last_ph = 0;
       for (uint32_t j = nfirst; j < nall; ++j) {
-        const uint32_t g = j % kGroups, c = j / kGroups;
-        const uint32_t ws = g * kWSlotsPerGroup + (c % kWSlotsPerGroup);
-        const uint32_t ph = (c / kWSlotsPerGroup) & 1u;
+        const uint32_t ws = j % kRW;
+        const uint32_t ph = (j / kRW) & 1u;
         if (!wait_or_abort(&wempty_bar[ws], ph ^ 1u, abort_flag)) break;
         issue_weights(j, ws);
         last_slot = static_cast<int>(ws);
@@ -766,7 +776,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
       if (*abort_flag && last_slot >= 0) (void)mbar_wait(&wfull_bar[last_slot], last_ph);
       else if (*abort_flag && nfirst > 0) {
         for (uint32_t j = 0; j < nfirst; ++j)
-          (void)mbar_wait(&wfull_bar[(j % kGroups) * kWSlotsPerGroup + (j / kGroups) % kWSlotsPerGroup], 0);
+          (void)mbar_wait(&wfull_bar[j % kRW], 0);
       }
     }
   } else {
