@@ -100,8 +100,8 @@ constexpr int kRW = kASlots;
 constexpr int kAWarps = 4 * kGroups, kEWarps = 4;
 constexpr int kEWarp0 = kAWarps, kMWarp = kEWarp0 + kEWarps, kPWarpW = kMWarp + 1, kPWarpB = kMWarp + 2;
 constexpr int kTThreads = (kPWarpB + 1) * 32;
-constexpr int kPrepThreads = 128;
-constexpr int kPrepHeld = 2;  // Q8_1 blocks a prep thread keeps in registers (k <= 8192: one pass over q8)
+constexpr int kPrepThreads = 256;
+constexpr int kPrepHeld = 4;  // 8-value groups a prep thread keeps in registers (k <= 8192: one pass over q8)
 constexpr int kBlockCols = 4 * 32;  // TMEM columns of one block of A (4 quarters x 32)
 
 constexpr int TOK = 128;                               // tokens per tile
@@ -432,21 +432,28 @@ __global__ void __launch_bounds__(kPrepThreads) tile_prep_kernel(const uint8_t* 
     return;
   }
   const uint8_t* qr = q8 + static_cast<int64_t>(tok) * nq * kQ8Bytes;
-  // Up to kPrepHeld whole blocks per thread are read once, into registers,
-  // before the token's maximum scale is known; larger k reads the scales
-  // first and the blocks again afterwards.
-  const bool held = nq <= kPrepHeld * kPrepThreads;
-  uint32_t blk[kPrepHeld][9];
+  // A thread handles 8-value groups i = tid, tid + kPrepThreads, ... (group
+  // i: block i / 4, words 1 + 2 (i % 4) and 2 + 2 (i % 4) of it), so that the
+  // fp16 stores of consecutive lanes are consecutive 16-byte pieces.  Up to
+  // kPrepHeld groups per thread are read once, into registers, before the
+  // token's maximum scale is known; larger k reads them again afterwards.
+  const int ng = k / 8;
+  const bool held = ng <= kPrepHeld * kPrepThreads;
+  uint32_t gq[kPrepHeld][2], gd[kPrepHeld];
+  auto load_group = [&](int i, uint32_t& q0, uint32_t& q1, uint32_t& d) {
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(qr + (i >> 2) * kQ8Bytes);
+    d = __ldg(b) & 0xFFFFu;
+    q0 = __ldg(b + 1 + 2 * (i & 3));
+    q1 = __ldg(b + 2 + 2 * (i & 3));
+  };
   float m = 0.0f;
   if (held) {
 #pragma unroll
-    for (int i = 0; i < kPrepHeld; ++i) {
-      const int j = tid + i * kPrepThreads;
-      if (j < nq) {
-        const uint32_t* b = reinterpret_cast<const uint32_t*>(qr + j * kQ8Bytes);
-#pragma unroll
-        for (int w = 0; w < 9; ++w) blk[i][w] = __ldg(b + w);
-        m = fmaxf(m, fabsf(__half2float(__ushort_as_half(static_cast<unsigned short>(blk[i][0] & 0xFFFFu)))));
+    for (int r = 0; r < kPrepHeld; ++r) {
+      const int i = tid + r * kPrepThreads;
+      if (i < ng) {
+        load_group(i, gq[r][0], gq[r][1], gd[r]);
+        m = fmaxf(m, fabsf(__half2float(__ushort_as_half(static_cast<unsigned short>(gd[r])))));
       }
     }
   } else {
@@ -468,30 +475,24 @@ __global__ void __launch_bounds__(kPrepThreads) tile_prep_kernel(const uint8_t* 
   }
   __syncthreads();
   const float inv = s_inv;
-  auto convert = [&](int j, const uint32_t (&b)[9]) {
-    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(b[0] & 0xFFFFu))) * inv;
-    const __half2 d2 = __float2half2_rn(d);
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint4 hv, lv;
-      acts_to_hilo(b[1 + 2 * g], b[2 + 2 * g], d2, hv, lv);
-      reinterpret_cast<uint4*>(hrow + kQK8 * j)[g] = hv;
-      reinterpret_cast<uint4*>(lrow + kQK8 * j)[g] = lv;
-    }
+  auto convert = [&](int i, uint32_t q0, uint32_t q1, uint32_t d16) {
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(d16))) * inv;
+    uint4 hv, lv;
+    acts_to_hilo(q0, q1, __float2half2_rn(d), hv, lv);
+    reinterpret_cast<uint4*>(hrow)[i] = hv;
+    reinterpret_cast<uint4*>(lrow)[i] = lv;
   };
   if (held) {
 #pragma unroll
-    for (int i = 0; i < kPrepHeld; ++i) {
-      const int j = tid + i * kPrepThreads;
-      if (j < nq) convert(j, blk[i]);
+    for (int r = 0; r < kPrepHeld; ++r) {
+      const int i = tid + r * kPrepThreads;
+      if (i < ng) convert(i, gq[r][0], gq[r][1], gd[r]);
     }
   } else {
-    for (int j = tid; j < nq; j += kPrepThreads) {
-      const uint32_t* b = reinterpret_cast<const uint32_t*>(qr + j * kQ8Bytes);
-      uint32_t r[9];
-#pragma unroll
-      for (int w = 0; w < 9; ++w) r[w] = __ldg(b + w);
-      convert(j, r);
+    for (int i = tid; i < ng; i += kPrepThreads) {
+      uint32_t q0, q1, d;
+      load_group(i, q0, q1, d);
+      convert(i, q0, q1, d);
     }
   }
 }
