@@ -46,9 +46,11 @@
 //       to the block being ready (measured: one group per block 77.6 us, both
 //       75.3 us; four groups of one quarter each crowd the thread that issues
 //       the MMAs: 94.2 us);
-//     * epilogue warps 8-11: TMEM -> registers -> y;
-//     * warp 12: TMEM allocation; its lane 0 issues the MMAs (A from TMEM);
-//     * warps 13 and 14: the weight and the activation copies.
+//     * epilogue warps 8-15 (two per TMEM lane quarter, 64 tokens each):
+//       TMEM -> registers, release the accumulator, then scale and store y
+//       while the next tile's MMAs run;
+//     * warp 16: TMEM allocation; its lane 0 issues the MMAs (A from TMEM);
+//     * warps 17 and 18: the weight and the activation copies.
 //     A group reaches block j only after block j - 2's MMAs completed, which
 //     needed both groups' arrivals for j - 2, and a raw-weight slot is
 //     reloaded only after all A warps released it: no warp can run a phase
@@ -97,7 +99,7 @@ constexpr int kASlots = 2;      // tensor-memory A block slots (block j uses slo
 // has the block's expansion and the wait for a free A slot to land in (the
 // shared memory goes to the B ring instead).
 constexpr int kRW = kASlots;
-constexpr int kAWarps = 4 * kGroups, kEWarps = 4;
+constexpr int kAWarps = 4 * kGroups, kEWarps = 8;  // two epilogue warps per TMEM lane quarter
 constexpr int kEWarp0 = kAWarps, kMWarp = kEWarp0 + kEWarps, kPWarpW = kMWarp + 1, kPWarpB = kMWarp + 2;
 constexpr int kTThreads = (kPWarpB + 1) * 32;
 constexpr int kPrepThreads = 256;
@@ -673,6 +675,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     // --------------------------------------------------------- epilogue --
     const int quarter = warp & 3;  // TMEM lane quarter this warp may read
     const int rl = quarter * 32 + lane;
+    const int c_lo = ((warp - kEWarp0) >> 2) * (TOK / 2);  // this warp's half of the tile's tokens
     float* tsc = s_tscale[warp - kEWarp0];
     pdl_wait();  // the scales are written by the prep kernel
     for (int u = 0; u < nunits; ++u) {
@@ -682,30 +685,39 @@ __global__ void __launch_bounds__(kTThreads, 1)
       const uint32_t aph = static_cast<uint32_t>(u) & 1u;
       // Scales of this tile's tokens, fetched while the MMAs run.
       __syncwarp();
-      for (int tl = lane; tl < TOK; tl += 32) tsc[tl] = __ldg(a.scale + tok0 + tl);
+      for (int tl = c_lo + lane; tl < c_lo + TOK / 2; tl += 32) tsc[tl] = __ldg(a.scale + tok0 + tl);
       __syncwarp();
       if (!warp_wait(&accf_bar, aph, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-#pragma unroll 1
-      for (int c0 = 0; c0 < TOK; c0 += C::kChunk) {
+      // Read the warp's 64 tokens (hi + lo) out of tensor memory first and
+      // release the accumulator, so the next tile's MMAs run while these
+      // outputs are scaled and stored (all CTAs finish a tile at about the
+      // same time, and the y writes of that moment are bandwidth-bound).
+      float sum[2][C::kChunk];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
         uint32_t vh[C::kChunk], vl[C::kChunk];
-        tmem_ld<C::kChunk>(tbase + c0, vh);
-        tmem_ld<C::kChunk>(tbase + TOK + c0, vl);
+        tmem_ld<C::kChunk>(tbase + c_lo + h * C::kChunk, vh);
+        tmem_ld<C::kChunk>(tbase + TOK + c_lo + h * C::kChunk, vl);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
+        for (int jj = 0; jj < C::kChunk; ++jj) sum[h][jj] = __uint_as_float(vh[jj]) + __uint_as_float(vl[jj]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
         for (int jj = 0; jj < C::kChunk; ++jj) {
-          const int tl = c0 + jj, tok = tok0 + tl;
-          const float v = (__uint_as_float(vh[jj]) + __uint_as_float(vl[jj])) * tsc[tl];
+          const int tl = c_lo + h * C::kChunk + jj, tok = tok0 + tl;
+          const float v = sum[h][jj] * tsc[tl];
           if (row < a.n && tok < a.t) {
             const int64_t yi = static_cast<int64_t>(tok) * a.n + row;
             a.y[yi] = a.res ? v + a.res[yi] : v;
           }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_bar);
     }
   } else if (warp == kMWarp) {
     // -------------------------------------------------------------- MMA --
