@@ -113,25 +113,23 @@ __global__ void __launch_bounds__(kMThreads, 3) moe_small_kernel(const MoeArgs a
     const uint8_t* wtask = a.w + (static_cast<int64_t>(e) * a.n + r0) * rowbytes;
     const uint32_t wlow = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(wtask));
 
-    if (tid == 0) {
-      // One bulk copy per 4-row group, from the 16-byte boundary at or below
-      // the group; the bytes past the last 16-byte boundary with plain loads.
-      // Groups past this task's rows complete their phase with no bytes, so
-      // every barrier advances once per task.
-      for (int g = 0; g < ngroups_max; ++g) {
-        if (g < ngroups) {
-          const int grows = min(kRowsPerTask, rows - g * kRowsPerTask);
-          const uint8_t* src = wtask + static_cast<int64_t>(g) * kRowsPerTask * rowbytes;
-          const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
-          const uint32_t tot = delta + static_cast<uint32_t>(grows) * rowbytes;
-          const uint32_t main = tot & ~15u;
-          uint8_t* dst = slab + static_cast<uint32_t>(g) * gstride;
-          for (uint32_t i = main; i < tot; ++i) dst[i] = __ldg(src - delta + i);
-          mbar_arrive_expect_tx(&bars[g], main);
-          if (main) bulk_g2s(dst, src - delta, main, &bars[g], policy);
-        } else {
-          mbar_arrive_expect_tx(&bars[g], 0);
-        }
+    // One bulk copy per 4-row group (thread g issues group g's), from the
+    // 16-byte boundary at or below the group; the bytes past the last 16-byte
+    // boundary with plain loads.  Groups past this task's rows complete their
+    // phase with no bytes, so every barrier advances once per task.
+    for (int g = tid; g < ngroups_max; g += kMThreads) {
+      if (g < ngroups) {
+        const int grows = min(kRowsPerTask, rows - g * kRowsPerTask);
+        const uint8_t* src = wtask + static_cast<int64_t>(g) * kRowsPerTask * rowbytes;
+        const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
+        const uint32_t tot = delta + static_cast<uint32_t>(grows) * rowbytes;
+        const uint32_t main = tot & ~15u;
+        uint8_t* dst = slab + static_cast<uint32_t>(g) * gstride;
+        for (uint32_t i = main; i < tot; ++i) dst[i] = __ldg(src - delta + i);
+        mbar_arrive_expect_tx(&bars[g], main);
+        if (main) bulk_g2s(dst, src - delta, main, &bars[g], policy);
+      } else {
+        mbar_arrive_expect_tx(&bars[g], 0);
       }
     }
     if (tid < kChunk) s_pair[tid] = tid < pc ? plist[bounds[e] + chunk * kChunk + tid] : 0;
