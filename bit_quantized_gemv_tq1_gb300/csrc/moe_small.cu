@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectAr
     for (int g = 0; g < ngroups; ++g) mbar_init(&bars[g], 1);
     fence_mbar_init();
   }
+  __syncthreads();  // the barriers are initialised before any thread arms one
   pdl_wait();  // ids and activations may come from the previous kernel
   const int e = __ldg(a.ids + pair);
   if (e < 0 || e >= a.n_experts) {
@@ -274,9 +275,9 @@ __global__ void __launch_bounds__(kDThreads, 2) moe_direct_kernel(const DirectAr
   }
   const uint8_t* wtask = a.w + (static_cast<int64_t>(e) * a.n + r0) * rowbytes;
   const uint32_t wlow = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(wtask));
-  if (tid == 0) {
+  {  // one bulk copy per 4-row group, thread g issuing group g's
     const uint64_t policy = l2_evict_first_policy();
-    for (int g = 0; g < ngroups; ++g) {
+    for (int g = tid; g < ngroups; g += kDThreads) {
       const int grows = min(kRowsPerTask, rows - g * kRowsPerTask);
       const uint8_t* src = wtask + static_cast<int64_t>(g) * kRowsPerTask * rowbytes;
       const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
