@@ -367,6 +367,11 @@ static int mmv_id_common(const void* expert_blocks, int64_t n_experts, const voi
     return launch_moe_direct(w, a, ids, y, n, k, top_k, n_experts, t * top_k, plan, s, st, act_div, fmt, part);
   const bool small = moe_small_plan(n, k, t * top_k, n_experts, &plan, fmt);
   if (part && !small) return TQ1_ERR_UNSUPPORTED;  // partials come from the routed decode kernels only
+  if (small && moe_table_smem(n_experts, t * top_k) <= kMoeTableSmemMax) {
+    // Few pairs: the routed decode kernel builds the routing table itself.
+    rc = launch_moe_small(w, a, y, n, k, top_k, n_experts, t * top_k, plan, nullptr, s, st, act_div, fmt, part, ids);
+    if (rc != TQ1_ERR_UNSUPPORTED || part) return rc;
+  }
   rc = launch_moe_compact(ids, t, top_k, n_experts, small ? plan.chunk : 1, small ? plan.row_blocks : 1, table, s,
                           st);
   if (rc != TQ1_OK) return rc;

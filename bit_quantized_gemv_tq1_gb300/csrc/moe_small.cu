@@ -46,7 +46,8 @@ struct MoeArgs {
   float* y;              // [t * top_k][n]
   int32_t* part;         // PART: exact partials [t * top_k][n][k/32] (y unused)
   unsigned* status;
-  const int32_t* table;  // compacted routing table (layout in tq1_internal.h)
+  const int32_t* table;  // compacted routing table (layout in tq1_internal.h), or
+  const int32_t* ids;    // the ids themselves ([t][top_k]): every CTA builds the table in shared memory
   int64_t n;
   int n_experts, top_k, nb, nkc;
   int act_div;           // activation row of a pair = pair / act_div (top_k, or 1: one row per pair)
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kMThreads, 3) moe_small_kernel(const MoeArgs a
   float* part = reinterpret_cast<float*>(recs + static_cast<size_t>(kChunk) * rstride);
   __shared__ __align__(8) uint64_t bars[kMaxGroupsM];
   __shared__ int s_abort;
+  __shared__ int s_nact;
   __shared__ int s_pair[kChunk];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -89,7 +91,87 @@ __global__ void __launch_bounds__(kMThreads, 3) moe_small_kernel(const MoeArgs a
   const int32_t* active = bounds + (a.n_experts + 1);
   const int32_t* plist = active + a.n_experts;
   const int32_t* tstart = plist + a.pairs;
-  const int n_active = a.table[0];
+  int n_active = 0;
+  if (a.ids) {
+    // Few routed pairs: every CTA builds the routing table itself, in shared
+    // memory, with the compaction kernel's steps (counts, one warp's scans,
+    // one warp's stable scatter), so there is no second kernel before this
+    // one.  The table (same layout as the compaction's, without the count
+    // word) follows the partials.
+    const int ne = a.n_experts;
+    int32_t* t_cnt = reinterpret_cast<int32_t*>(part + static_cast<size_t>(a.rows) * nkc * kChunk);
+    int32_t* t_bounds = t_cnt + ne;
+    int32_t* t_active = t_bounds + ne + 1;
+    int32_t* t_tstart = t_active + ne;
+    int32_t* t_plist = t_tstart + ne + 1;
+    for (int i = tid; i < ne; i += kMThreads) t_cnt[i] = 0;
+    __syncthreads();
+    for (int64_t p = tid; p < a.pairs; p += kMThreads) {
+      const int e = __ldg(a.ids + p);
+      if (e >= 0 && e < ne) atomicAdd(&t_cnt[e], 1);
+      else if (blockIdx.x == 0) raise_status(a.status, kStatusBadId);
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive scans of the counts and the tasks, and the active list
+      int running = 0, nact = 0, running_tasks = 0;
+      for (int base = 0; base < ne; base += 32) {
+        const int i = base + lane;
+        const int v = i < ne ? t_cnt[i] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        if (i < ne) t_bounds[i] = running + incl - v;
+        const uint32_t has = __ballot_sync(0xffffffffu, v > 0);
+        const int nt = v > 0 ? ((v + kChunk - 1) / kChunk) * a.row_blocks : 0;
+        int tincl = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, tincl, o);
+          if (lane >= o) tincl += u;
+        }
+        if (v > 0) {
+          const int slot = nact + __popc(has & ((1u << lane) - 1u));
+          t_active[slot] = i;
+          t_tstart[slot] = running_tasks + tincl - nt;
+        }
+        nact += __popc(has);
+        running += __shfl_sync(0xffffffffu, incl, 31);
+        running_tasks += __shfl_sync(0xffffffffu, tincl, 31);
+      }
+      if (lane == 0) {
+        t_bounds[ne] = running;
+        t_tstart[nact] = running_tasks;
+        s_nact = nact;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < ne; i += kMThreads) t_cnt[i] = t_bounds[i];  // scatter cursors
+    __syncthreads();
+    if (warp == 0) {  // stable scatter of pair indices, 32 at a time, in order
+      for (int64_t base = 0; base < a.pairs; base += 32) {
+        const int64_t p = base + lane;
+        int e = p < a.pairs ? __ldg(a.ids + p) : -1;
+        if (e >= ne || e < -1) e = -1;
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0) t_plist[t_cnt[e] + rank] = static_cast<int32_t>(p);
+        __syncwarp();
+        if (e >= 0 && rank == 0) t_cnt[e] += __popc(peers);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    bounds = t_bounds;
+    active = t_active;
+    plist = t_plist;
+    tstart = t_tstart;
+    n_active = s_nact;
+  } else {
+    n_active = a.table[0];
+  }
   const int total = tstart[n_active];
   const uint64_t policy = l2_evict_first_policy();
   uint32_t iter = 0;  // tasks done by this CTA: every group barrier completes one phase per task
@@ -444,9 +526,10 @@ bool moe_small_plan(int64_t n, int64_t k, int64_t pairs, int64_t n_experts, MoeP
 
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
-                     unsigned* status, int act_div, int fmt, int32_t* part) {
+                     unsigned* status, int act_div, int fmt, int32_t* part, const int32_t* ids) {
   const DeviceInfo& di = device_info();
   MoeArgs a = {};
+  a.ids = ids;
   a.part = part;
   a.act_div = act_div;
   a.w = w;
@@ -465,7 +548,8 @@ int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, i
   const uint32_t rowbytes = static_cast<uint32_t>(a.nb) * (fmt == kFmtTq2 ? kTq2BlockBytes : kBlockBytes);
   a.slab_bytes = static_cast<uint32_t>(plan.rows / kRowsPerTask) * group_stride(rowbytes);
   const size_t smem = a.slab_bytes + static_cast<size_t>(kChunk) * a.nb * kPRec * 4 +
-                      static_cast<size_t>(plan.rows) * a.nkc * kChunk * 4;
+                      static_cast<size_t>(plan.rows) * a.nkc * kChunk * 4 + (ids ? moe_table_smem(n_experts, pairs) : 0);
+  if (smem > kMoeSmemBudget) return TQ1_ERR_UNSUPPORTED;
   const int kv = (fmt == kFmtTq2 ? 1 : 0) + (part ? 2 : 0);
   auto kern = kv == 0   ? moe_small_kernel<kFmtTq1, false>
               : kv == 1 ? moe_small_kernel<kFmtTq2, false>

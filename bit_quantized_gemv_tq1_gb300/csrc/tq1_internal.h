@@ -113,8 +113,16 @@ bool moe_direct_plan(int64_t n, int64_t k, int64_t pairs, MoePlan* plan, int fmt
 int launch_moe_direct(const uint8_t* w, const uint8_t* q8, const int32_t* ids, float* y, int64_t n, int64_t k,
                       int64_t top_k, int64_t n_experts, int64_t pairs, const MoePlan& plan, cudaStream_t s,
                       unsigned* status, int act_div, int fmt = 0, int32_t* part = nullptr);
+// With `ids` (and `ws` unused) every CTA builds the routing table itself in
+// shared memory (moe_table_smem bytes; for few pairs and experts: at most
+// kMoeTableSmemMax), so no compaction kernel runs before it.
 int launch_moe_small(const uint8_t* w, const uint8_t* q8, float* y, int64_t n, int64_t k, int64_t top_k,
                      int64_t n_experts, int64_t pairs, const MoePlan& plan, const int32_t* ws, cudaStream_t s,
-                     unsigned* status, int act_div, int fmt = 0, int32_t* part = nullptr);
+                     unsigned* status, int act_div, int fmt = 0, int32_t* part = nullptr,
+                     const int32_t* ids = nullptr);
+inline size_t moe_table_smem(int64_t n_experts, int64_t pairs) {
+  return static_cast<size_t>(4 * n_experts + 2 + pairs) * sizeof(int32_t);
+}
+constexpr size_t kMoeTableSmemMax = 16 * 1024;
 
 }  // namespace tq1
