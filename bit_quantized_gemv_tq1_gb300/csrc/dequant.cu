@@ -63,9 +63,16 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
     boff = 48;              // qh[0..3], digits 2 (lane - 30) and 2 (lane - 30) + 1
     dig = 2 * (lane - 30);
   }
+  // The warp's units are u = first, first + wstride, ...; their (output row,
+  // block) advance by the stride's quotient and remainder (one division per
+  // warp instead of one per unit).
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kDqWarps + (threadIdx.x >> 5);
+  const int64_t sq = wstride / nb;
+  const int sr = static_cast<int>(wstride - sq * nb);
+  int64_t crow = first / nb;  // the next unit's output row and block
+  int cb = static_cast<int>(first - crow * nb);
   // kDqUnits units per iteration: their loads are in flight together.
-  for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * kDqWarps + (threadIdx.x >> 5); u0 < units;
-       u0 += kDqUnits * wstride) {
+  for (int64_t u0 = first; u0 < units; u0 += kDqUnits * wstride) {
     uint32_t hw[kDqUnits][5];  // per unit: 4 halfwords of the lane's bytes, the fp16 scale
     int64_t orow[kDqUnits];
     int bb[kDqUnits];
@@ -74,8 +81,14 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
     for (int x = 0; x < kDqUnits; ++x) {
       const int64_t u = u0 + x * wstride;
       live[x] = u < units;
-      orow[x] = live[x] ? u / nb : 0;
-      bb[x] = static_cast<int>(u - orow[x] * nb);
+      orow[x] = crow;
+      bb[x] = cb;
+      crow += sq;
+      cb += sr;
+      if (cb >= nb) {
+        cb -= nb;
+        ++crow;
+      }
       int64_t srow = orow[x];
       if (live[x] && row_ids) {
         srow = __ldg(row_ids + orow[x]);
