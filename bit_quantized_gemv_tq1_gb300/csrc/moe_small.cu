@@ -215,15 +215,17 @@ __global__ void __launch_bounds__(kMThreads, 3) moe_small_kernel(const MoeArgs a
       }
     }
     if (tid < kChunk) s_pair[tid] = tid < pc ? plist[bounds[e] + chunk * kChunk + tid] : 0;
-    __syncthreads();
-    // Activation records of the task's pairs (token = pair / top_k).
+    // Activation records of the task's pairs (token = pair / top_k), each
+    // thread reading its pair from the table (s_pair is read after the next
+    // barrier only).
     {
       const int nchunks = pc * nb * 8;
+      const int32_t* tpairs = plist + bounds[e] + chunk * kChunk;
       for (int i = tid; i < nchunks; i += kMThreads) {
         const int c = i / (nb * 8);
         const int rem = i - c * nb * 8;
         const int b = rem >> 3, j = rem & 7;
-        const int64_t token = s_pair[c] / a.act_div;
+        const int64_t token = tpairs[c] / a.act_div;
         fill_precord_chunk(a.q8 + (token * nb * 8 + b * 8 + j) * kQ8Bytes, recs + c * rstride + b * kPRec, j);
       }
     }
