@@ -265,3 +265,24 @@ def test_tq2_per_slot_activations(t, top_k, n_experts):
             e = int(m.ids[c, s])
             ref[c, s] = orc.tq2_mmv_f64(ob[e], oq[c * top_k + s], m.n, m.k, 1)[0]
     G.assert_close(y, ref)
+
+
+def test_large_expert_count_runs_the_compaction_kernel():
+    # 1100 experts: the routing table (four words per expert plus one per
+    # pair) is larger than the routed kernel builds in shared memory, so the
+    # compaction kernel writes it into the workspace first; 40 pairs take the
+    # compacted mode.  Outputs and exact partials against the oracle.
+    m = synth.moe(1100, 64, 512, 20, 2, seed=77)
+    t_ = G.torch()
+    eb = m.n * (m.k // 256) * 54
+    used = np.unique(m.ids)
+    blocks = t_.zeros(m.n_experts * eb, dtype=t_.uint8, device="cuda")
+    for e in used:
+        blocks[e * eb:(e + 1) * eb] = G.quantize_rows(m.expert_weights(int(e)))
+    q8 = G.quantize_acts(m.x)
+    y, st = _mmv_id(blocks, m, m.ids, q8)
+    assert st == 0
+    ob = _oracle_blocks(m, used)
+    G.assert_close(G.host(y), orc.mmv_id_f64(ob, m.n_experts, orc.q8_1_quantize(m.x), m.ids, m.n, m.k, m.t, m.top_k))
+    rows = np.arange(m.n)
+    np.testing.assert_array_equal(_mmv_id_partials(blocks, m, m.ids, q8), _oracle_id_partials(m, m.ids, rows))
