@@ -6,10 +6,14 @@
 // into per-expert bounds and runs a grid over the compacted list, so each
 // expert's weights are read once for all the tokens routed to it.  Here a
 // task is (active expert, a chunk of up to kChunk of its (token, slot)
-// pairs, a range of its rows); the compaction kernel lays the tasks of each
-// active expert out contiguously and records where they start.  Persistent
-// CTAs walk the tasks: per task they request the rows' packed weights with
-// one 1-D bulk copy (TMA engine) per 4-row group, stage the chunk's
+// pairs, a range of its rows); the routing table lays the tasks of each
+// active expert out contiguously and records where they start.  For small
+// routings every CTA builds that table itself in shared memory (the
+// compaction kernel's steps; no second kernel ahead of this one), larger ones
+// read it from the workspace the compaction kernel filled.  Persistent CTAs
+// walk the tasks: per task they request the rows' packed weights with one
+// 1-D bulk copy (TMA engine) per 4-row group, each group's copy issued by its
+// own thread, stage the chunk's
 // activation records, and run the decode kernel's expansion and dot products
 // (packed 2-bit digits, masked dp4a) for every pair of the chunk, so each
 // packed weight byte is expanded once per chunk.  Outputs go to
