@@ -238,7 +238,9 @@ int tq1_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void
 /*
  * Workspace bytes tq1_mmv_id needs for n_experts experts and t*top_k routed
  * pairs (the compacted routing table: n_active, expert bounds, active
- * experts, sorted pairs, task offsets).
+ * experts, sorted pairs, task offsets).  Small routings (four words per
+ * expert plus one per pair within 16 KiB) build the table inside the routed
+ * kernel and leave the workspace untouched; it is required all the same.
  * Source: AMD-Ecosystem/llama.cpp PR #76, "Summary" (ids -> expert_bounds ->
  * compacted grid: the table this workspace holds).
  */
