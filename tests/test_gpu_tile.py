@@ -104,3 +104,23 @@ def test_workspace_too_small_is_refused_before_launch():
     assert rc == -5  # TQ1_ERR_WORKSPACE
     assert L.tq1_sync_status() == 0
     assert np.all(G.host(y) == 7.0)  # nothing ran
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_tile_residual_epilogue(in_place):
+    # y = res + W x through the tile path's epilogue (tq1_mmv_ws with res),
+    # a separate residual buffer and in place (y is the residual).
+    n, k, t = 200, 2048, 140
+    p = synth.matvec(n, k, t, seed=303)
+    blocks, q8 = G.quantize_rows(p.w), G.quantize_acts(p.x)
+    res = np.random.default_rng(5).standard_normal((t, n)).astype(np.float32)
+    L, torch = G.lib(), G.torch()
+    ws_bytes = L.tq1_mmv_workspace_size(n, k, t)
+    assert ws_bytes > 0
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    r = G.dev(res)
+    y = r if in_place else torch.full((t, n), float("nan"), dtype=torch.float32, device="cuda")
+    L.tq1_mmv_ws(blocks, q8, y, n, k, t, ws, ws_bytes, res=r)
+    assert L.tq1_sync_status() == 0
+    ref = orc.mmv_f64(orc.tq1_encode_rows(p.w), orc.q8_1_quantize(p.x), n, k, t) + res.astype(np.float64)
+    G.assert_close(G.host(y), ref)
