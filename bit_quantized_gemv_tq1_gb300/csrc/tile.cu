@@ -192,7 +192,7 @@ __device__ __forceinline__ bool spin_wait_or_abort(uint64_t* bar, uint32_t parit
   }
 }
 
-// Lane 0 waits; the verdict is broadcast and the warp re-converges, which
+// Lane 0 waits; the outcome is broadcast and the warp re-converges, which
 // orders the other lanes' later accesses after the wait.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   int ok = 1;
