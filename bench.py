@@ -597,13 +597,16 @@ def fused_chain_bench(lib, L, synth, dev, stream, capture, args) -> dict:
 
 def dequant_bench(lib, L, synth, dev, stream, capture, args) -> dict:
     """Dequantisation of config 2's matrix (N=5120, K=6144) to fp32 and fp16,
-    cycling weight copies; bytes = packed weights read + values written."""
+    cycling weight copies and output buffers (each over 2x L2 in total, so
+    neither the weights nor the written rows are still in L2 when a call
+    reaches them again); bytes = packed weights read + values written."""
     import torch
 
     c2 = synth.CONFIGS["c2"]
     n, k = c2["n"], c2["k"]
     wbytes = n * (k // QK) * BLOCK_BYTES
-    copies = 20
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20))
+    copies = -(-2 * l2 // wbytes)
     gen = torch.Generator(device=dev)
     gen.manual_seed(2000)
     blocks = torch.empty(copies * wbytes, dtype=torch.uint8, device=dev)
@@ -614,11 +617,14 @@ def dequant_bench(lib, L, synth, dev, stream, capture, args) -> dict:
     peak = float(measured_peaks()["hbm_gbs"])
     out = {"workload": "c2 matrix N=5120 K=6144 -> fp32 / fp16 rows"}
     for f16 in (False, True):
-        y = torch.empty((n, k), dtype=torch.float16 if f16 else torch.float32, device=dev)
+        obytes = n * k * (2 if f16 else 4)
+        ocopies = -(-2 * l2 // obytes)
+        y = torch.empty((ocopies, n, k), dtype=torch.float16 if f16 else torch.float32, device=dev)
 
-        def calls(s, y=y, f16=f16):
+        def calls(s, y=y, f16=f16, ocopies=ocopies):
             for l in range(copies):
-                assert lib.tq1_dequantize_rows(blocks.data_ptr() + l * wbytes, y.data_ptr(), n, k, int(f16), s) == 0
+                assert lib.tq1_dequantize_rows(blocks.data_ptr() + l * wbytes, y[l % ocopies].data_ptr(), n, k,
+                                               int(f16), s) == 0
 
         g = capture(calls)
         ms = _time_graph(g, stream, 5) / copies

@@ -7,16 +7,25 @@
 // the number of 8-token n-tiles (NT = 1..4) one mma covers, so a call pays for
 // ceil(t / 8) tiles of tokens, never for 32.
 //
-// Exactness.  A holds d_w * trit (trit in {-1, 0, +1}: exact in fp16), B holds
-// the Q8_1 integers q (|q| <= 127: exact in fp16).  Each product is an exact
-// multiple of d_w's last place, and a 32-element chunk's sum (at most 4064
-// d_w) needs 23 bits, so the fp32 accumulation of one chunk is exact: the
-// tensor core returns d_w * I_j, I_j the chunk's exact integer partial
-// (PrismML-Eng/llama.cpp issue #139, "Current behavior": the per-32-block
-// integer dot product).  Every chunk starts from a zero accumulator; the
-// epilogue adds d_a[j] * (d_w * I_j) in fp32, chunk by chunk, in a fixed
-// order.  The partials mode (the debug entry points) uses the unscaled table
-// {-1, 0, +1}, so the accumulator is I_j itself, stored as int32.
+// Exactness.  B holds the Q8_1 integers q (|q| <= 127: exact in fp16).  On the
+// rung of one n-tile, A holds 1024 + digit (digit = trit + 1 in
+// {0, 1, 2}; TQ2_0's code 0..3), an exact fp16 integer, and each chunk's
+// accumulator starts at -1025 * sum(q) (the chunk's activations summed
+// exactly when they are staged): the tensor core returns
+// sum((1024 + digit) q) - 1025 sum(q) = sum((digit - 1) q) = I_j, the chunk's
+// exact integer partial (PrismML-Eng/llama.cpp issue #139, "Current
+// behavior": the per-32-block integer dot product); every product and partial
+// sum on the way is an integer below 2^22 in magnitude, so the fp32
+// accumulation is exact.  The epilogue sums d_a[j] * I_j over a block's chunks
+// and adds that sum times d_w to the row's total.  On the rungs of two to
+// four n-tiles (whose registers are fuller) A holds d_w * trit from a per-row
+// table: each product is an exact
+// multiple of d_w's last place and a chunk's sum (at most 4064 d_w) needs 23
+// bits, so the tensor core returns d_w * I_j from a zero accumulator and the
+// epilogue adds d_a[j] * (d_w * I_j).  Either way in fp32, chunk by chunk, in a
+// fixed order.  The partials mode (the debug entry points) takes I_j from the
+// first form, or from the second with the unscaled table {-1, 0, +1}, and
+// stores it as int32.
 //
 // Expansion (byte-major, each packed byte loaded once: issue #139, "Proposed
 // approach").  A thread (group g = lane / 4, q = lane % 4) of a warp holds
@@ -27,7 +36,9 @@
 // 0/1, 2/3, 4) and digit q of the four qh bytes.  A digit word (four digits
 // 0..2 in byte lanes, P_{k+1} - 3 P_k with P_k = floor(b 3^k / 256) from
 // 16-bit-lane multiplies and one byte permute) becomes two fp16x2 fragment
-// registers through a byte permute over the row's table {-d_w, 0, +d_w}.
+// registers by one byte permute each: in the first form the digit byte under
+// byte 0x64 (the fp16 value 1024 + digit), in the second a pair of bytes of
+// the row's table {-d_w, 0, +d_w}.
 // The activations are staged in shared memory as fp16 in the same per-chunk
 // slot order (chunks 5..7 of TQ1_0 permuted), so one 16-byte load gives a
 // thread both k16 halves of its B fragment.
@@ -60,6 +71,13 @@ constexpr int kMmaWarps = 16;
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kMmaMaxSplit = 8;
 constexpr size_t kMmaSmemBudget = 225 * 1024;
+// The rung of one n-tile uses the biased operand form (no per-row table, no
+// selector arithmetic: ~60 fewer integer operations per 16-row block; a seed
+// per chunk and token in shared memory, a block sum per row and token in
+// registers): 11.6 -> 9.9 us at t = 8, N=5120, K=6144.  At two to four
+// n-tiles those registers pass the 128 a thread has and it measured no
+// faster (two) or slower (four: 19.7 -> 24.4 us), so they keep the table form.
+__host__ __device__ constexpr bool mma_biased(int nt) { return nt == 1; }
 
 struct MmaArgs {
   const uint8_t* w;
@@ -115,6 +133,15 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ void digits_to_frag(uint32_t D, uint32_t t0, uint32_t t1, uint32_t& lo, uint32_t& hi) {
   lo = prmt(t0, t1, D * 0x22u + 0x10101010u);
   hi = prmt(t0, t1, __umulhi(D, 0x220000u) + 0x1010u);
+}
+
+// The biased form: the fp16 value 1024 + d has the bits 0x6400 + d, so the
+// digit byte under byte 0x64 is that value.  lo = (1024 + d0, 1024 + d1),
+// hi = (1024 + d2, 1024 + d3): selector nibbles 0..3 pick digit bytes, 4..7
+// bytes of 0x64646464.
+__device__ __forceinline__ void digits_to_frag_biased(uint32_t D, uint32_t& lo, uint32_t& hi) {
+  lo = prmt(D, 0x64646464u, 0x5140u);
+  hi = prmt(D, 0x64646464u, 0x7362u);
 }
 
 // acc[0..1] += s[0..1] * d[0..1] as one paired fp32 FMA (two fp32 lanes, each
@@ -228,9 +255,10 @@ template <int NT, int FMT, bool PART, bool RES>
 __global__ void __launch_bounds__(kMmaThreads, 1) mmv_mma_kernel(const MmaArgs a) {
   constexpr int kBB = fmt_block_bytes<FMT>();
   constexpr int TP = 8 * NT;  // token slots
+  constexpr bool kBiased = mma_biased(NT);  // 1024 + digit operands, seeded accumulators
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* act = smem;                                            // [TP][act_row] fp16 slots
-  float* da = reinterpret_cast<float*>(smem + a.off_da);          // [bc * 8][TP]
+  float* da = reinterpret_cast<float*>(smem + a.off_da);          // [bc * 8][TP] scales, or [bc * 8][TP / 2][4] scales and seeds
   uint8_t* slab = smem + a.off_slab;                              // [mt * 16][slab_row]
   float* P = reinterpret_cast<float*>(smem + a.off_p);            // [mt * 16][TP] CTA partial tile
   float* slot = reinterpret_cast<float*>(smem + a.off_slot);      // [warps][MP * 16][TP] continued runs
@@ -325,7 +353,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mmv_mma_kernel(const MmaArgs a
         const int c = c0 + 32 * h;
         if (c >= bc * 8) break;
         const int j = c & 7;
-        da[c * TP + tok] = __half2float(__ushort_as_half(static_cast<unsigned short>(wq[h][0] & 0xFFFFu)));
+        // Per chunk and token pair: d_a of tokens 2p, 2p + 1, and in the
+        // biased form their seeds -1025 * sum(q) (exact: |sum(q)| <= 4064).
+        float* dsl = kBiased ? da + (c * (TP / 2) + (tok >> 1)) * 4 + (tok & 1) : da + c * TP + tok;
+        dsl[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(wq[h][0] & 0xFFFFu)));
+        if constexpr (kBiased) {
+          int sq = 0;
+#pragma unroll
+          for (int e = 1; e < 9; ++e) sq = __dp4a(static_cast<int>(wq[h][e]), 0x01010101, sq);
+          dsl[2] = -1025.0f * static_cast<float>(sq);
+        }
         uint8_t* dst = dst_tok + static_cast<uint32_t>(c) * 64;
         const bool perm = FMT != kFmtTq2 && j >= 5;
 #pragma unroll
@@ -422,7 +459,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mmv_mma_kernel(const MmaArgs a
     }
     // This thread's rows and their block bytes: table (zero: no row) and the
     // packed words of each of its 2 * MP rows.
-    uint32_t tt[MP][2][2];
+    uint32_t tt[MP][2][2];  // second form: the rows' tables
+    float dw[MP][2];        // first form: the rows' block scales (0 past the matrix)
     uint32_t wd[MP][2][4];
 #pragma unroll
     for (int i = 0; i < MP; ++i) {
@@ -449,8 +487,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mmv_mma_kernel(const MmaArgs a
           wd[i][h][3] = __funnelshift_r(pp[12], pp[13], sh);
           dh = (pp[13] >> sh) & 0xFFFFu;
         }
-        tt[i][h][0] = tt[i][h][1] = 0;
-        if (r < rows) scale_table(PART ? 0x3C00u : dh, tt[i][h][0], tt[i][h][1]);  // PART: the unscaled trits
+        if constexpr (kBiased) {
+          dw[i][h] = r < rows ? __half2float(__ushort_as_half(static_cast<unsigned short>(dh))) : 0.0f;
+        } else {
+          tt[i][h][0] = tt[i][h][1] = 0;
+          if (r < rows) scale_table(PART ? 0x3C00u : dh, tt[i][h][0], tt[i][h][1]);  // PART: the unscaled trits
+        }
       }
     }
 
@@ -459,27 +501,52 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mmv_mma_kernel(const MmaArgs a
     // g and g+8, k16 halves 0 and 1), two MMAs, and the epilogue (or the
     // partials store).
     const uint8_t* abase = act + static_cast<uint32_t>(b * 256) * 2 + 16 * q + static_cast<uint32_t>(g) * a.act_row;
-    const float* dab = da + b * 8 * TP + 2 * q;  // chunk scales of this block, tokens 2q, 2q+1
+    // chunk scales (and seeds) of this block, tokens 2q, 2q+1
+    const float* dab = kBiased ? da + (b * 8 * (TP / 2) + q) * 4 : da + b * 8 * TP + 2 * q;
+    float au[MP][NT][4];  // biased form: this block's sum of d_a[j] * I_j per row and token
+#pragma unroll
+    for (int i = 0; i < MP; ++i)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) au[i][nt][0] = au[i][nt][1] = au[i][nt][2] = au[i][nt][3] = 0.f;
     auto chunk = [&](int j, const uint32_t (&dA0)[MP], const uint32_t (&dB0)[MP], const uint32_t (&dA1)[MP],
                      const uint32_t (&dB1)[MP]) {
       uint32_t f0[MP][4], f1[MP][4];
 #pragma unroll
       for (int i = 0; i < MP; ++i) {
-        digits_to_frag(dA0[i], tt[i][0][0], tt[i][0][1], f0[i][0], f0[i][2]);
-        digits_to_frag(dB0[i], tt[i][1][0], tt[i][1][1], f0[i][1], f0[i][3]);
-        digits_to_frag(dA1[i], tt[i][0][0], tt[i][0][1], f1[i][0], f1[i][2]);
-        digits_to_frag(dB1[i], tt[i][1][0], tt[i][1][1], f1[i][1], f1[i][3]);
+        if constexpr (kBiased) {
+          digits_to_frag_biased(dA0[i], f0[i][0], f0[i][2]);
+          digits_to_frag_biased(dB0[i], f0[i][1], f0[i][3]);
+          digits_to_frag_biased(dA1[i], f1[i][0], f1[i][2]);
+          digits_to_frag_biased(dB1[i], f1[i][1], f1[i][3]);
+        } else {
+          digits_to_frag(dA0[i], tt[i][0][0], tt[i][0][1], f0[i][0], f0[i][2]);
+          digits_to_frag(dB0[i], tt[i][1][0], tt[i][1][1], f0[i][1], f0[i][3]);
+          digits_to_frag(dA1[i], tt[i][0][0], tt[i][0][1], f1[i][0], f1[i][2]);
+          digits_to_frag(dB1[i], tt[i][1][0], tt[i][1][1], f1[i][1], f1[i][3]);
+        }
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const uint4 bf = *reinterpret_cast<const uint4*>(abase + static_cast<uint32_t>(nt * 8) * a.act_row + j * 64);
         const int tok = nt * 8 + 2 * q;
-        float2 sc = make_float2(0.f, 0.f);
-        if constexpr (!PART) sc = *reinterpret_cast<const float2*>(dab + j * TP + nt * 8);
+        // d_a of tokens 2q, 2q+1 and, in the biased form, their seeds
+        float2 sc = make_float2(0.f, 0.f), sd = make_float2(0.f, 0.f);
+        if constexpr (kBiased) {
+          const float4 s4 = *reinterpret_cast<const float4*>(dab + (j * (TP / 2) + nt * 4) * 4);
+          sc = make_float2(s4.x, s4.y);
+          sd = make_float2(s4.z, s4.w);
+        } else if constexpr (!PART) {
+          sc = *reinterpret_cast<const float2*>(dab + j * TP + nt * 8);
+        }
 #pragma unroll
         for (int i = 0; i < MP; ++i) {
           float d[4];
-          mma_f16(d, f0[i], bf.x, bf.y, zero4);
+          if constexpr (kBiased) {
+            const float seed[4] = {sd.x, sd.y, sd.x, sd.y};
+            mma_f16(d, f0[i], bf.x, bf.y, seed);
+          } else {
+            mma_f16(d, f0[i], bf.x, bf.y, zero4);
+          }
           mma_f16(d, f1[i], bf.z, bf.w, d);
           if constexpr (PART) {
             const int ra = (mg * MP + i) * 16 + g, rb = ra + 8;
@@ -495,6 +562,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mmv_mma_kernel(const MmaArgs a
               if (rb < rows)
                 a.part[(static_cast<int64_t>(tok + 1) * a.n + row0 + rb) * kc + cidx] = __float2int_rn(d[3]);
             }
+          } else if constexpr (kBiased) {
+            ffma2(au[i][nt][0], au[i][nt][1], sc.x, sc.y, d[0], d[1]);
+            ffma2(au[i][nt][2], au[i][nt][3], sc.x, sc.y, d[2], d[3]);
           } else {
             ffma2(acc[i][nt][0], acc[i][nt][1], sc.x, sc.y, d[0], d[1]);
             ffma2(acc[i][nt][2], acc[i][nt][3], sc.x, sc.y, d[2], d[3]);
@@ -588,6 +658,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mmv_mma_kernel(const MmaArgs a
         }
         chunk(7, xa0, xb0, xa1, xb1);
       }
+    }
+    if constexpr (kBiased && !PART) {
+#pragma unroll
+      for (int i = 0; i < MP; ++i)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          ffma2(acc[i][nt][0], acc[i][nt][1], dw[i][0], dw[i][0], au[i][nt][0], au[i][nt][1]);
+          ffma2(acc[i][nt][2], acc[i][nt][3], dw[i][1], dw[i][1], au[i][nt][2], au[i][nt][3]);
+        }
     }
   }
   if (cur_m >= 0 && ok) flush(cur_m);
@@ -698,7 +777,7 @@ MmaLayout mma_layout(int nt, int fmt, int nb, int split, int mt_max, bool alias 
   L.recv_alias = alias && split > 1;
   size_t off = static_cast<size_t>(tp) * L.act_row;
   L.off_da = static_cast<uint32_t>(off);
-  off += static_cast<size_t>(bc_max) * 8 * tp * 4;
+  off += static_cast<size_t>(bc_max) * 8 * tp * (mma_biased(nt) ? 8 : 4);  // d_a (and the seeds)
   if (L.recv_alias) off = std::max(off, recv_bytes);
   off = (off + 127) & ~size_t(127);
   L.off_slab = static_cast<uint32_t>(off);

@@ -20,7 +20,7 @@ def _dequant(blocks, n, k, f16):
 
 
 @pytest.mark.parametrize("f16", [False, True])
-@pytest.mark.parametrize("n,k", [(1, 256), (7, 512), (300, 2048), (33, 1280), (129, 6144)])
+@pytest.mark.parametrize("n,k", [(1, 256), (7, 512), (300, 2048), (33, 1280), (129, 6144), (61, 2816)])
 def test_dequantize_rows_exact(n, k, f16):
     p = synth.matvec(n, k, 1, p_zero=0.4, seed=n + k)
     blocks = G.quantize_rows(p.w)
@@ -67,6 +67,26 @@ def _tq2_blocks(w):
     return b
 
 
+
+def test_get_rows_many_ids_ragged_segments():
+    # 16000 gathered rows of 11 blocks each: every warp takes several row
+    # segments (8 blocks and a ragged 3) in turn, rows start at every even
+    # offset modulo 16, and some ids are out of range.
+    n, k = 300, 2816
+    p = synth.matvec(n, k, 1, p_zero=0.3, seed=31)
+    blocks = G.quantize_rows(p.w)
+    rng = np.random.default_rng(32)
+    ids = rng.integers(-2, n + 2, size=16000).astype(np.int32)
+    t = G.torch()
+    out = t.full((ids.size, k), 7.0, dtype=t.float16, device="cuda")
+    G.lib().tq1_get_rows(blocks, G.dev(ids), ids.size, out, n, k, 1)
+    assert G.lib().tq1_sync_status() == -8
+    got = G.host(out)
+    ref = orc.tq1_dequantize_rows(orc.tq1_encode_rows(p.w), n, k).astype(np.float16)
+    ok = (ids >= 0) & (ids < n)
+    np.testing.assert_array_equal(got[ok], ref[ids[ok]])
+    assert np.all(got[~ok] == 7.0)
+
 def _tq2_dequant(blocks, n, k, f16):
     t = G.torch()
     out = t.full((n, k), float("nan"), dtype=t.float16 if f16 else t.float32, device="cuda")
@@ -76,7 +96,7 @@ def _tq2_dequant(blocks, n, k, f16):
 
 
 @pytest.mark.parametrize("f16", [False, True])
-@pytest.mark.parametrize("n,k", [(1, 256), (7, 512), (300, 2048), (33, 1280), (129, 6144)])
+@pytest.mark.parametrize("n,k", [(1, 256), (7, 512), (300, 2048), (33, 1280), (129, 6144), (61, 2816)])
 def test_tq2_dequantize_rows_exact(n, k, f16):
     p = synth.matvec(n, k, 1, p_zero=0.4, seed=n + 2 * k)
     got = _tq2_dequant(_tq2_blocks(p.w), n, k, f16)
