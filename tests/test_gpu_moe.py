@@ -128,6 +128,35 @@ def test_many_tokens_one_expert_beyond_32_columns():
     G.assert_close(G.host(y), ref)
 
 
+@pytest.mark.parametrize("fmt", ["tq1", "tq2"])
+def test_grouped_tasks_ragged_rows_blocks_and_pairs(fmt):
+    # 72 pairs on 9 experts, 200 rows (three 64-row tasks and a ragged 8),
+    # 6 blocks (the four parts of an M-tile take 2, 2, 1, 1), one expert with
+    # 21 pairs (n-tiles of 8, 8 and 5): outputs and exact partials.
+    m = synth.moe(9, 200, 1536, 24, 3, seed=88)
+    ids = m.ids.copy()
+    ids[:19, 0] = 4
+    ids[:19, 1:] = np.where(ids[:19, 1:] == 4, 5, ids[:19, 1:])
+    ids[:19, 2] = np.where(ids[:19, 2] == ids[:19, 1], (ids[:19, 1] + 1) % 9, ids[:19, 2])
+    ids[:19, 2] = np.where(ids[:19, 2] == 4, 6, ids[:19, 2])
+    m.ids = ids.astype(np.int32)
+    q8 = G.quantize_acts(m.x)
+    oq = orc.q8_1_quantize(m.x)
+    if fmt == "tq1":
+        blocks = _experts_gpu(m)
+        y, st = _mmv_id(blocks, m, m.ids, q8)
+        assert st == 0
+        ref = orc.mmv_id_f64(_oracle_blocks(m, range(9)), 9, oq, m.ids, m.n, m.k, m.t, m.top_k)
+        G.assert_close(G.host(y), ref)
+    else:
+        blocks = _experts_gpu_tq2(m)
+        y = _tq2_id(blocks, m, m.ids, q8)
+        ref = orc.tq2_mmv_id_f64(_oracle_blocks_tq2(m, range(9)), 9, oq, m.ids, m.n, m.k, m.t, m.top_k)
+        G.assert_close(y, ref)
+    part = _mmv_id_partials(blocks, m, m.ids, q8, fmt)
+    np.testing.assert_array_equal(part, _oracle_id_partials(m, m.ids, np.arange(m.n), fmt))
+
+
 def test_equals_per_expert_mmv():
     m = synth.moe(6, 256, 2048, 4, 3, seed=12)
     blocks = _experts_gpu(m)
