@@ -764,7 +764,8 @@ def run_profile_case(args, local):
     """A fixed, small, eager workload for Nsight Compute captures: set-up, then
     `--profile-calls` mat-vec calls over distinct weight copies (larger than L2
     in total), no timing.  Cases: c2 (T=1), c3t<T> (config 3 at T columns),
-    c4t<T> (MoE), c5 (prefill)."""
+    c4t<T> (MoE), c5 (prefill), tq2c2 / tq2c2t<T> (TQ2_0), dq16 / dq32
+    (dequantise config 2's matrix to fp16 / fp32)."""
     import torch
 
     import __graft_entry__
@@ -820,6 +821,23 @@ def run_profile_case(args, local):
         for i in range(args.profile_calls):
             l = i % copies
             assert lib.tq2_mmv(blocks.data_ptr() + l * wbytes, q8.data_ptr(), y.data_ptr(), n, k, t, s) == 0
+    elif case in ("dq16", "dq32"):
+        # Dequantise config 2's matrix to fp16 (dq16) or fp32 (dq32) rows,
+        # over distinct weight copies and two output buffers.
+        c = synth.CONFIGS["c2"]
+        n, k = c["n"], c["k"]
+        wbytes = n * (k // QK) * BLOCK_BYTES
+        copies = max(1, min(args.layers or 40, (2 * 2 ** 30) // wbytes))
+        blocks = torch.empty(copies * wbytes, dtype=torch.uint8, device=dev)
+        for l in range(copies):
+            w = synth.device_weights(n, k, c["p_zero"], c["d_lo"], c["d_hi"], gen, dev)
+            L.tq1_quantize_rows(w, blocks[l * wbytes:(l + 1) * wbytes], n, k)
+            del w
+        f16 = case == "dq16"
+        y = torch.empty((2, n, k), dtype=torch.float16 if f16 else torch.float32, device=dev)
+        for i in range(args.profile_calls):
+            l = i % copies
+            assert lib.tq1_dequantize_rows(blocks.data_ptr() + l * wbytes, y[i % 2].data_ptr(), n, k, int(f16), s) == 0
     elif case.startswith("c4"):
         t = int(case[3:].lstrip("t")) if len(case) > 3 else 1
         m = synth.config_moe(t)
@@ -863,7 +881,7 @@ def main(argv=None):
                     help="dram bytes per mat-vec launch from an ncu capture of the current kernel")
     ap.add_argument("--profile", default=None,
                     help="run a fixed eager workload for ncu instead of timing "
-                         "(c2, c3t<T>, c4t<T>, c5, tq2c2, tq2c2t<T>)")
+                         "(c2, c3t<T>, c4t<T>, c5, tq2c2, tq2c2t<T>, dq16, dq32)")
     ap.add_argument("--profile-calls", type=int, default=12)
     args = ap.parse_args(argv)
     if args.profile:

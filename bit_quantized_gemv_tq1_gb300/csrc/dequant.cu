@@ -37,7 +37,10 @@ constexpr int kDqThreads = 256;
 constexpr int kDqWarps = kDqThreads / 32;
 constexpr int kDqSeg = 8;       // 256-blocks per segment
 constexpr int kDqDepth = 3;     // segments whose copies are in flight per warp
-constexpr int kDqCtasPerSm = 4; // resident CTAs per SM the grid is sized for
+// Resident CTAs per SM the grid is sized for: fp32 rows 5, fp16 rows 4
+// (measured at N=5120, K=6144: fp32 22.8 -> 21.9 us with 5, fp16 11.3 ->
+// 11.7 us).
+constexpr int dq_ctas_per_sm(bool f16) { return f16 ? 4 : 5; }
 // A slot holds the 16-byte pieces covering one segment (a segment starts at
 // an even byte offset, so at most 14 bytes before it share its first piece).
 template <int FMT>
@@ -241,7 +244,7 @@ int launch_dequant(const uint8_t* blocks, const int32_t* row_ids, int64_t n_out,
   const int nb = static_cast<int>(k / kQK);
   const int64_t units = n_out * nb;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + kDqWarps * kDqSeg - 1) / (kDqWarps * kDqSeg),
-                                                               static_cast<int64_t>(di.num_sms) * kDqCtasPerSm));
+                                                               static_cast<int64_t>(di.num_sms) * dq_ctas_per_sm(f16)));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kDqThreads);
