@@ -20,15 +20,16 @@ constexpr int64_t kMaxK = 62720;  // activation records of one column must fit t
 // The mat-vec ladder (tq1_mmv and its variants), from the crossovers measured
 // on GB300 at N=5120, K=6144 (us per call in a chain of dependent calls):
 //   t <  kMmaMinT:   the dp4a decode kernel, rungs of 1/2/4/8 columns (its
-//                    cost grows ~1.1-1.5 us per column: 11.7 us at t = 7)
+//                    cost grows ~1.1-1.5 us per column: 9.4 us at t = 5,
+//                    10.5 at 6, 11.7 at 7)
 //   t >= kMmaMinT:   the warp-level tensor-core kernel, rungs of 8/16/24/32
-//                    columns (12.5 us at t = 8, 13.6 at 16, 19.2 at 32), in
-//                    slices of 32 columns above 32
+//                    columns (~9.9 us for any t <= 8, 13.2 at 9-16, 19.6 at
+//                    32), in slices of 32 columns above 32
 //   t >= kTileMinT with a caller workspace (tq1_mmv_ws): the tcgen05 tile
 //                    path (prefill)
 // Shapes a kernel cannot stage fall through to the general dp4a kernel.
 #ifndef TQ1_MMA_MIN_T
-#define TQ1_MMA_MIN_T 8
+#define TQ1_MMA_MIN_T 6
 #endif
 #ifndef TQ1_TILE_MIN_T
 #define TQ1_TILE_MIN_T 33

@@ -123,10 +123,11 @@ int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* str
  * w = d_w * trit and x = d_a * q, accumulated as
  *   sum_blocks d_w * sum_{chunks j} d_a[j] * I_j,   I_j = sum (trit * q) (exact int32)
  * in fp32.  blocks [n][k/256] TQ1_0, q8 [t][k/32] Q8_1, y fp32 [t][n].
- * The ladder: t <= 7 runs the byte-major dp4a decode kernel (rungs of
- * 1/2/4/8 columns); t >= 8 runs the warp-level tensor-core kernel (mma.sync
- * on exact fp16 operands: d_w*trit and the int8 q, fp32 accumulation of each
- * 32-element chunk, which is exact) with rungs of 8/16/24/32 token columns,
+ * The ladder: t <= 5 runs the byte-major dp4a decode kernel (rungs of
+ * 1/2/4/8 columns); t >= 6 runs the warp-level tensor-core kernel (mma.sync
+ * on exact fp16 operands, trit-derived and the int8 q, with an fp32
+ * accumulation of each 32-element chunk that is exact) with rungs of
+ * 8/16/24/32 token columns,
  * in slices of 32 columns above 32; shapes either cannot stage take a
  * general dp4a kernel.  Nothing
  * is allocated; for prefill-sized t, tq1_mmv_ws with a workspace runs the
@@ -200,9 +201,9 @@ int tq1_mmv_add(const void* blocks, const void* q8, const float* res, float* y, 
 /*
  * Debug entry: the exact integer partials part[c][r][j] = I_j (int32,
  * [t][n][k/32]) that tq1_mmv scales, for any t, from the kernel tq1_mmv runs
- * for that t: the dp4a decode kernel at t <= 7 (its dp4a sums, stored before
- * scaling), the tensor-core rungs at t >= 8 (each chunk's accumulator with
- * the unscaled trit table, which is exactly I_j); shapes neither can stage
+ * for that t: the dp4a decode kernel at t <= 5 (its dp4a sums, stored before
+ * scaling), the tensor-core rungs at t >= 6 (each chunk's accumulator, which
+ * holds exactly I_j when the operands are unscaled); shapes neither can stage
  * take the general kernel.  Bit-exact by construction.
  * Source: PrismML-Eng/llama.cpp issue #139, "Acceptance criteria" (the new
  * kernel checked case by case against a CPU reference), and the per-32-block
@@ -333,9 +334,9 @@ int tq1_sync_status(void* stream);
  * tq2_mmv: y[c][r] = sum_k w[r][k] * x[c][k] for TQ2_0 blocks [n][k/256] and
  * Q8_1 q8 [t][k/32], accumulated exactly as tq1_mmv (exact int32 per-32
  * partials, fp32 scale-and-sum per block).  The same ladder as tq1_mmv:
- * t <= 7 runs the decode kernel (the codes already are its packed-digit
- * registers: masked dp4a, no expansion), t >= 8 the warp-level tensor-core
- * rungs (the codes select fp16 trit values by a byte permute), with the
+ * t <= 5 runs the decode kernel (the codes already are its packed-digit
+ * registers: masked dp4a, no expansion), t >= 6 the warp-level tensor-core
+ * rungs (the codes become fp16 operands by a byte permute), with the
  * tcgen05 tile path through tq2_mmv_ws.  Deterministic; allocates nothing.
  *
  * tq2_mmv_partials: the exact int32 partials part[c][r][k/32] of tq2_mmv

@@ -27,8 +27,10 @@ SMALL = [
     (1, 256, 1), (3, 256, 2), (7, 512, 3), (33, 1024, 1), (256, 1024, 1), (100, 2048, 4),
     (77, 6144, 5), (301, 768 * 4, 8), (64, 4096, 16), (130, 2048, 32), (45, 256 * 9, 31),
     (17, 6144, 2), (1000, 512, 1), (5, 256 * 63, 1),
-    # the 8-column decode rung: one row and block, long K (records beyond the
-    # two-CTA budget), ragged rows at 7 columns
+    # the 8-column decode rung (t = 5): one row and block, long K (records
+    # beyond the two-CTA budget), ragged rows
+    (1, 256, 5), (9, 256 * 63, 5), (130, 2304, 5),
+    # the one-n-tile tensor-core rung below and at 8 columns
     (1, 256, 8), (9, 256 * 63, 6), (130, 2304, 7),
 ]
 
@@ -147,10 +149,11 @@ def _one_hot_columns(k, cols):
 # of row e'_c is 127 at chunk e'_c / 32.  A transposed element order, a wrong
 # digit or a chunk mapped to the wrong activation word fails these.
 # (k, t, cols): k = 256 with t = 32 runs the general kernel (k not a multiple
-# of 2048); k = 2048 with t <= 8 the decode rungs; k = 2048 with t >= 9 the
-# tensor-core tile path.  cols: every element of the first and the last block.
+# of 2048); k = 2048 with t <= 5 the decode rungs, with t >= 6 the
+# tensor-core rungs.  cols: every element of the first and the last block.
 ONE_HOT = [(256, 32, range(256)), (2048, 1, list(range(0, 256, 5)) + list(range(1792, 2048, 7))),
            (2048, 2, list(range(256)) + list(range(1792, 2048))), (2048, 4, range(0, 256, 3)),
+           (2048, 5, list(range(256)) + list(range(1792, 2048))), (2048, 6, list(range(256)) + list(range(1792, 2048))),
            (2048, 8, list(range(256)) + list(range(1792, 2048))), (2048, 32, list(range(256)) + list(range(1792, 2048)))]
 
 
@@ -167,7 +170,7 @@ def test_one_hot_layout_probes(k, t, cols):
         expect = np.zeros((t, k), bool)
         expect[np.arange(t), cg] = True
         np.testing.assert_array_equal(y != 0, expect)
-        if t <= 8:
+        if t <= 8 or k % 2048 == 0:
             part = G.partials(blocks, q8, k, k, t)
             ref = np.zeros_like(part)
             ref[np.arange(t), cg, cg // 32] = 127
@@ -175,9 +178,10 @@ def test_one_hot_layout_probes(k, t, cols):
 
 
 def test_decode_kernel_partials_c3_whole_ctas():
-    """The decode kernel's own integer partials (every rung, pair mode
-    included) against the oracle's, bit for bit, on whole CTAs of config 3's
-    shape (N=5120, K=6144) at t = 1..8."""
+    """The integer partials of the kernels tq1_mmv runs (the decode kernel's
+    rungs, pair mode included, at t = 1..5; the one-n-tile tensor-core rung
+    at 6..8) against the oracle's, bit for bit, on whole decode-kernel CTAs
+    of config 3's shape (N=5120, K=6144)."""
     p = synth.config_matvec("c3")
     blocks = G.quantize_rows(p.w)
     rows = _cta_rows(p.n)
@@ -207,7 +211,7 @@ def test_decode_kernel_partials_several_rounds():
 def test_multi_column_equals_single_columns(t):
     # strata PR #1418 method: a multi-column call equals single-column calls.
     # Integer partials always bit-exact; fp32 outputs within the float
-    # tolerance (t = 1 runs the dp4a decode kernel, t >= 8 the tensor-core
+    # tolerance (t = 1 runs the dp4a decode kernel, t >= 6 the tensor-core
     # rungs, whose accumulation orders differ).
     p = synth.matvec(5120, 6144, t, seed=8)
     blocks, q8 = _run(p)

@@ -1,7 +1,7 @@
 """TQ2_0 (2-bit ternary codes) on the GPU vs the oracle: encoder bytes
 bit-exact, integer partials bit-exact, fp32 outputs within max(1e-3 |ref|,
 1e-4), over the decode kernel (t = 1 and the fused-quantisation entry), the
-tensor-core rungs (t >= 2), the tcgen05 tile path (tq2_mmv_ws with a
+tensor-core rungs (t >= 6), the tcgen05 tile path (tq2_mmv_ws with a
 workspace) and the full-size decode and prefill shapes (sampled rows)."""
 import numpy as np
 import pytest
@@ -138,8 +138,10 @@ def test_decode_rungs_several_rounds_sampled_rows():
 
 
 def test_decode_kernel_partials_whole_ctas():
-    """The decode kernel's own integer partials on TQ2_0 weights (every rung)
-    against the oracle's, bit for bit, on whole CTAs of N=5120, K=6144."""
+    """The integer partials on TQ2_0 weights of the kernels tq2_mmv runs (the
+    decode kernel's rungs at t = 1..5, the one-n-tile tensor-core rung at
+    6..8) against the oracle's, bit for bit, on whole decode-kernel CTAs of
+    N=5120, K=6144."""
     p = synth.matvec(5120, 6144, 8, seed=61)
     blocks = _quantize_tq2(p.w)
     ctas = 152
