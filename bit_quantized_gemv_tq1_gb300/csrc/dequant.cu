@@ -9,20 +9,21 @@
 // consecutive blocks (for get_rows, never across an output row): a segment's
 // bytes (the 16-byte pieces covering them) are copied global -> shared memory
 // by asynchronous copies, three segments in flight per warp, so the load
-// latency is paid once per three segments rather than once per block.  Lane l
-// then produces elements 8l .. 8l+7 of each block.  Those eight elements are
-// digit k of eight consecutive packed bytes (element order of the block:
-// e < 160 -> qs[e % 32] digit e/32; e < 240 -> qs[32 + (e-160) % 16] digit
-// (e-160)/16; else qh[(e-240) % 4] digit (e-240)/4), so each lane reads its
-// eight bytes once and expands them with the specification's digit formula
-// ((uint8)(b*3^k)*3) >> 8.  Stores are 16-byte vectors, a warp writing one
-// contiguous 1 KiB (fp32) or 512 B (fp16) span per block: the kernel is bound
-// by the output bytes written to HBM.
+// latency is paid once per three segments rather than once per block.  Each
+// lane then produces eight elements of each block as two groups of four:
+// elements 8l .. 8l+7 for fp16 rows (one 16-byte store), 4l .. 4l+3 and
+// 128+4l .. 128+4l+3 for fp32 rows (two 16-byte stores, each instruction of
+// the warp writing 512 contiguous bytes).  A group of four is digit k of four
+// consecutive packed bytes (element order of the block: e < 160 -> qs[e % 32]
+// digit e/32; e < 240 -> qs[32 + (e-160) % 16] digit (e-160)/16; else
+// qh[(e-240) % 4] digit (e-240)/4), expanded with the specification's digit
+// formula ((uint8)(b*3^k)*3) >> 8.  The kernel is bound by the output bytes
+// written to HBM.
 //
-// TQ2_0 blocks (2-bit codes, 66 bytes) take the same path: lane l's eight
-// elements lie in chunk c = l / 4, so they are field c % 4 of the eight
-// consecutive bytes qs[32 * (c / 4) + 8 * (l % 4) ..]; code 3 (never written
-// by the encoder) gives +2d, the fourth entry of the value table.
+// TQ2_0 blocks (2-bit codes, 66 bytes) take the same path: a group of four is
+// field (e/32) % 4 of four consecutive bytes qs[32 * (e/128) + e % 32 ..];
+// code 3 (never written by the encoder) gives +2d, the fourth entry of the
+// value table.
 #include <algorithm>
 
 #include "../../include/tq1.h"
