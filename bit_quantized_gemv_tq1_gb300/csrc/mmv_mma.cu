@@ -1,6 +1,6 @@
-// mmv_mma.cu -- TQ1_0 / TQ2_0 x Q8_1 mat-vec for 2 to 32 token columns on the
-// warp-level tensor cores (mma.sync m16n8k16, fp16 operands, fp32
-// accumulation): the 8/16/24/32-column rungs of the ladder.
+// mmv_mma.cu -- TQ1_0 / TQ2_0 x Q8_1 mat-vec for up to 32 token columns on
+// the warp-level tensor cores (mma.sync m16n8k16, fp16 operands, fp32
+// accumulation): the 8/16/24/32-column rungs of the ladder (from t = 6 on).
 //
 // Neroued/ninfer issue #293: one rung sized for the largest batch makes every
 // small batch pay its price; rungs per column count do not.  Here a rung is
@@ -19,11 +19,10 @@
 // accumulation is exact.  The epilogue sums d_a[j] * I_j over a block's chunks
 // and adds that sum times d_w to the row's total.  On the rungs of two to
 // four n-tiles (whose registers are fuller) A holds d_w * trit from a per-row
-// table: each product is an exact
-// multiple of d_w's last place and a chunk's sum (at most 4064 d_w) needs 23
-// bits, so the tensor core returns d_w * I_j from a zero accumulator and the
-// epilogue adds d_a[j] * (d_w * I_j).  Either way in fp32, chunk by chunk, in a
-// fixed order.  The partials mode (the debug entry points) takes I_j from the
+// table: each product is an exact multiple of d_w's last place and a chunk's
+// sum (at most 4064 d_w) needs 23 bits, so the tensor core returns d_w * I_j
+// from a zero accumulator and the epilogue adds d_a[j] * (d_w * I_j).  Either
+// way in fp32, chunk by chunk, in a fixed order.  The partials mode (the debug entry points) takes I_j from the
 // first form, or from the second with the unscaled table {-1, 0, +1}, and
 // stores it as int32.
 //
