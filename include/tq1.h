@@ -83,7 +83,7 @@ const char* tq1_version(void);
  * Test hook for the error path of the bounded transfer waits.  The next
  * tq1_mmv / tq1_mmv_add / tq2_mmv / tq2_mmv_add call consumes the hook,
  * whichever kernel it runs; when that call runs the decode kernel
- * (1 <= t <= 8), its first CTA issues no copy (and no byte count) for its
+ * (1 <= t <= 5), its first CTA issues no copy (and no byte count) for its
  * first 4-row group, so every wait on that group gives up after about 2 s:
  * the call then reports TQ1_ERR_TIMEOUT through tq1_sync_status, its outputs
  * are unspecified, and the device and the library stay usable.  Nothing
