@@ -37,8 +37,12 @@ constexpr int64_t kMaxK = 62720;  // activation records of one column must fit t
 constexpr int64_t kMmaMinT = TQ1_MMA_MIN_T;
 constexpr int64_t kTileMinT = TQ1_TILE_MIN_T;
 // Routed pairs up to which tq1_mmv_id skips the routing table (each pair's
-// rows are then read once per pair, not once per distinct expert).
-constexpr int64_t kMoeDirectMaxPairs = 32;
+// rows are then read once per pair, not once per distinct expert; pairs of
+// one expert read them at about the same time, mostly from L2).  Measured on
+// 128 experts of 768 x 2048, Zipf top-8, direct against compacted mode (us,
+// single graph replays): 40 pairs 8.9 / 13.1, 64 pairs 14.9 / 16.4, 128
+// pairs 24.7 / 25.2, 256 pairs 44.6 / 36.8, 512 pairs 81.9 / 57.4.
+constexpr int64_t kMoeDirectMaxPairs = 128;
 std::mutex g_mu;
 std::atomic<int> g_inject_timeout{0};  // one-shot test hook (tq1_debug_inject_wait_timeout)
 DeviceInfo g_info[kMaxDevices];

@@ -284,7 +284,7 @@ int tq1_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q
  * Debug entry: the exact integer partials part[c][s][r][j] = I_j (int32,
  * [t][top_k][n][k/32]) that tq1_mmv_id / tq2_mmv_id scale, from the routed
  * decode kernels themselves (their expansion and dp4a sums, stored before
- * scaling): direct mode for up to 32 routed pairs, the compacted mode above.
+ * scaling): direct mode for up to 128 routed pairs, the compacted mode above.
  * Arguments, workspace and errors as tq1_mmv_id (part replaces y); shapes
  * that only the general kernel can stage return TQ1_ERR_UNSUPPORTED.
  * Source: AMD-Ecosystem/llama.cpp PR #76, "Summary" (the expert-routed grid

@@ -130,10 +130,10 @@ def test_many_tokens_one_expert_beyond_32_columns():
 
 @pytest.mark.parametrize("fmt", ["tq1", "tq2"])
 def test_grouped_tasks_ragged_rows_blocks_and_pairs(fmt):
-    # 72 pairs on 9 experts, 200 rows (three 64-row tasks and a ragged 8),
-    # 6 blocks (the four parts of an M-tile take 2, 2, 1, 1), one expert with
-    # 21 pairs (n-tiles of 8, 8 and 5): outputs and exact partials.
-    m = synth.moe(9, 200, 1536, 24, 3, seed=88)
+    # 144 pairs (the compacted mode) on 9 experts, 200 rows (ragged last
+    # task), 6 blocks, one expert with at least 19 pairs (several 4-pair
+    # chunks and a ragged one): outputs and exact partials.
+    m = synth.moe(9, 200, 1536, 48, 3, seed=88)
     ids = m.ids.copy()
     ids[:19, 0] = 4
     ids[:19, 1:] = np.where(ids[:19, 1:] == 4, 5, ids[:19, 1:])
@@ -198,7 +198,7 @@ def test_deterministic_repeat():
     np.testing.assert_array_equal(G.host(a), G.host(b))
 
 
-@pytest.mark.parametrize("t,top_k,n_experts", [(1, 8, 16), (3, 4, 6), (40, 2, 5)])
+@pytest.mark.parametrize("t,top_k,n_experts", [(1, 8, 16), (3, 4, 6), (40, 2, 5), (70, 2, 5)])
 def test_per_slot_activations(t, top_k, n_experts):
     # One activation row per (token, slot): direct mode (few pairs) and the
     # compacted path (80 pairs).
@@ -299,9 +299,9 @@ def test_tq2_per_slot_activations(t, top_k, n_experts):
 def test_large_expert_count_runs_the_compaction_kernel():
     # 1100 experts: the routing table (four words per expert plus one per
     # pair) is larger than the routed kernel builds in shared memory, so the
-    # compaction kernel writes it into the workspace first; 40 pairs take the
+    # compaction kernel writes it into the workspace first; 160 pairs take the
     # compacted mode.  Outputs and exact partials against the oracle.
-    m = synth.moe(1100, 64, 512, 20, 2, seed=77)
+    m = synth.moe(1100, 64, 512, 80, 2, seed=77)
     t_ = G.torch()
     eb = m.n * (m.k // 256) * 54
     used = np.unique(m.ids)
