@@ -40,10 +40,11 @@ constexpr int kMThreads = 256;
 constexpr int kMWarps = kMThreads / 32;
 constexpr int kChunk = 4;        // pairs per task
 constexpr int kMaxRows = 96;     // rows per task: task granularity (128-row tasks left some CTAs a whole extra task)
-// Routings of up to this many pairs take tasks of at most 64 rows: with few
-// pairs there are fewer tasks than the CTAs can hold, and the longest task
-// sets the time (config 4 at T = 8, 64 pairs: 19.1 -> 16.4 us; at T = 64,
-// 512 pairs, 64-row tasks took 59.7 against 57.4 us).
+// Routings of up to this many pairs (those direct mode cannot stage) take
+// tasks of at most 64 rows: with few pairs there are fewer tasks than the
+// CTAs can hold, and the longest task sets the time (config 4 at T = 8, 64
+// pairs: 19.1 -> 16.4 us; at T = 64, 512 pairs, 64-row tasks took 59.7
+// against 57.4 us).
 constexpr int64_t kFinePairs = 128;
 constexpr int kFineRows = 64;
 constexpr int kMaxGroupsM = kMaxRows / kRowsPerTask;
