@@ -76,7 +76,7 @@ enum tq1_status {
  * library (the pages define no API). */
 const char* tq1_status_string(int status);
 
-/* Library version, e.g. "0.1.0". */
+/* Library version, e.g. "0.1.0".  No passage: a convention of this library. */
 const char* tq1_version(void);
 
 /*
@@ -92,11 +92,13 @@ const char* tq1_version(void);
 void tq1_debug_inject_wait_timeout(void);
 
 /* Name and text of the last CUDA runtime error this thread saw inside the
- * library (empty if none); explains a TQ1_ERR_CUDA. */
+ * library (empty if none); explains a TQ1_ERR_CUDA.  No passage: a
+ * convention of this library. */
 const char* tq1_last_cuda_error(void);
 
 /* Bytes of a TQ1_0 matrix [n][k/256], a TQ2_0 matrix [n][k/256] and a Q8_1
- * matrix [t][k/32]. */
+ * matrix [t][k/32] (54, 66 and 36 bytes per block, as the formats at the top
+ * of this file lay them out).  No passage: a convention of this library. */
 size_t tq1_blocks_bytes(int64_t n, int64_t k);
 size_t tq2_blocks_bytes(int64_t n, int64_t k);
 size_t tq1_q8_1_bytes(int64_t t, int64_t k);
@@ -105,8 +107,9 @@ size_t tq1_q8_1_bytes(int64_t t, int64_t k);
  * Quantise fp32 weights w[n][k] (row-major) to TQ1_0 blocks.
  * Per 256-weight block: d = fp16(max |w|); trit = clamp(round_half_away(w / max|w|),
  * -1, 1), or 0 when the block is all zero.  Bit-exact, deterministic.
- * Format: PrismML-Eng/llama.cpp issue #139, "Current behavior"; rounding is
- * this library's reading (the pages do not state one).
+ * Source: PrismML-Eng/llama.cpp issue #139, "Current behavior" (the block
+ * format); the rounding is this library's reading (the pages do not state
+ * one).
  */
 int tq1_quantize_rows(const float* w, void* blocks, int64_t n, int64_t k, void* stream);
 
@@ -115,6 +118,10 @@ int tq1_quantize_rows(const float* w, void* blocks, int64_t n, int64_t k, void* 
  * Per 32-value block: d = max|x| / 127 (fp32); q = clamp(round_half_away(x / d),
  * -127, 127), or 0 when d == 0; stored fp16(d), fp16(d * sum q), q.
  * k must be a positive multiple of 32 here.  Bit-exact, deterministic.
+ * Source: PrismML-Eng/llama.cpp issue #139, "Current behavior" (the Q8_1
+ * activation blocks of 32 values whose per-block dot product the mat-vec
+ * computes); the rounding is this library's reading (the pages do not state
+ * one).
  */
 int q8_1_quantize_acts(const float* x, void* q8, int64_t t, int64_t k, void* stream);
 
@@ -311,7 +318,8 @@ int tq2_mmv_id_partials(const void* expert_blocks, int64_t n_experts, const void
  * device current; make that first call before any stream capture begins.
  * All calls on a device share the array (each call rewrites what it reads,
  * so nothing needs clearing); calls that may overlap on the GPU race on it.
- * The pages have no counterpart to this entry point.
+ * No passage: a convention of this library (the pages have no counterpart
+ * to this entry point).
  */
 int tq1_mmv_id_noalloc(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
                        int64_t n, int64_t k, int64_t t, int64_t top_k, void* stream);
@@ -357,6 +365,8 @@ int tq2_mmv_partials(const void* blocks, const void* q8, int32_t* part, int64_t 
  * kernel's prologue, 1 <= t <= 4, bit-identical to q8_1_quantize_acts +
  * tq2_mmv) and tq1_mmv_add (y = res + W x, res may be y).  Arguments and
  * errors as those.
+ * Source: as tq1_mmv_f32 and tq1_mmv_add, with PrismML-Eng/llama.cpp issue
+ * #139, "Upstream state" (the TQ2_0 sibling format).
  */
 int tq2_mmv_f32(const void* blocks, const float* x, float* y, int64_t n, int64_t k, int64_t t, void* stream);
 int tq2_mmv_add(const void* blocks, const void* q8, const float* res, float* y, int64_t n, int64_t k, int64_t t,
@@ -370,21 +380,24 @@ int tq2_mmv_add(const void* blocks, const void* q8, const float* res, float* y, 
  * Source: PrismML-Eng/llama.cpp issue #139, "Upstream state" (the TQ2_0
  * sibling format) and "Current behavior" (the dequantise walk of a block).
  */
+int tq2_dequantize_rows(const void* blocks, void* out, int64_t n, int64_t k, int out_f16, void* stream);
+int tq2_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n, int64_t k,
+                 int out_f16, void* stream);
+
 /*
  * Expert-routed mat-vec over TQ2_0 experts (each expert [n][k/256] x 66
  * bytes, back to back): the same routing, workspace
  * (tq1_mmv_id_workspace_size), kernels, layouts and errors as tq1_mmv_id
  * (one activation row per token) and tq1_mmv_id_slots (one per token and
  * slot).
+ * Source: AMD-Ecosystem/llama.cpp PR #76, "Summary" (ids -> expert_bounds ->
+ * compacted grid); PrismML-Eng/llama.cpp issue #139, "Upstream state" (the
+ * TQ2_0 sibling format).
  */
 int tq2_mmv_id(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
                int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
 int tq2_mmv_id_slots(const void* expert_blocks, int64_t n_experts, const void* q8, const int32_t* ids, float* y,
                      int64_t n, int64_t k, int64_t t, int64_t top_k, void* ws, size_t ws_bytes, void* stream);
-
-int tq2_dequantize_rows(const void* blocks, void* out, int64_t n, int64_t k, int out_f16, void* stream);
-int tq2_get_rows(const void* blocks, const int32_t* row_ids, int64_t n_ids, void* out, int64_t n, int64_t k,
-                 int out_f16, void* stream);
 
 #ifdef __cplusplus
 }

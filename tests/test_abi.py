@@ -36,6 +36,22 @@ def test_header_declares_the_entry_points():
         assert want in names
 
 
+def test_every_declaration_cites_a_passage():
+    # The comment block nearest above each declaration names the passage
+    # that defines the operation, or says that it is a convention of this
+    # library.
+    src = open(HEADER).read()
+    missing = []
+    for m in re.finditer(r"^(?:const\s+char\s*\*|int|size_t|void)\s+(\w+)\s*\(", src, flags=re.M):
+        before = src[:m.start()]
+        end = before.rfind("*/")
+        start = before.rfind("/*", 0, end)
+        block = before[start:end] if start >= 0 and end >= 0 else ""
+        if "Source:" not in block and "No passage" not in block:
+            missing.append(m.group(1))
+    assert not missing, missing
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
